@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of the top-k block-sparse GQA attention hot path on one B300.
+
+Default workload (decode GQA): batch 8, Hq 32, Hkv 8, d 128, context 32768,
+KV block 64 (512 blocks), top-k 32 + sink + local, bf16, 1% needle blocks.
+One step = the whole decode hot path over one batch: append the new token's
+K/V and refresh its block sketch (a1), score every block and select the top-k
+(a2 + a3), sparse split-KV attention over the selected blocks (a4).
+
+Prints ONE JSON line.  `value` = bytes the step must move (selected K/V blocks
++ sketch scan + append) / device time per step, with inputs resident in HBM;
+8 input sets (distinct K/V caches) are rotated so that no step finds its
+blocks in L2.  `e2e` = the same bytes / wall time per step through the C-ABI
+decode-step call with pinned host q/k_new/v_new/out, copies included.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload c2|c3]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- workloads
+
+def workload(name):
+    import synth
+    return synth.WORKLOADS[name]
+
+
+def decode_bytes(wl, cnt_np, L):
+    """Algorithmic bytes of one decode step (selected K/V + sketch scan + append)."""
+    es = wl.esize
+    kv = 0
+    for c in cnt_np.reshape(-1):
+        kv += int(c) * wl.Bk * wl.d * es * 2
+    groups = wl.B * wl.Hkv
+    sketch = groups * wl.nb * wl.d * 4
+    touched_rows = (L - 1) % wl.Bk + 1
+    append = groups * (wl.T * wl.d * es * 2 + touched_rows * wl.d * es + wl.d * 4)
+    return kv, sketch, append
+
+
+def oracle_decode_sample(wl, x, nbatch):
+    """One CPU-oracle decode step (sketch -> score -> select -> attend) on the first
+    `nbatch` batch entries.  Returns (seconds, algorithmic bytes)."""
+    import numpy as np
+
+    import oracle
+    sub = wl.replace(B=nbatch)
+    q, k, v = x.q[:nbatch], x.k[:nbatch], x.v[:nbatch]
+    t0 = time.perf_counter()
+    idx, cnt, _, _ = oracle.decode_select(q, k, sub)
+    rows = np.array([(b, t, h) for b in range(nbatch) for t in range(sub.T) for h in range(sub.Hq)])
+    oracle.attend(q, k, v, sub.Hkv, sub.L, sub.L - sub.T, sub.Bk, sub.scale, rows, idx, cnt)
+    dt = time.perf_counter() - t0
+    kv, sk, ap = decode_bytes(sub, cnt, sub.L)
+    return dt, kv + sk + ap
+
+
+def cpu_oracle_decode(wl, x, budget_s):
+    """Time the CPU oracle on a bounded sample (a prefix of the batch) for about budget_s seconds.
+    Returns (GB/s, cores, sample text)."""
+    import oracle
+    dt, _ = oracle_decode_sample(wl, x, 1)
+    nbatch = 1
+    while nbatch < wl.B and dt * 2 < budget_s / 3:
+        nbatch = min(wl.B, nbatch * 2)
+        dt, _ = oracle_decode_sample(wl, x, nbatch)
+    reps = max(1, int(budget_s // max(dt, 1e-3)))
+    total_t, total_b = 0.0, 0
+    for _ in range(reps):
+        t, b = oracle_decode_sample(wl, x, nbatch)
+        total_t += t
+        total_b += b
+    sample = "%d of %d batch entries (%d of %d groups), full context %d, %d rep(s)" % (
+        nbatch, wl.B, nbatch * wl.Hkv, wl.B * wl.Hkv, wl.L, reps)
+    return total_b / total_t / 1e9, oracle.threads(), sample
+
+
+# ------------------------------------------------------------------ our arm
+
+def bench_decode(args, wl, rank, world):
+    import numpy as np
+    import torch
+
+    import synth
+    import top_block_sparse_pooled_b300 as sa
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    x = synth.make_inputs(wl.replace(seed=wl.seed + 100 * rank))
+    R = args.rotate
+    bf = wl.dtype == "bf16"
+
+    def up(a):
+        import numpy as np
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+        return t.to(dev)
+
+    q0, k0, v0 = up(x.q), up(x.k), up(x.v)
+    pos = wl.L - wl.T
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
+    dtype_code = sa.SA_BF16 if bf else sa.SA_F32
+    ws_bytes = sa.sa_decode_step_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, dtype_code, kmax)
+    sets = []
+    for r in range(R):
+        kc, vc = k0.clone(), v0.clone()
+        sk = torch.empty((wl.B, wl.Hkv, wl.nb, wl.d), dtype=torch.float32, device=dev)
+        sa.sa_build_sketch(kc, wl.L, wl.Bk, sk)
+        sets.append(dict(
+            q=q0.clone(), kc=kc, vc=vc, sk=sk,
+            k_new=k0[:, :, pos:].permute(0, 2, 1, 3).contiguous(),
+            v_new=v0[:, :, pos:].permute(0, 2, 1, 3).contiguous(),
+            idx=torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device=dev),
+            cnt=torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device=dev),
+            out=torch.empty_like(q0),
+            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=dev)))
+    del k0, v0
+
+    def step(s):
+        sa.sa_decode_step(s["q"], s["k_new"], s["v_new"], s["kc"], s["vc"], s["sk"], wl.L, wl.Bk, wl.k, wl.scale,
+                          s["idx"], s["cnt"], s["out"], s["ws"])
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(sets[i % R])
+    torch.cuda.synchronize()
+    if sa.sa_device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+    cnt_np = sets[0]["cnt"].cpu().numpy()
+    kv_b, sk_b, ap_b = decode_bytes(wl, cnt_np, wl.L)
+    step_bytes = kv_b + sk_b + ap_b
+
+    # one CUDA graph per input set (the step is 4 kernels)
+    graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(sets[r])
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            graphs[i % R].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    K = args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(20_000_000)  # keep the device busy while the host queues the replays
+        ev0.record(stream)
+        for i in range(K):
+            graphs[i % R].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    t_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    ms_per_step = t_ms / K
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    # ---- dominant kernel pair (split-KV decode + merge) timed alone, CUDA events on its stream
+    nd = min(K, 3000)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nd)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)
+        for i in range(nd):
+            s = sets[i % R]
+            evs[i][0].record(stream)
+            sa.sa_decode(s["q"], s["kc"], s["vc"], s["idx"], s["cnt"], wl.L, wl.Bk, wl.scale, s["out"], s["ws"])
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs[10:] if True) if nd > 20 else \
+        statistics.mean(a.elapsed_time(b) for a, b in evs)
+    dec_gbs = kv_b / (dec_ms * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with pinned host buffers
+    hq = sets[0]["q"].cpu().pin_memory()
+    hkn = sets[0]["k_new"].cpu().pin_memory()
+    hvn = sets[0]["v_new"].cpu().pin_memory()
+    hout = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
+    ne = min(K, 2000)
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            s = sets[i % R]
+            sa.sa_decode_step(hq, hkn, hvn, s["kc"], s["vc"], s["sk"], wl.L, wl.Bk, wl.k, wl.scale, s["idx"],
+                              s["cnt"], hout, s["ws"], host_io=True)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for i in range(ne):
+            s = sets[i % R]
+            sa.sa_decode_step(hq, hkn, hvn, s["kc"], s["vc"], s["sk"], wl.L, wl.Bk, wl.k, wl.scale, s["idx"],
+                              s["cnt"], hout, s["ws"], host_io=True)
+            stream.synchronize()  # the next token needs this one's output
+        t_e2e = (time.perf_counter() - t0) / ne
+    es = wl.esize
+    h2d = hq.numel() * es + hkn.numel() * es * 2
+    d2h = hout.numel() * es
+
+    res = {
+        "metric": "sparse-attn decode KV GB/s (% HBM peak)",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic: seeded N(0,1) q/k/v, %d needle blocks per group (keys + %g * q_hat)" % (wl.needles,
+                                                                                                    wl.alpha),
+        "config": {
+            "workload": "%s decode: B=%d T=%d Hq=%d Hkv=%d d=%d L=%d block=%d top-k=%d + sink + local" % (
+                wl.name, wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, wl.L, wl.Bk, wl.k),
+            "step": "append+sketch refresh, score+top-k select, split-KV sparse decode (4 kernels, CUDA graph)",
+            "bytes_per_step": {"selected_kv": kv_b, "sketch_scan": sk_b, "append": ap_b},
+            "l2": "%d resident input sets rotated (%.1f GB of K/V); no step reuses L2 from the previous" % (
+                R, R * x.k.nbytes * 2 / 1e9),
+        },
+        "pct_hbm_peak": round(100 * value / peaks["hbm_gbs"], 2),
+        "roofline": {
+            "kernel": "sa_decode (decode_split_kernel + decode_combine_kernel)",
+            "bound": "hbm",
+            "achieved": round(dec_gbs, 2),
+            "peak": peaks["hbm_gbs"],
+            "peak_source": peak_src,
+            "unit": "GB/s",
+            "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
+            "traffic": None,
+            "avg_launch_us": round(dec_ms * 1e3, 3),
+            "algorithmic_bytes_per_launch": kv_b,
+        },
+        "e2e": {"value": round(step_bytes / t_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 4)},
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and args.cpu_baseline:
+        gbs, cores, sample = cpu_oracle_decode(wl, x, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                               "sample": sample}
+    traffic = os.path.join(ROOT, "profiles", "decode_c2_traffic.json")
+    if os.path.exists(traffic) and wl.name == "c2":
+        try:
+            with open(traffic) as f:
+                t = json.load(f)
+            if t.get("kernel_source_hash") == _kernel_hash():
+                res["roofline"]["traffic"] = t["dram_bytes_per_launch"]
+        except Exception:
+            pass
+    return res
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for fn in ("k_decode.cu", "sa_ptx.cuh"):
+        with open(os.path.join(ROOT, "top_block_sparse_pooled_b300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def bench_reference(args, wl, rank, world):
+    """The CPU oracle as it stands, on the same workload; each step is the oracle's decode
+    step on a bounded sample (a prefix of the batch) so that K steps take a few minutes."""
+    import oracle
+    import synth
+    if rank != 0:
+        return None
+    x = synth.make_inputs(wl)
+    budget = max(0.005, 150.0 / max(1, args.steps + args.warmup))
+    dt, _ = oracle_decode_sample(wl, x, 1)
+    nbatch = 1
+    while nbatch < wl.B and dt * 2 <= budget:
+        nbatch = min(wl.B, nbatch * 2)
+        dt, _ = oracle_decode_sample(wl, x, nbatch)
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_decode_sample(wl, x, nbatch)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        t, b = oracle_decode_sample(wl, x, nbatch)
+        tot_t += t
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    sample = "%d of %d batch entries (%d of %d groups) per step, full context %d" % (
+        nbatch, wl.B, nbatch * wl.Hkv, wl.B * wl.Hkv, wl.L)
+    return {
+        "impl": "reference",
+        "metric": "sparse-attn decode KV GB/s (% HBM peak)",
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same generator and seed as the CUDA arm)",
+        "config": {"workload": "%s decode: B=%d T=%d Hq=%d Hkv=%d d=%d L=%d block=%d top-k=%d + sink + local" % (
+            wl.name, wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, wl.L, wl.Bk, wl.k)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3"])
+    ap.add_argument("--rotate", type=int, default=8)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    wl = workload(args.workload)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        res = bench_reference(args, wl, rank, world)
+    else:
+        res = bench_decode(args, wl, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

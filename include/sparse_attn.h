@@ -1,0 +1,223 @@
+/*
+ * sparse_attn.h -- C ABI of libsparse_attn: top-k block-sparse GQA attention
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * The method (web summaries of the papers, by title and section):
+ *  - "Faster Than Flash: Exploiting Attention Sparsity for Efficient
+ *    Long-Context Decoding", Sec. 1 and 3: a small, compressed sketch of the KV
+ *    cache is scanned first to estimate which parts matter; only the selected
+ *    blocks are then loaded for the exact attention computation.  Sink
+ *    (initial) and local tokens dominate the attention distribution (Sec. 2).
+ *  - "How Much Dense Attention is Necessary? Oracle-Guided Sparse Prefill ...",
+ *    Sec. 2.1: an oracle ranks keys by their exact dense attention mass,
+ *    aggregated over the query heads; the top-k under a fixed budget form the
+ *    support, optionally shared by a block of consecutive queries; attention
+ *    is then recomputed with the original q, k, v on that support only.
+ *    Sec. 2.2: the same score -> top-k -> sparse-GQA shape at inference.
+ *  - "Pulsar Attention", Phase 1: a fixed attention-sink prefix is always kept;
+ *    Phase 2: partial softmaxes over disjoint key sets merge exactly (online
+ *    softmax), which is how split-KV partials are combined here.
+ *  - "The Sparse Frontier", Sec. 1 and RQ2: block-wise selection for prefill,
+ *    page selection with the full cache retained for decode.
+ *
+ * Notation: B batch, Hq query heads, Hkv kv heads, G = Hq / Hkv, query head h
+ * reads kv head h / G; d head dim; L context length (keys); Bk = `block` keys
+ * per KV block, nb = ceil(L / Bk); a "group" is one (batch, kv-head) pair,
+ * g = b * Hkv + kvh.  scale is the softmax scale (1/sqrt(d) is the usual one).
+ *
+ * Layouts (all row-major, contiguous, caller-owned DEVICE memory):
+ *   K, V cache / prefill K, V : [B, Hkv, L_stride, d]   (rows j < L valid)
+ *   decode q, out             : [B, T, Hq, d]           (query t sits at key
+ *                                                       position L - T + t)
+ *   prefill q, out            : [B, L, Hq, d]           (query t at position t)
+ *   k_new, v_new (append)     : [B, T, Hkv, d]
+ *   sketch                    : [B, Hkv, ceil(L_stride / Bk), d] float32 (blocks
+ *                               past ceil(L / Bk) unused)
+ *   scores / mass             : [B, Hkv, nq, nb] float32, nq = 1 for decode,
+ *                               ceil(L / qtile) for prefill
+ *   idx                       : [B, Hkv, nq, kmax] int32, ascending block ids,
+ *                               padded with -1;   cnt : [B, Hkv, nq] int32
+ *
+ * dtype: SA_F32 or SA_BF16 for q, k, v, k_new, v_new, out (all the same).
+ *
+ * Conventions.  Every call validates its arguments on the host before any
+ * launch and returns SA_ERR_INVALID_ARG / SA_ERR_UNSUPPORTED without touching
+ * the device when they are bad; sa_last_error() then gives a message.  Calls
+ * are asynchronous: they enqueue work on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream) and return.  The library allocates no device memory:
+ * scratch space is passed in as `workspace` (sizes from the *_workspace_bytes
+ * queries).  Kernels that wait on the tensor-memory-access (TMA) engine bound
+ * every wait; a wait that gives up records SA_ERR_TIMEOUT in a device-side
+ * status word that sa_device_status() reads.
+ */
+#ifndef SPARSE_ATTN_H
+#define SPARSE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1, /* bad pointer, shape, budget or buffer size */
+  SA_ERR_UNSUPPORTED = 2, /* valid but not implemented: dtype, d, block, device */
+  SA_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the name) */
+  SA_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up */
+} sa_status_t;
+
+typedef enum { SA_F32 = 0, SA_BF16 = 1 } sa_dtype_t;
+
+typedef enum {
+  SA_SELECT_SKETCH = 0, /* score blocks by max over the group's rows of scale*q.sketch */
+  SA_SELECT_MASS = 1    /* rank blocks by a given score array (e.g. sa_oracle_mass) */
+} sa_select_mode_t;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int sa_version(void);
+
+/* Message for the last failing call on this host thread ("" if none). */
+const char* sa_last_error(void);
+
+/* Name of a status code. */
+const char* sa_status_name(int status);
+
+/*
+ * Device-side status word.  Synchronizes the current device, then stores in
+ * *code the first error code a kernel recorded since the last clear (SA_OK if
+ * none) and, if clear != 0, resets it.  Returns SA_ERR_CUDA if the device
+ * synchronization itself fails.
+ */
+sa_status_t sa_device_status(int* code, int clear);
+
+/*
+ * a1. Block sketch ("Faster Than Flash" Sec. 1: a compressed summary scanned
+ * in place of the keys).  sketch[g, b, :] = mean of the valid key rows
+ * j in [b*Bk, min((b+1)*Bk, L)) of k[g], accumulated in float32.
+ * k: [B, Hkv, L_stride, d] (dtype); sketch: [B, Hkv, ceil(L_stride/Bk), d]
+ * float32, blocks b < nb written.
+ * Requires L >= 1, L <= L_stride, d in {64, 128}, block in [1, 1024].
+ */
+sa_status_t sa_build_sketch(const void* k, int dtype, int B, int Hkv, int L, int L_stride, int d,
+                            int block, float* sketch, void* stream);
+
+/*
+ * a1 fused with the cache append ("Sparse Attention as a Range Searching
+ * Problem" Sec. 2: new keys join the index incrementally, without a rebuild).
+ * Writes k_new[b, t, kvh, :] / v_new[...] to cache rows pos + t (t < T) of
+ * group (b, kvh), then rewrites the sketch of every block those rows touch as
+ * the mean of its valid rows j < pos + T.  Blocks wholly before pos are not
+ * read.  k_new, v_new: [B, T, Hkv, d]; caches [B, Hkv, L_stride, d];
+ * sketch [B, Hkv, ceil(L_stride/Bk), d] float32.  Requires pos + T <= L_stride.
+ */
+sa_status_t sa_append_kv(const void* k_new, const void* v_new, int dtype, int B, int Hkv, int T,
+                         int d, void* k_cache, void* v_cache, int L_stride, int pos, int block,
+                         float* sketch, void* stream);
+
+/*
+ * a2 + a3. Block scoring and top-k selection ("How Much Dense Attention is
+ * Necessary?" Sec. 2.1-2.2; sink/local kept: "Pulsar Attention" Phase 1,
+ * "Faster Than Flash" Sec. 2).
+ *
+ * prefill == 0 (decode): one selection per group for the T = Tq query tokens
+ *   at positions L-T..L-1.  Candidate blocks: 1..nb-2; forced: {0, nb-1}.
+ *   Budget: k.
+ * prefill != 0: one selection per (group, query tile i of `qtile` rows),
+ *   i.e. a support shared by the tile's queries (b_sel = qtile).  The causal
+ *   blocks of tile i are 0..c_i-1 with c_i = (last query position of the tile)
+ *   / Bk + 1; forced: {0, c_i - 1} (sink and diagonal); candidates: the rest.
+ *   Budget of tile i: k + ceil(frac_num * c_i / frac_den) (frac_num = 0: k).
+ * Ranking: the budget's worth of highest-scoring candidates, ties to the lower
+ *   block index; the output is the union with the forced blocks, ascending.
+ *
+ * mode SA_SELECT_SKETCH: score s = max over the group's query heads and the
+ *   unit's query rows of scale * (q . sketch[g, b]), in float32.  `sketch`
+ *   must be given.  If `scores` is not NULL the scores are written there
+ *   ([B, Hkv, nq, nb]; non-causal entries of prefill tiles are -inf).
+ * mode SA_SELECT_MASS: `scores` is an input (e.g. from sa_oracle_mass);
+ *   q and sketch are not read.
+ * idx: [B, Hkv, nq, kmax] int32 written (ascending, -1 padded), cnt:
+ *   [B, Hkv, nq] int32 written.  kmax must be >= sa_select_kmax(...).
+ * Requires d in {64, 128}; G * Tq <= 32 for decode; qtile == Bk == 128 and
+ * d == 128 for prefill in SKETCH mode.
+ */
+sa_status_t sa_select_topk(int mode, const void* q, int dtype, const float* sketch, float* scores,
+                           int B, int Tq, int Hq, int Hkv, int d, int L, int L_stride, int block,
+                           int qtile, int prefill, int k, int frac_num, int frac_den, float scale,
+                           int32_t* idx, int32_t* cnt, int kmax, void* stream);
+
+/* Smallest kmax that holds every selection of the given problem (or -1 if invalid). */
+int sa_select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num, int frac_den);
+
+/*
+ * a4, decode. Exact softmax attention over the selected blocks only ("How
+ * Much Dense Attention is Necessary?" Sec. 2.1), split over the selected
+ * blocks (flash-decoding) with an exact online-softmax merge of the partials
+ * ("Pulsar Attention" Phase 2).  For query row (b, t, h), g = b*Hkv + h/G:
+ *   out[b,t,h] = sum_j softmax_j(scale * q[b,t,h] . k[g,j]) v[g,j]
+ * over keys j in the blocks idx[g, 0:cnt[g]] with j < L and
+ * j <= L - T + t.  workspace: >= sa_decode_workspace_bytes(...) bytes of
+ * device memory, no initial contents needed, 16-byte aligned.
+ * Requires d in {64, 128}; block == 64; G*T <= 32; T <= block;
+ * 16-byte-aligned k/v caches.
+ */
+size_t sa_decode_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int kmax);
+sa_status_t sa_decode(const void* q, const void* k_cache, const void* v_cache, int dtype,
+                      const int32_t* idx, const int32_t* cnt, int kmax, int B, int T, int Hq,
+                      int Hkv, int d, int L, int L_stride, int block, float scale, void* out,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * a4, prefill. Causal exact attention per query tile over the tile's
+ * selected blocks ("How Much Dense Attention is Necessary?" Sec. 2.1,
+ * support shared by the tile; "The Sparse Frontier" RQ2, block-sparse
+ * prefill).  For query row (b, t, h) in tile i = t / qtile:
+ *   out[b,t,h] = sum_j softmax_j(scale * q[b,t,h] . k[g,j]) v[g,j],
+ * keys j in blocks idx[g, i, 0:cnt[g,i]] with j <= t.  lse_out (optional,
+ * [B, Hq, L] float32): natural-log sum of exp of the row's logits.
+ * Tensor cores (tcgen05, TMEM accumulators).  Requires dtype SA_BF16,
+ * d == 128, qtile == block == 128.
+ */
+sa_status_t sa_prefill(const void* q, const void* k, const void* v, int dtype, const int32_t* idx,
+                       const int32_t* cnt, int kmax, int B, int L, int Hq, int Hkv, int d,
+                       int qtile, int block, float scale, void* out, float* lse_out, void* stream);
+
+/*
+ * a5. Exact per-block attention mass ("How Much Dense Attention is
+ * Necessary?" Sec. 2.1: the full dense distribution of each query,
+ * aggregated over the query heads).  For group g and query tile i:
+ *   mass[g, i, b] = sum over the group's heads h and the tile's rows t of
+ *                   sum_{j in block b, j <= t} P_{h,t}(j),
+ * P_{h,t} the dense causal softmax of row (h, t).  Non-causal entries are 0.
+ * workspace: >= sa_oracle_mass_workspace_bytes(...) bytes of device memory.
+ * Requires dtype SA_BF16, d == 128, qtile == block == 128.
+ */
+size_t sa_oracle_mass_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int qtile, int block);
+sa_status_t sa_oracle_mass(const void* q, const void* k, int dtype, int B, int L, int Hq, int Hkv,
+                           int d, int qtile, int block, float scale, float* mass, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * One decode step: a1 append (k_new, v_new at cache rows L-T..L-1, sketch
+ * refreshed), a2+a3 sketch selection with budget k, a4 decode.  If
+ * host_io != 0, q, k_new, v_new and out are HOST pointers (pinned memory for
+ * asynchronous copies): the step copies the inputs to the device staging
+ * area in `workspace`, runs, and copies `out` back, all on `stream`.
+ * Otherwise they are device pointers.  sketch, caches, idx, cnt, scores
+ * (optional) are device memory as above.  workspace: >=
+ * sa_decode_step_workspace_bytes(...) bytes of device memory.
+ */
+size_t sa_decode_step_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int dtype, int kmax);
+sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, int dtype,
+                           void* k_cache, void* v_cache, float* sketch, int B, int T, int Hq,
+                           int Hkv, int d, int L, int L_stride, int block, int k, float scale,
+                           int32_t* idx, int32_t* cnt, int kmax, float* scores, void* out,
+                           int host_io, void* workspace, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ATTN_H */

@@ -1,0 +1,134 @@
+"""The C-ABI library: loads, exports every declared symbol, validates on the host.
+
+No GPU is needed: every call below is rejected by host-side validation before
+any CUDA call, or is a pure size query.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sa():
+    from top_block_sparse_pooled_b300 import _build
+    _build.build()
+    import top_block_sparse_pooled_b300 as m
+    return m
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(sa):
+    declared = _declared_symbols()
+    assert len(declared) >= 14
+    for name in declared:
+        assert hasattr(sa.lib, name), name
+    # the binding covers every entry point under the same name
+    assert declared <= set(sa.SIGNATURES)
+
+
+def test_version_and_status_names(sa):
+    assert sa.lib.sa_version() >= 100
+    assert sa.lib.sa_status_name(0) == b"SA_OK"
+    assert sa.lib.sa_status_name(4) == b"SA_ERR_TIMEOUT"
+
+
+def test_kmax_queries(sa):
+    # decode: forced {0, nb-1} + k candidates
+    assert sa.sa_select_kmax(32768, 64, 0, False, 32) == 34
+    assert sa.sa_select_kmax(64, 64, 0, False, 8) == 1      # one block: sink == local
+    assert sa.sa_select_kmax(128, 64, 0, False, 8) == 2     # two blocks, no candidates
+    assert sa.sa_select_kmax(4096, 64, 0, False, 8) == 10
+    # prefill: k_i = ceil(2 * c_i / 100) over c_i = 1..nq, + 2 forced (capped by the candidates)
+    assert sa.sa_select_kmax(131072, 128, 128, True, 0, 2, 100) == 23
+    assert sa.sa_select_kmax(32768, 128, 128, True, 0, 2, 100) == 8
+    assert sa.sa_select_kmax(128, 128, 128, True, 0, 2, 100) == 1
+    assert sa.sa_select_kmax(0, 64, 0, False, 8) == -1
+
+
+def test_workspace_queries(sa):
+    assert sa.sa_decode_workspace_bytes(8, 1, 32, 8, 128, 34) >= 8 * 8 * 34 * 4 * 130 * 4
+    assert sa.sa_decode_workspace_bytes(1, 1, 3, 2, 128, 10) == 0  # Hq not a multiple of Hkv
+    assert sa.sa_decode_step_workspace_bytes(8, 1, 32, 8, 128, sa.SA_BF16, 34) > \
+        sa.sa_decode_workspace_bytes(8, 1, 32, 8, 128, 34)
+
+
+def _expect(sa, status_code, call):
+    with pytest.raises(sa.SparseAttnError) as e:
+        call()
+    assert e.value.status == status_code, str(e.value)
+    return str(e.value)
+
+
+def test_invalid_arguments_rejected_on_host(sa):
+    L = sa.lib
+    # null pointers / bad shapes return without a launch
+    st = L.sa_build_sketch(None, sa.SA_BF16, 1, 1, 64, 64, 128, 64, None, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"null" in L.sa_last_error()
+    st = L.sa_build_sketch(16, sa.SA_BF16, 1, 1, 128, 64, 128, 64, 16, None)  # L > L_stride
+    assert st == sa.SA_ERR_INVALID_ARG
+    st = L.sa_build_sketch(16, 7, 1, 1, 64, 64, 128, 64, 16, None)  # bad dtype
+    assert st == sa.SA_ERR_INVALID_ARG and b"dtype" in L.sa_last_error()
+    st = L.sa_build_sketch(16, sa.SA_BF16, 1, 1, 64, 64, 96, 64, 16, None)  # d unsupported
+    assert st == sa.SA_ERR_UNSUPPORTED
+    # decode: kmax too small for the workspace, block size unsupported, G*T too big
+    args = [16, 16, 16, sa.SA_BF16, 16, 16, 34, 8, 1, 32, 8, 128, 32768, 32768, 64, 0.088, 16, 16, 0, None]
+    st = L.sa_decode(*args)
+    assert st == sa.SA_ERR_INVALID_ARG and b"workspace" in L.sa_last_error()
+    bad = list(args)
+    bad[14] = 128
+    assert L.sa_decode(*bad) == sa.SA_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[8], bad[9] = 16, 64  # T = 16, Hq = 64 -> G*T = 128
+    assert L.sa_decode(*bad) == sa.SA_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[1] = 17  # misaligned cache
+    bad[17] = 1 << 30
+    assert L.sa_decode(*bad) == sa.SA_ERR_INVALID_ARG
+    # select: kmax smaller than the selection needs
+    st = L.sa_select_topk(sa.SA_SELECT_SKETCH, 16, sa.SA_BF16, 16, None, 8, 1, 32, 8, 128, 32768, 32768, 64, 0, 0,
+                          32, 0, 1, 0.088, 16, 16, 33, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"kmax" in L.sa_last_error()
+    # select: MASS mode without scores
+    st = L.sa_select_topk(sa.SA_SELECT_MASS, None, sa.SA_BF16, None, None, 1, 32768, 16, 2, 128, 32768, 32768, 128,
+                          128, 1, 0, 2, 100, 0.088, 16, 16, 8, None)
+    assert st == sa.SA_ERR_INVALID_ARG
+    # prefill: unsupported dtype / tile shape
+    st = L.sa_prefill(16, 16, 16, sa.SA_F32, 16, 16, 8, 1, 4096, 16, 2, 128, 128, 128, 0.088, 16, None, None)
+    assert st == sa.SA_ERR_UNSUPPORTED
+    st = L.sa_prefill(16, 16, 16, sa.SA_BF16, 16, 16, 8, 1, 4096, 16, 2, 128, 64, 128, 0.088, 16, None, None)
+    assert st == sa.SA_ERR_UNSUPPORTED
+    # append past the cache
+    st = L.sa_append_kv(16, 16, sa.SA_BF16, 1, 1, 4, 128, 16, 16, 64, 62, 64, 16, None)
+    assert st == sa.SA_ERR_INVALID_ARG
+    # device status needs an output pointer
+    assert L.sa_device_status(None, 0) == sa.SA_ERR_INVALID_ARG
+
+
+def test_binding_raises_with_message(sa):
+    msg = _expect(sa, sa.SA_ERR_INVALID_ARG,
+                  lambda: sa._check(sa.lib.sa_build_sketch(None, 1, 1, 1, 64, 64, 128, 64, None, None)))
+    assert "null" in msg
+
+
+def test_package_has_no_cpu_fallback():
+    """The product package never imports the oracle or the generator."""
+    pkg = os.path.join(ROOT, "top_block_sparse_pooled_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "oracle.c" not in text and "liboracle" not in text, fn

@@ -1,0 +1,434 @@
+// k_select.cu -- block scoring and deterministic top-k selection.
+//
+// "How Much Dense Attention is Necessary?" Sec. 2.1-2.2: score the candidate
+// blocks, keep the top-k under a fixed budget, recompute attention on them.
+// Sink block 0 and the local / diagonal block are always kept ("Pulsar
+// Attention" Phase 1, "Faster Than Flash" Sec. 2) and do not count against
+// the budget.  Ties go to the lower block index; the output is ascending.
+//
+// Top-k is an exact MSB-first radix select on order-preserving 32-bit keys of
+// the float32 scores (four 8-bit digit passes over a 256-bin shared-memory
+// histogram), followed by an index-ordered scan that resolves ties at the
+// threshold key and compacts the selection in ascending order.
+#pragma once
+
+#include "sa_ptx.cuh"
+
+namespace sa {
+
+constexpr int kSelThreads = 256;
+
+struct TopkShared {
+  uint32_t hist[256];
+  uint32_t warp_tot[kSelThreads / 32];
+  uint32_t dsel;
+  uint32_t rem_next;
+};
+
+// Exclusive block-wide prefix sum of v (all kSelThreads threads); *total gets the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, TopkShared& S, uint32_t* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) S.warp_tot[w] = inc;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < kSelThreads / 32; ++i) {
+    const uint32_t x = S.warp_tot[i];
+    before += (i < w) ? x : 0u;
+    all += x;
+  }
+  __syncthreads();
+  *total = all;
+  return before + inc - v;
+}
+
+// Select from scores sc[0:n) (shared memory): forced {0, f1}; candidates the
+// rest; keep min(budget, #candidates) highest (ties -> lower index).  Writes
+// idx_out[0:kmax] (ascending, -1 padded) and *cnt_out.  All threads call.
+__device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax, int32_t* __restrict__ idx_out,
+                           int32_t* __restrict__ cnt_out, TopkShared& S) {
+  const int tid = threadIdx.x;
+  const bool has_f1 = (f1 > 0 && f1 < n);
+  const int ncand = n - (n > 0 ? 1 : 0) - (has_f1 ? 1 : 0);
+  int take = budget < ncand ? budget : ncand;
+  if (take < 0) take = 0;
+  const bool take_all = (take == ncand);
+  uint32_t thr = 0xFFFFFFFFu;
+  uint32_t need_eq = 0;
+  if (!take_all && take > 0) {
+    uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(take);
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kSelThreads) S.hist[i] = 0;
+      __syncthreads();
+      for (int b = tid; b < n; b += kSelThreads) {
+        if (b == 0 || b == f1) continue;
+        const uint32_t key = float_key(sc[b]);
+        if ((key & mask) == prefix) atomicAdd(&S.hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        uint32_t c[8], s = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          c[e] = S.hist[255 - 8 * tid - e];
+          s += c[e];
+        }
+        uint32_t inc = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+          if (tid >= o) inc += y;
+        }
+        const uint32_t exc = inc - s;
+        if (exc < remaining && remaining <= inc) {
+          uint32_t run = exc;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (run + c[e] >= remaining) {
+              S.dsel = 255u - 8u * tid - e;
+              S.rem_next = remaining - run;
+              break;
+            }
+            run += c[e];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= S.dsel << shift;
+      mask |= 255u << shift;
+      remaining = S.rem_next;
+      __syncthreads();
+    }
+    thr = prefix;
+    need_eq = remaining;
+  }
+  // contiguous index range per thread, so that ranks follow index order
+  const int per = (n + kSelThreads - 1) / kSelThreads;
+  const int lo = tid * per, hi = min(n, lo + per);
+  uint32_t eq_before = 0, tot;
+  if (!take_all && take > 0) {
+    uint32_t eqc = 0;
+    for (int b = lo; b < hi; ++b)
+      if (b != 0 && b != f1 && float_key(sc[b]) == thr) ++eqc;
+    eq_before = block_excl_scan(eqc, S, &tot);
+  }
+  uint32_t nsel = 0;
+  {
+    uint32_t eqr = eq_before;
+    for (int b = lo; b < hi; ++b) {
+      bool sel;
+      if (b == 0 || b == f1) {
+        sel = true;
+      } else if (take_all) {
+        sel = true;
+      } else if (take == 0) {
+        sel = false;
+      } else {
+        const uint32_t key = float_key(sc[b]);
+        sel = key > thr || (key == thr && eqr < need_eq);
+        if (key == thr) ++eqr;
+      }
+      nsel += sel ? 1u : 0u;
+    }
+  }
+  uint32_t total;
+  uint32_t pos = block_excl_scan(nsel, S, &total);
+  {
+    uint32_t eqr = eq_before;
+    for (int b = lo; b < hi; ++b) {
+      bool sel;
+      if (b == 0 || b == f1) {
+        sel = true;
+      } else if (take_all) {
+        sel = true;
+      } else if (take == 0) {
+        sel = false;
+      } else {
+        const uint32_t key = float_key(sc[b]);
+        sel = key > thr || (key == thr && eqr < need_eq);
+        if (key == thr) ++eqr;
+      }
+      if (sel) {
+        if (pos < static_cast<uint32_t>(kmax)) idx_out[pos] = b;
+        ++pos;
+      }
+    }
+  }
+  for (int i = static_cast<int>(total) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
+  if (tid == 0) *cnt_out = static_cast<int32_t>(total);
+}
+
+// --------------------------------------------------------------------------
+// Decode selection.  grid (CS, groups), cluster (CS, 1, 1), kSelThreads.
+// Each CTA of a group's cluster scores blocks [rank*per, rank*per + per) from
+// a TMA-staged, 128B-swizzled sketch tile (thread per block, q broadcast from
+// shared memory); CTA rank 0 then gathers the group's scores through
+// distributed shared memory and runs the top-k.
+constexpr int kSelTileRows = 256;
+
+template <int D, int RMAX>
+struct SelDecodeSmem {
+  static constexpr int kBoxes = D * 4 / 128;                      // 128-byte column boxes
+  static constexpr int kTileBytes = kBoxes * kSelTileRows * 128;  // one staged tile
+  static constexpr int kMaxScores = 16384;                        // gathered scores (rank 0)
+  static constexpr int kRegion = kTileBytes > kMaxScores * 4 ? kTileBytes : kMaxScores * 4;
+  static constexpr int kQOff = kRegion;
+  static constexpr int kScOff = kQOff + RMAX * D * 4;
+  static constexpr int kMaxPer = 1024;
+  static constexpr int kTopkOff = kScOff + kMaxPer * 4;
+  static constexpr int kBarOff = kTopkOff + ((sizeof(TopkShared) + 15) / 16) * 16;
+  static constexpr int kBytes = kBarOff + 16;
+};
+
+template <typename TE, int D, int RMAX>
+__global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
+    const __grid_constant__ CUtensorMap sk_map, const TE* __restrict__ q, int T, int Hq, int Hkv, int nb,
+    int nb_cap, float scale, int per, int k, float* __restrict__ scores_out, int32_t* __restrict__ idx,
+    int32_t* __restrict__ cnt, int kmax) {
+  using SM = SelDecodeSmem<D, RMAX>;
+  extern __shared__ __align__(1024) uint8_t smem_sel_dec[];
+  uint8_t* smem_raw = smem_sel_dec;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* q_s = reinterpret_cast<float*>(smem + SM::kQOff);
+  float* sc = reinterpret_cast<float*>(smem + SM::kScOff);
+  TopkShared& S = *reinterpret_cast<TopkShared*>(smem + SM::kTopkOff);
+  const uint32_t bar = smem_u32(smem + SM::kBarOff);
+
+  const int tid = threadIdx.x;
+  const int g = blockIdx.y;
+  const uint32_t rank = cluster_ctarank();
+  const int G = Hq / Hkv, R = G * T;
+  const int b = g / Hkv, kvh = g % Hkv;
+  const int b0 = static_cast<int>(rank) * per;
+  const int b1 = min(nb, b0 + per);
+
+  if (tid == 0) {
+    prefetch_tmap(&sk_map);
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  for (int i = tid; i < RMAX * D; i += kSelThreads) {
+    const int r = i / D, c = i % D;
+    float v = 0.f;
+    if (r < R) {
+      const int t = r / G, hh = r % G;
+      v = static_cast<float>(q[((static_cast<size_t>(b) * T + t) * Hq + kvh * G + hh) * D + c]) * scale;
+    }
+    q_s[i] = v;
+  }
+  __syncthreads();
+
+  bool ok = true;
+  uint32_t phase = 0;
+  for (int t0 = b0; t0 < b1; t0 += kSelTileRows) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar, SM::kTileBytes);
+#pragma unroll
+      for (int bx = 0; bx < SM::kBoxes; ++bx)
+        tma_g2s_2d(smem_u32(smem + bx * kSelTileRows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
+    }
+    ok = mbar_wait(bar, phase);
+    phase ^= 1;
+    if (__syncthreads_or(!ok)) break;
+    const int row = t0 + tid;
+    if (row < b1) {
+      float acc[RMAX];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+#pragma unroll 4
+      for (int c = 0; c < D / 4; ++c) {
+        const int bx = c >> 3, cc = c & 7;
+        const float4 kv = *reinterpret_cast<const float4*>(smem + bx * kSelTileRows * 128 + tid * 128 +
+                                                           ((cc ^ (tid & 7)) << 4));
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          const float4 qv = *reinterpret_cast<const float4*>(q_s + r * D + c * 4);
+          acc[r] = fmaf(qv.x, kv.x, acc[r]);
+          acc[r] = fmaf(qv.y, kv.y, acc[r]);
+          acc[r] = fmaf(qv.z, kv.z, acc[r]);
+          acc[r] = fmaf(qv.w, kv.w, acc[r]);
+        }
+      }
+      float s = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+        if (r < R) s = fmaxf(s, acc[r]);
+      sc[row - b0] = s;
+      if (scores_out) scores_out[static_cast<size_t>(g) * nb + row] = s;
+    }
+    __syncthreads();
+  }
+  if (!ok) {
+    // a TMA wait gave up: leave the selection untouched; the host sees SA_ERR_TIMEOUT
+  }
+  cluster_sync();
+  float* all = reinterpret_cast<float*>(smem);  // reuses the tile region
+  if (rank == 0) {
+    for (int bb = tid; bb < nb; bb += kSelThreads) {
+      const uint32_t owner = static_cast<uint32_t>(bb / per);
+      all[bb] = ld_cluster_f32(map_cluster(smem_u32(sc + (bb - static_cast<int>(owner) * per)), owner));
+    }
+  }
+  cluster_sync();
+  if (rank != 0) return;
+  __syncthreads();
+  block_topk(all, nb, nb - 1, k, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, S);
+}
+
+// --------------------------------------------------------------------------
+// Selection from a given score array (mass mode, decode or prefill).
+// grid (nq, groups).  Scores: [groups, nq, nb]; unit (g, i) considers its
+// causal blocks 0..c_i-1 (c_i from the host-side rule), forced {0, c_i - 1}.
+__global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* __restrict__ scores, int nb,
+                                                                   int prefill, int L, int qtile, int Bk, int k,
+                                                                   int frac_num, int frac_den,
+                                                                   int32_t* __restrict__ idx,
+                                                                   int32_t* __restrict__ cnt, int kmax) {
+  extern __shared__ __align__(1024) uint8_t smem_sel_given[];
+  uint8_t* smem_raw = smem_sel_given;
+  TopkShared& S = *reinterpret_cast<TopkShared*>(smem_raw);
+  float* sc = reinterpret_cast<float*>(smem_raw + ((sizeof(TopkShared) + 15) / 16) * 16);
+  const int i = blockIdx.x, g = blockIdx.y, nq = gridDim.x;
+  int nvalid = nb, budget = k;
+  if (prefill) {
+    const int last = min((i + 1) * qtile, L) - 1;
+    nvalid = last / Bk + 1;
+    if (frac_num > 0) budget = k + (frac_num * nvalid + frac_den - 1) / frac_den;
+  }
+  const size_t u = static_cast<size_t>(g) * nq + i;
+  for (int bb = threadIdx.x; bb < nvalid; bb += kSelThreads) sc[bb] = scores[u * nb + bb];
+  __syncthreads();
+  block_topk(sc, nvalid, nvalid - 1, budget, kmax, idx + u * kmax, cnt + u, S);
+}
+
+// --------------------------------------------------------------------------
+// Prefill sketch selection (CUDA cores, float32).  grid (nq, groups).
+// For tile i: s[b] = max over the group's heads and the tile's rows of
+// scale * q . sketch[b] for b <= i (qtile == Bk), then top-k.
+// Rows are processed in chunks of kPfRowChunk; each thread owns rows and
+// accumulates 32 block scores at a time against a shared sketch slab.
+constexpr int kPfRowChunk = 256;
+constexpr int kPfBlk = 32;
+
+template <int D>
+struct SelPrefillSmem {
+  static constexpr int kQBytes = kPfRowChunk * D * 2;       // bf16 rows, swizzled 16-byte chunks
+  static constexpr int kSkOff = kQBytes;
+  static constexpr int kSkBytes = kPfBlk * D * 4;
+  static constexpr int kRedOff = kSkOff + kSkBytes;
+  static constexpr int kRedBytes = (kSelThreads / 32) * kPfBlk * 4;
+  static constexpr int kScOff = kRedOff + kRedBytes;
+  static constexpr int kMaxBlocks = 8192;
+  static constexpr int kTopkOff = kScOff + kMaxBlocks * 4;
+  static constexpr int kBytes = kTopkOff + ((sizeof(TopkShared) + 15) / 16) * 16;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kSelThreads) select_prefill_sketch_kernel(
+    const __nv_bfloat16* __restrict__ q, const float* __restrict__ sketch, int L, int Hq, int Hkv, int nb_cap,
+    int qtile, int Bk, float scale, int k, int frac_num, int frac_den, float* __restrict__ scores_out, int nb,
+    int32_t* __restrict__ idx, int32_t* __restrict__ cnt, int kmax) {
+  using SM = SelPrefillSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_sel_pf[];
+  uint8_t* smem_raw = smem_sel_pf;
+  uint8_t* q_s = smem_raw;
+  float* sk_s = reinterpret_cast<float*>(smem_raw + SM::kSkOff);
+  float* red = reinterpret_cast<float*>(smem_raw + SM::kRedOff);
+  float* sc = reinterpret_cast<float*>(smem_raw + SM::kScOff);
+  TopkShared& S = *reinterpret_cast<TopkShared*>(smem_raw + SM::kTopkOff);
+  constexpr int CPR = D / 8;  // 16-byte chunks per bf16 row
+
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int i = blockIdx.x, g = blockIdx.y, nq = gridDim.x;
+  const int G = Hq / Hkv, b = g / Hkv, kvh = g % Hkv;
+  const int t0 = i * qtile, t1 = min(t0 + qtile, L);
+  const int nvalid = (t1 - 1) / Bk + 1;
+  const int nrows = (t1 - t0) * G;
+  for (int bb = tid; bb < nvalid; bb += kSelThreads) sc[bb] = -INFINITY;
+  __syncthreads();
+  for (int rc = 0; rc < nrows; rc += kPfRowChunk) {
+    const int nr = min(kPfRowChunk, nrows - rc);
+    // stage rows (row r of the chunk = tile row (rc + r) / G, head (rc + r) % G)
+    for (int e = tid; e < nr * CPR; e += kSelThreads) {
+      const int r = e / CPR, c = e % CPR;
+      const int rr = rc + r;
+      const int t = t0 + rr / G, h = kvh * G + rr % G;
+      const uint4 v = *reinterpret_cast<const uint4*>(q + ((static_cast<size_t>(b) * L + t) * Hq + h) * D + c * 8);
+      *reinterpret_cast<uint4*>(q_s + r * (D * 2) + ((c ^ (r & (CPR - 1))) << 4)) = v;
+    }
+    __syncthreads();
+    for (int bs = 0; bs < nvalid; bs += kPfBlk) {
+      const int nbk = min(kPfBlk, nvalid - bs);
+      for (int e = tid; e < kPfBlk * D; e += kSelThreads) {
+        const int bb = e / D;
+        sk_s[e] = bb < nbk ? sketch[(static_cast<size_t>(g) * nb_cap + bs + bb) * D + e % D] * scale : 0.f;
+      }
+      __syncthreads();
+      float mx[kPfBlk];
+#pragma unroll
+      for (int j = 0; j < kPfBlk; ++j) mx[j] = -INFINITY;
+      for (int r = tid; r < nr; r += kSelThreads) {
+        float acc[kPfBlk];
+#pragma unroll
+        for (int j = 0; j < kPfBlk; ++j) acc[j] = 0.f;
+        for (int c = 0; c < CPR; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(q_s + r * (D * 2) + ((c ^ (r & (CPR - 1))) << 4));
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+          float qf[8];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            qf[2 * e2] = __uint_as_float(wv[e2] << 16);
+            qf[2 * e2 + 1] = __uint_as_float(wv[e2] & 0xFFFF0000u);
+          }
+#pragma unroll
+          for (int j = 0; j < kPfBlk; ++j) {
+            const float4 s0 = *reinterpret_cast<const float4*>(sk_s + j * D + c * 8);
+            const float4 s1 = *reinterpret_cast<const float4*>(sk_s + j * D + c * 8 + 4);
+            float a = acc[j];
+            a = fmaf(qf[0], s0.x, a);
+            a = fmaf(qf[1], s0.y, a);
+            a = fmaf(qf[2], s0.z, a);
+            a = fmaf(qf[3], s0.w, a);
+            a = fmaf(qf[4], s1.x, a);
+            a = fmaf(qf[5], s1.y, a);
+            a = fmaf(qf[6], s1.z, a);
+            a = fmaf(qf[7], s1.w, a);
+            acc[j] = a;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kPfBlk; ++j) mx[j] = fmaxf(mx[j], acc[j]);
+      }
+      // max over the CTA's rows for each of the kPfBlk blocks
+#pragma unroll
+      for (int j = 0; j < kPfBlk; ++j) {
+        float v = mx[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+        if (lane == 0) red[w * kPfBlk + j] = v;
+      }
+      __syncthreads();
+      if (tid < nbk) {
+        float v = -INFINITY;
+        for (int ww = 0; ww < kSelThreads / 32; ++ww) v = fmaxf(v, red[ww * kPfBlk + tid]);
+        sc[bs + tid] = fmaxf(sc[bs + tid], v);
+      }
+      __syncthreads();
+    }
+  }
+  const size_t u = static_cast<size_t>(g) * nq + i;
+  if (scores_out)
+    for (int bb = tid; bb < nb; bb += kSelThreads) scores_out[u * nb + bb] = bb < nvalid ? sc[bb] : -INFINITY;
+  int budget = k;
+  if (frac_num > 0) budget = k + (frac_num * nvalid + frac_den - 1) / frac_den;
+  __syncthreads();
+  block_topk(sc, nvalid, nvalid - 1, budget, kmax, idx + u * kmax, cnt + u, S);
+}
+
+}  // namespace sa

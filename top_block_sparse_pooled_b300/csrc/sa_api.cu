@@ -1,0 +1,643 @@
+// sa_api.cu -- the C ABI of libsparse_attn (see include/sparse_attn.h):
+// argument validation on the host, tensor-map encoding, launch sizing.
+// The kernels are compiled into this one translation unit.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "sparse_attn.h"
+
+#include "k_decode.cu"
+#include "k_select.cu"
+#include "k_sketch.cu"
+
+namespace {
+
+thread_local std::string t_err;
+
+sa_status_t fail(sa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return st;
+}
+
+#define SA_ARG(cond, ...) \
+  do {                    \
+    if (!(cond)) return fail(SA_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+#define SA_SUP(cond, ...) \
+  do {                    \
+    if (!(cond)) return fail(SA_ERR_UNSUPPORTED, __VA_ARGS__); \
+  } while (0)
+#define SA_CUDA(call)                                                                 \
+  do {                                                                                \
+    cudaError_t e_ = (call);                                                          \
+    if (e_ != cudaSuccess) return fail(SA_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+#define SA_TRY(expr)              \
+  do {                            \
+    sa_status_t s_ = (expr);      \
+    if (s_ != SA_OK) return s_;   \
+  } while (0)
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+inline int esize(int dtype) { return dtype == SA_F32 ? 4 : 2; }
+
+// ------------------------------------------------------------------ device info
+struct DevInfo {
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+
+sa_status_t dev_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  SA_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(SA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!have[dev]) {
+    DevInfo d;
+    SA_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+    SA_CUDA(cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev));
+    SA_CUDA(cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  if (out->cc_major != 10 || out->cc_minor != 3)
+    return fail(SA_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", out->cc_major, out->cc_minor);
+  return SA_OK;
+}
+
+// Per-kernel shared-memory opt-in (cached per function).
+template <typename K>
+sa_status_t set_smem(K kernel, int bytes) {
+  SA_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bytes));
+  return SA_OK;
+}
+
+// --------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+sa_status_t get_encode(EncodeTiledFn* fn) {
+  static std::once_flag once;
+  static EncodeTiledFn f = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) f = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!f) return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *fn = f;
+  return SA_OK;
+}
+
+// 2-D tiled map over a row-major [rows, inner] array; box {box_inner, box_rows}.
+sa_status_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc;
+  SA_TRY(get_encode(&enc));
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d): inner=%llu rows=%llu stride=%llu box=%ux%u", (int)r,
+                (unsigned long long)inner, (unsigned long long)rows, (unsigned long long)row_stride_bytes, box_inner,
+                box_rows);
+  return SA_OK;
+}
+
+inline CUtensorMapDataType map_dtype(int dtype) {
+  return dtype == SA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+sa_status_t check_dtype(int dtype) {
+  SA_ARG(dtype == SA_F32 || dtype == SA_BF16, "dtype must be SA_F32 (0) or SA_BF16 (1), got %d", dtype);
+  return SA_OK;
+}
+
+int rmax_for(int R) { return R <= 4 ? 4 : R <= 8 ? 8 : R <= 16 ? 16 : 32; }
+
+// ===================================================================== a1
+template <typename TE>
+sa_status_t launch_build_sketch(const void* k, int groups, int L, int Ls, int d, int block, float* sketch,
+                                cudaStream_t st) {
+  const int nb = cdiv(L, block);
+  const dim3 grid(nb, groups);
+  if (d == 128)
+    sa::build_sketch_kernel<TE, 128><<<grid, sa::kSketchThreads, 0, st>>>(static_cast<const TE*>(k), L, Ls, block,
+                                                                           sketch);
+  else
+    sa::build_sketch_kernel<TE, 64><<<grid, sa::kSketchThreads, 0, st>>>(static_cast<const TE*>(k), L, Ls, block,
+                                                                          sketch);
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
+}
+
+template <typename TE>
+sa_status_t launch_append(const void* kn, const void* vn, int B, int Hkv, int T, int d, void* kc, void* vc, int Ls,
+                          int pos, int block, float* sketch, cudaStream_t st) {
+  const int nb_cap = cdiv(Ls, block);
+  if (d == 128)
+    sa::append_kv_kernel<TE, 128><<<B * Hkv, sa::kSketchThreads, 0, st>>>(
+        static_cast<const TE*>(kn), static_cast<const TE*>(vn), T, Hkv, static_cast<TE*>(kc), static_cast<TE*>(vc),
+        Ls, pos, block, nb_cap, sketch);
+  else
+    sa::append_kv_kernel<TE, 64><<<B * Hkv, sa::kSketchThreads, 0, st>>>(
+        static_cast<const TE*>(kn), static_cast<const TE*>(vn), T, Hkv, static_cast<TE*>(kc), static_cast<TE*>(vc),
+        Ls, pos, block, nb_cap, sketch);
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
+}
+
+// ================================================================== a2 + a3
+struct SelectArgs {
+  int mode;
+  const void* q;
+  int dtype;
+  const float* sketch;
+  float* scores;
+  int B, Tq, Hq, Hkv, d, L, Ls, block, qtile, prefill, k, frac_num, frac_den;
+  float scale;
+  int32_t* idx;
+  int32_t* cnt;
+  int kmax;
+};
+
+int max_cluster_size(const void* fn, int smem, int groups, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, groups);
+  cfg.blockDim = dim3(sa::kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 16;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int size = 0;
+  if (cudaOccupancyMaxPotentialClusterSize(&size, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 8;
+  }
+  return size;
+}
+
+template <typename TE, int D, int RMAX>
+sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStream_t st) {
+  using SM = sa::SelDecodeSmem<D, RMAX>;
+  const int groups = a.B * a.Hkv;
+  const int nb = cdiv(a.L, a.block);
+  const int nb_cap = cdiv(a.Ls, a.block);
+  auto kern = sa::select_decode_kernel<TE, D, RMAX>;
+  const int smem = SM::kBytes + 1024;
+  SA_TRY(set_smem(kern, smem));
+  static int max_cs = 0;  // per instantiation
+  if (max_cs == 0) {
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    max_cs = std::max(1, std::min(16, max_cluster_size(reinterpret_cast<const void*>(kern), smem, groups, st)));
+  }
+  int cs = std::min(max_cs, std::max(1, cdiv(di.sms, groups)));
+  cs = std::max(cs, cdiv(nb, SM::kMaxPer));
+  SA_SUP(cs <= max_cs, "decode selection over %d blocks needs a cluster of %d CTAs (device allows %d)", nb, cs,
+         max_cs);
+  cs = std::min(cs, nb);
+  const int per = cdiv(nb, cs);
+  cs = cdiv(nb, per);
+  CUtensorMap map;
+  SA_TRY(make_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.sketch, D, static_cast<uint64_t>(groups) * nb_cap,
+                     D * 4, 32, sa::kSelTileRows, CU_TENSOR_MAP_SWIZZLE_128B));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, groups);
+  cfg.blockDim = dim3(sa::kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  SA_CUDA(cudaLaunchKernelEx(&cfg, kern, map, static_cast<const TE*>(a.q), a.Tq, a.Hq, a.Hkv, nb, nb_cap, a.scale,
+                             per, a.k, a.scores, a.idx, a.cnt, a.kmax));
+  return SA_OK;
+}
+
+template <typename TE, int D>
+sa_status_t dispatch_select_decode_r(const SelectArgs& a, const DevInfo& di, cudaStream_t st) {
+  const int R = (a.Hq / a.Hkv) * a.Tq;
+  switch (rmax_for(R)) {
+    case 4: return launch_select_decode<TE, D, 4>(a, di, st);
+    case 8: return launch_select_decode<TE, D, 8>(a, di, st);
+    case 16: return launch_select_decode<TE, D, 16>(a, di, st);
+    default: return launch_select_decode<TE, D, 32>(a, di, st);
+  }
+}
+
+sa_status_t run_select(const SelectArgs& a, cudaStream_t st) {
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  const int groups = a.B * a.Hkv;
+  const int nb = cdiv(a.L, a.block);
+  if (a.mode == SA_SELECT_MASS) {
+    const int nq = a.prefill ? cdiv(a.L, a.qtile) : 1;
+    const int smem = static_cast<int>(((sizeof(sa::TopkShared) + 15) / 16) * 16) + nb * 4;
+    SA_TRY(set_smem(sa::select_given_kernel, smem));
+    sa::select_given_kernel<<<dim3(nq, groups), sa::kSelThreads, smem, st>>>(
+        a.scores, nb, a.prefill, a.L, a.qtile, a.block, a.k, a.frac_num, a.frac_den, a.idx, a.cnt, a.kmax);
+    SA_CUDA(cudaGetLastError());
+    return SA_OK;
+  }
+  if (!a.prefill) {
+    if (a.dtype == SA_F32)
+      return a.d == 128 ? dispatch_select_decode_r<float, 128>(a, di, st) : dispatch_select_decode_r<float, 64>(a, di, st);
+    return a.d == 128 ? dispatch_select_decode_r<__nv_bfloat16, 128>(a, di, st)
+                      : dispatch_select_decode_r<__nv_bfloat16, 64>(a, di, st);
+  }
+  // prefill, sketch mode (bf16 queries)
+  const int nq = cdiv(a.L, a.qtile);
+  const int nb_cap = cdiv(a.Ls, a.block);
+  if (a.d == 128) {
+    using SM = sa::SelPrefillSmem<128>;
+    SA_TRY(set_smem(sa::select_prefill_sketch_kernel<128>, SM::kBytes));
+    sa::select_prefill_sketch_kernel<128><<<dim3(nq, groups), sa::kSelThreads, SM::kBytes, st>>>(
+        static_cast<const __nv_bfloat16*>(a.q), a.sketch, a.L, a.Hq, a.Hkv, nb_cap, a.qtile, a.block, a.scale, a.k,
+        a.frac_num, a.frac_den, a.scores, nb, a.idx, a.cnt, a.kmax);
+  } else {
+    using SM = sa::SelPrefillSmem<64>;
+    SA_TRY(set_smem(sa::select_prefill_sketch_kernel<64>, SM::kBytes));
+    sa::select_prefill_sketch_kernel<64><<<dim3(nq, groups), sa::kSelThreads, SM::kBytes, st>>>(
+        static_cast<const __nv_bfloat16*>(a.q), a.sketch, a.L, a.Hq, a.Hkv, nb_cap, a.qtile, a.block, a.scale, a.k,
+        a.frac_num, a.frac_den, a.scores, nb, a.idx, a.cnt, a.kmax);
+  }
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
+}
+
+// ====================================================================== a4
+struct DecodeArgs {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  int dtype;
+  const int32_t* idx;
+  const int32_t* cnt;
+  int kmax, B, T, Hq, Hkv, d, L, Ls, block;
+  float scale;
+  void* out;
+  void* ws;
+  size_t ws_bytes;
+};
+
+size_t decode_ws_bytes(int groups, int R, int d, int kmax) {
+  const size_t rm = static_cast<size_t>(rmax_for(R));
+  const size_t o = static_cast<size_t>(groups) * kmax * rm * d * 4;
+  const size_t ml = static_cast<size_t>(groups) * kmax * rm * 2 * 4;
+  return ((o + 255) / 256) * 256 + ((ml + 255) / 256) * 256;
+}
+
+template <typename TE, int D, int RMAX>
+sa_status_t launch_decode(const DecodeArgs& a, const DevInfo& di, cudaStream_t st) {
+  using C = sa::DecodeCfg<TE, D, RMAX>;
+  auto kern = sa::decode_split_kernel<TE, D, RMAX>;
+  SA_TRY(set_smem(kern, C::kBytes));
+  static int occ = 0;  // per instantiation
+  if (occ == 0) {
+    SA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, sa::kDecThreads, C::kBytes));
+    occ = std::max(occ, 1);
+  }
+  const int groups = a.B * a.Hkv;
+  const int target = di.sms * occ;
+  int nsplit = std::max(1, std::min(a.kmax, target / std::max(groups, 1)));
+  const int chunk = cdiv(a.kmax, nsplit);
+  nsplit = cdiv(a.kmax, chunk);
+  const size_t o_bytes = ((static_cast<size_t>(groups) * a.kmax * RMAX * D * 4 + 255) / 256) * 256;
+  float* ws_o = static_cast<float*>(a.ws);
+  float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(a.ws) + o_bytes);
+  CUtensorMap km, vm;
+  const uint64_t rows = static_cast<uint64_t>(groups) * a.Ls;
+  SA_TRY(make_map_2d(&km, map_dtype(a.dtype), a.kc, D, rows, D * sizeof(TE), C::EPB, sa::kDecBk,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  SA_TRY(make_map_2d(&vm, map_dtype(a.dtype), a.vc, D, rows, D * sizeof(TE), C::EPB, sa::kDecBk,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  const float qscale = a.scale * 1.4426950408889634f;
+  kern<<<dim3(nsplit, groups), sa::kDecThreads, C::kBytes, st>>>(km, vm, static_cast<const TE*>(a.q), a.idx, a.cnt,
+                                                                 a.kmax, a.T, a.Hq, a.Hkv, a.L, a.Ls, qscale, chunk,
+                                                                 nsplit, ws_o, ws_ml);
+  SA_CUDA(cudaGetLastError());
+  sa::decode_combine_kernel<TE, D, RMAX><<<groups, sa::kDecThreads, 0, st>>>(ws_o, ws_ml, nsplit, a.T, a.Hq, a.Hkv,
+                                                                            static_cast<TE*>(a.out));
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
+}
+
+template <typename TE, int D>
+sa_status_t dispatch_decode_r(const DecodeArgs& a, const DevInfo& di, cudaStream_t st) {
+  switch (rmax_for((a.Hq / a.Hkv) * a.T)) {
+    case 4: return launch_decode<TE, D, 4>(a, di, st);
+    case 8: return launch_decode<TE, D, 8>(a, di, st);
+    case 16: return launch_decode<TE, D, 16>(a, di, st);
+    default: return launch_decode<TE, D, 32>(a, di, st);
+  }
+}
+
+sa_status_t run_decode(const DecodeArgs& a, cudaStream_t st) {
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  if (a.dtype == SA_F32)
+    return a.d == 128 ? dispatch_decode_r<float, 128>(a, di, st) : dispatch_decode_r<float, 64>(a, di, st);
+  return a.d == 128 ? dispatch_decode_r<__nv_bfloat16, 128>(a, di, st) : dispatch_decode_r<__nv_bfloat16, 64>(a, di, st);
+}
+
+// ------------------------------------------------------------ validation
+sa_status_t check_common(int dtype, int B, int Hq, int Hkv, int d) {
+  SA_TRY(check_dtype(dtype));
+  SA_ARG(B >= 1 && Hq >= 1 && Hkv >= 1, "B, Hq, Hkv must be >= 1 (got %d, %d, %d)", B, Hq, Hkv);
+  SA_ARG(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  SA_ARG(static_cast<long long>(B) * Hkv <= 65535, "B*Hkv must be <= 65535");
+  SA_SUP(d == 64 || d == 128, "head dim d must be 64 or 128, got %d", d);
+  return SA_OK;
+}
+
+sa_status_t validate_decode(const DecodeArgs& a) {
+  SA_TRY(check_common(a.dtype, a.B, a.Hq, a.Hkv, a.d));
+  SA_ARG(a.q && a.kc && a.vc && a.idx && a.cnt && a.out, "null pointer argument");
+  SA_ARG(a.T >= 1, "T must be >= 1");
+  SA_ARG(a.L >= 1 && a.L <= a.Ls, "need 1 <= L (%d) <= L_stride (%d)", a.L, a.Ls);
+  SA_SUP(a.block == sa::kDecBk, "decode supports block == %d, got %d", sa::kDecBk, a.block);
+  SA_ARG(a.T <= a.block && a.T <= a.L, "T (%d) must be <= block and <= L", a.T);
+  SA_SUP((a.Hq / a.Hkv) * a.T <= 32, "G*T (%d) must be <= 32", (a.Hq / a.Hkv) * a.T);
+  SA_ARG(a.kmax >= 1, "kmax must be >= 1");
+  SA_ARG(aligned16(a.kc) && aligned16(a.vc), "k/v caches must be 16-byte aligned");
+  SA_ARG(static_cast<long long>(a.B) * a.Hkv * a.Ls < (1LL << 31), "B*Hkv*L_stride too large");
+  SA_ARG(a.ws && aligned16(a.ws), "workspace must be a 16-byte-aligned device pointer");
+  const size_t need = decode_ws_bytes(a.B * a.Hkv, (a.Hq / a.Hkv) * a.T, a.d, a.kmax);
+  SA_ARG(a.ws_bytes >= need, "workspace too small: %zu < %zu bytes", a.ws_bytes, need);
+  return SA_OK;
+}
+
+int select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num, int frac_den) {
+  if (L < 1 || block < 1 || k < 0 || (prefill && qtile < 1) || frac_num < 0 || (frac_num > 0 && frac_den < 1))
+    return -1;
+  const int nb = cdiv(L, block);
+  if (!prefill) return (nb >= 2 ? 2 : 1) + std::min(k, std::max(nb - 2, 0));
+  const int nq = cdiv(L, qtile);
+  int best = 0;
+  for (int i = 0; i < nq; ++i) {
+    const int last = std::min((i + 1) * qtile, L) - 1;
+    const int c = last / block + 1;
+    const long long bud = k + (frac_num > 0 ? (static_cast<long long>(frac_num) * c + frac_den - 1) / frac_den : 0);
+    const int forced = c >= 2 ? 2 : 1;
+    const int take = static_cast<int>(std::min<long long>(bud, c - forced));
+    best = std::max(best, forced + take);
+  }
+  return best;
+}
+
+sa_status_t validate_select(const SelectArgs& a) {
+  SA_ARG(a.mode == SA_SELECT_SKETCH || a.mode == SA_SELECT_MASS, "mode must be SA_SELECT_SKETCH or SA_SELECT_MASS");
+  SA_ARG(a.B >= 1 && a.Hq >= 1 && a.Hkv >= 1 && a.Hq % a.Hkv == 0, "bad head counts");
+  SA_ARG(a.idx && a.cnt, "idx and cnt are required");
+  SA_ARG(a.L >= 1 && a.L <= a.Ls, "need 1 <= L <= L_stride");
+  SA_ARG(a.block >= 1 && a.k >= 0, "block >= 1 and k >= 0 required");
+  SA_ARG(a.frac_num >= 0 && (a.frac_num == 0 || a.frac_den >= 1), "bad budget fraction");
+  const int need = select_kmax(a.L, a.block, a.qtile, a.prefill, a.k, a.frac_num, a.frac_den);
+  SA_ARG(need >= 1, "bad selection parameters");
+  SA_ARG(a.kmax >= need, "kmax (%d) too small: the selection needs %d", a.kmax, need);
+  const int nb = cdiv(a.L, a.block);
+  SA_SUP(nb <= 16384, "at most 16384 blocks per sequence (got %d)", nb);
+  if (a.prefill) SA_ARG(a.qtile >= 1 && a.Tq == a.L, "prefill: qtile >= 1 and Tq == L required");
+  if (a.mode == SA_SELECT_MASS) {
+    SA_ARG(a.scores != nullptr, "MASS mode needs the scores array");
+    return SA_OK;
+  }
+  SA_TRY(check_common(a.dtype, a.B, a.Hq, a.Hkv, a.d));
+  SA_ARG(a.q && a.sketch, "SKETCH mode needs q and sketch");
+  SA_ARG(aligned16(a.sketch), "sketch must be 16-byte aligned");
+  if (!a.prefill) {
+    SA_ARG(a.Tq >= 1, "Tq must be >= 1");
+    SA_SUP((a.Hq / a.Hkv) * a.Tq <= 32, "G*Tq (%d) must be <= 32 for decode selection", (a.Hq / a.Hkv) * a.Tq);
+  } else {
+    SA_SUP(a.dtype == SA_BF16, "prefill sketch selection needs bf16 queries");
+    SA_SUP(nb <= sa::SelPrefillSmem<128>::kMaxBlocks, "prefill sketch selection supports <= %d blocks",
+           sa::SelPrefillSmem<128>::kMaxBlocks);
+    SA_ARG(aligned16(a.q), "q must be 16-byte aligned");
+  }
+  return SA_OK;
+}
+
+// ---------------------------------------------------------- prefill / mass
+sa_status_t prefill_impl(const void*, const void*, const void*, const int32_t*, const int32_t*, int, int, int, int,
+                         int, float, void*, float*, cudaStream_t) {
+  return fail(SA_ERR_UNSUPPORTED, "sa_prefill: not built yet");
+}
+size_t mass_ws_bytes(int, int, int, int, int, int) { return 0; }
+sa_status_t mass_impl(const void*, const void*, int, int, int, int, float, float*, void*, cudaStream_t) {
+  return fail(SA_ERR_UNSUPPORTED, "sa_oracle_mass: not built yet");
+}
+
+}  // namespace
+
+// ========================================================================= ABI
+extern "C" {
+
+int sa_version(void) { return 100; }
+
+const char* sa_last_error(void) { return t_err.c_str(); }
+
+const char* sa_status_name(int s) {
+  switch (s) {
+    case SA_OK: return "SA_OK";
+    case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG";
+    case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED";
+    case SA_ERR_CUDA: return "SA_ERR_CUDA";
+    case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT";
+    default: return "SA_UNKNOWN_STATUS";
+  }
+}
+
+sa_status_t sa_device_status(int* code, int clear) {
+  SA_ARG(code != nullptr, "code must not be NULL");
+  SA_CUDA(cudaDeviceSynchronize());
+  int v = 0;
+  SA_CUDA(cudaMemcpyFromSymbol(&v, sa::g_device_status, sizeof(int)));
+  *code = v;
+  if (clear) {
+    const int zero = 0;
+    SA_CUDA(cudaMemcpyToSymbol(sa::g_device_status, &zero, sizeof(int)));
+  }
+  return SA_OK;
+}
+
+sa_status_t sa_build_sketch(const void* k, int dtype, int B, int Hkv, int L, int L_stride, int d, int block,
+                            float* sketch, void* stream) {
+  t_err.clear();
+  SA_TRY(check_common(dtype, B, Hkv, Hkv, d));
+  SA_ARG(k && sketch, "null pointer argument");
+  SA_ARG(L >= 1 && L <= L_stride, "need 1 <= L (%d) <= L_stride (%d)", L, L_stride);
+  SA_ARG(block >= 1 && block <= 1024, "block must be in [1, 1024]");
+  SA_ARG(aligned16(k) && aligned16(sketch), "k and sketch must be 16-byte aligned");
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  if (dtype == SA_F32) return launch_build_sketch<float>(k, B * Hkv, L, L_stride, d, block, sketch, as_stream(stream));
+  return launch_build_sketch<__nv_bfloat16>(k, B * Hkv, L, L_stride, d, block, sketch, as_stream(stream));
+}
+
+sa_status_t sa_append_kv(const void* k_new, const void* v_new, int dtype, int B, int Hkv, int T, int d,
+                         void* k_cache, void* v_cache, int L_stride, int pos, int block, float* sketch,
+                         void* stream) {
+  t_err.clear();
+  SA_TRY(check_common(dtype, B, Hkv, Hkv, d));
+  SA_ARG(k_new && v_new && k_cache && v_cache && sketch, "null pointer argument");
+  SA_ARG(T >= 1 && pos >= 0 && static_cast<long long>(pos) + T <= L_stride, "need T >= 1, 0 <= pos, pos+T <= L_stride");
+  SA_ARG(block >= 1 && block <= 1024, "block must be in [1, 1024]");
+  SA_ARG(aligned16(k_new) && aligned16(v_new) && aligned16(k_cache) && aligned16(v_cache) && aligned16(sketch),
+         "pointers must be 16-byte aligned");
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  if (dtype == SA_F32)
+    return launch_append<float>(k_new, v_new, B, Hkv, T, d, k_cache, v_cache, L_stride, pos, block, sketch,
+                                as_stream(stream));
+  return launch_append<__nv_bfloat16>(k_new, v_new, B, Hkv, T, d, k_cache, v_cache, L_stride, pos, block, sketch,
+                                      as_stream(stream));
+}
+
+int sa_select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num, int frac_den) {
+  return select_kmax(L, block, qtile, prefill, k, frac_num, frac_den);
+}
+
+sa_status_t sa_select_topk(int mode, const void* q, int dtype, const float* sketch, float* scores, int B, int Tq,
+                           int Hq, int Hkv, int d, int L, int L_stride, int block, int qtile, int prefill, int k,
+                           int frac_num, int frac_den, float scale, int32_t* idx, int32_t* cnt, int kmax,
+                           void* stream) {
+  t_err.clear();
+  SelectArgs a{mode, q, dtype, sketch, scores, B, Tq, Hq, Hkv, d, L, L_stride, block, qtile, prefill ? 1 : 0, k,
+               frac_num, frac_den, scale, idx, cnt, kmax};
+  SA_TRY(validate_select(a));
+  return run_select(a, as_stream(stream));
+}
+
+size_t sa_decode_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int kmax) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || kmax < 1 || d < 1) return 0;
+  return decode_ws_bytes(B * Hkv, (Hq / Hkv) * T, d, kmax);
+}
+
+sa_status_t sa_decode(const void* q, const void* k_cache, const void* v_cache, int dtype, const int32_t* idx,
+                      const int32_t* cnt, int kmax, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
+                      int block, float scale, void* out, void* workspace, size_t ws_bytes, void* stream) {
+  t_err.clear();
+  DecodeArgs a{q, k_cache, v_cache, dtype, idx, cnt, kmax, B, T, Hq, Hkv, d, L, L_stride, block, scale, out,
+               workspace, ws_bytes};
+  SA_TRY(validate_decode(a));
+  return run_decode(a, as_stream(stream));
+}
+
+sa_status_t sa_prefill(const void* q, const void* k, const void* v, int dtype, const int32_t* idx, const int32_t* cnt,
+                       int kmax, int B, int L, int Hq, int Hkv, int d, int qtile, int block, float scale, void* out,
+                       float* lse_out, void* stream) {
+  t_err.clear();
+  SA_TRY(check_common(dtype, B, Hq, Hkv, d));
+  SA_ARG(q && k && v && idx && cnt && out, "null pointer argument");
+  SA_ARG(L >= 1 && kmax >= 1, "L >= 1 and kmax >= 1 required");
+  SA_SUP(dtype == SA_BF16 && d == 128 && qtile == 128 && block == 128,
+         "prefill supports bf16, d == 128, qtile == block == 128");
+  return prefill_impl(q, k, v, idx, cnt, kmax, B, L, Hq, Hkv, scale, out, lse_out, as_stream(stream));
+}
+
+size_t sa_oracle_mass_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int qtile, int block) {
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || qtile < 1 || block < 1) return 0;
+  return mass_ws_bytes(B, L, Hq, Hkv, qtile, block);
+}
+
+sa_status_t sa_oracle_mass(const void* q, const void* k, int dtype, int B, int L, int Hq, int Hkv, int d, int qtile,
+                           int block, float scale, float* mass, void* workspace, size_t ws_bytes, void* stream) {
+  t_err.clear();
+  SA_TRY(check_common(dtype, B, Hq, Hkv, d));
+  SA_ARG(q && k && mass, "null pointer argument");
+  SA_ARG(L >= 1, "L >= 1 required");
+  SA_SUP(dtype == SA_BF16 && d == 128 && qtile == 128 && block == 128,
+         "oracle mass supports bf16, d == 128, qtile == block == 128");
+  const size_t need = mass_ws_bytes(B, L, Hq, Hkv, qtile, block);
+  SA_ARG(need == 0 || (workspace && ws_bytes >= need), "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  return mass_impl(q, k, B, L, Hq, Hkv, scale, mass, workspace, as_stream(stream));
+}
+
+size_t sa_decode_step_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int dtype, int kmax) {
+  const size_t dec = sa_decode_workspace_bytes(B, T, Hq, Hkv, d, kmax);
+  if (!dec || (dtype != SA_F32 && dtype != SA_BF16)) return 0;
+  const size_t es = static_cast<size_t>(esize(dtype));
+  const size_t qb = static_cast<size_t>(B) * T * Hq * d * es;
+  const size_t kb = static_cast<size_t>(B) * T * Hkv * d * es;
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  return up(dec) + 2 * up(qb) + 2 * up(kb);
+}
+
+sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, int dtype, void* k_cache,
+                           void* v_cache, float* sketch, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
+                           int block, int k, float scale, int32_t* idx, int32_t* cnt, int kmax, float* scores,
+                           void* out, int host_io, void* workspace, size_t ws_bytes, void* stream) {
+  t_err.clear();
+  SA_TRY(check_common(dtype, B, Hq, Hkv, d));
+  SA_ARG(q && k_new && v_new && out && workspace, "null pointer argument");
+  SA_ARG(L >= T && T >= 1, "need 1 <= T <= L");
+  const size_t need = sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax);
+  SA_ARG(need && ws_bytes >= need, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  cudaStream_t st = as_stream(stream);
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  const size_t es = static_cast<size_t>(esize(dtype));
+  const size_t dec = up(sa_decode_workspace_bytes(B, T, Hq, Hkv, d, kmax));
+  const size_t qb = static_cast<size_t>(B) * T * Hq * d * es;
+  const size_t kb = static_cast<size_t>(B) * T * Hkv * d * es;
+  char* w = static_cast<char*>(workspace);
+  const void* qd = q;
+  const void* knd = k_new;
+  const void* vnd = v_new;
+  void* outd = out;
+  if (host_io) {
+    void* q_dev = w + dec;
+    void* out_dev = w + dec + up(qb);
+    void* kn_dev = w + dec + 2 * up(qb);
+    void* vn_dev = w + dec + 2 * up(qb) + up(kb);
+    SA_CUDA(cudaMemcpyAsync(q_dev, q, qb, cudaMemcpyHostToDevice, st));
+    SA_CUDA(cudaMemcpyAsync(kn_dev, k_new, kb, cudaMemcpyHostToDevice, st));
+    SA_CUDA(cudaMemcpyAsync(vn_dev, v_new, kb, cudaMemcpyHostToDevice, st));
+    qd = q_dev;
+    knd = kn_dev;
+    vnd = vn_dev;
+    outd = out_dev;
+  }
+  SA_TRY(sa_append_kv(knd, vnd, dtype, B, Hkv, T, d, k_cache, v_cache, L_stride, L - T, block, sketch, stream));
+  SA_TRY(sa_select_topk(SA_SELECT_SKETCH, qd, dtype, sketch, scores, B, T, Hq, Hkv, d, L, L_stride, block, 0, 0, k,
+                        0, 1, scale, idx, cnt, kmax, stream));
+  SA_TRY(sa_decode(qd, k_cache, v_cache, dtype, idx, cnt, kmax, B, T, Hq, Hkv, d, L, L_stride, block, scale, outd, w,
+                   dec, stream));
+  if (host_io) SA_CUDA(cudaMemcpyAsync(out, outd, qb, cudaMemcpyDeviceToHost, st));
+  return SA_OK;
+}
+
+}  // extern "C"
