@@ -114,40 +114,62 @@ def decode_bytes(wl, cnt_np, L):
     return kv, sketch, append
 
 
-def oracle_decode_sample(wl, x, nbatch):
+def _sub_workload(wl, x, ngroups):
+    """The first `ngroups` (batch, kv-head) groups of the workload, as a smaller workload."""
+    if ngroups <= wl.Hkv:
+        sub = wl.replace(B=1, Hkv=ngroups, Hq=ngroups * wl.G)
+        return sub, x.q[:1, :, : ngroups * wl.G], x.k[:1, :ngroups], x.v[:1, :ngroups]
+    nbatch = ngroups // wl.Hkv
+    return wl.replace(B=nbatch), x.q[:nbatch], x.k[:nbatch], x.v[:nbatch]
+
+
+def oracle_decode_sample(wl, x, ngroups):
     """One CPU-oracle decode step (sketch -> score -> select -> attend) on the first
-    `nbatch` batch entries.  Returns (seconds, algorithmic bytes)."""
+    `ngroups` groups.  Returns (seconds, algorithmic bytes)."""
     import numpy as np
 
     import oracle
-    sub = wl.replace(B=nbatch)
-    q, k, v = x.q[:nbatch], x.k[:nbatch], x.v[:nbatch]
+    sub, q, k, v = _sub_workload(wl, x, ngroups)
     t0 = time.perf_counter()
     idx, cnt, _, _ = oracle.decode_select(q, k, sub)
-    rows = np.array([(b, t, h) for b in range(nbatch) for t in range(sub.T) for h in range(sub.Hq)])
+    rows = np.array([(b, t, h) for b in range(sub.B) for t in range(sub.T) for h in range(sub.Hq)])
     oracle.attend(q, k, v, sub.Hkv, sub.L, sub.L - sub.T, sub.Bk, sub.scale, rows, idx, cnt)
     dt = time.perf_counter() - t0
     kv, sk, ap = decode_bytes(sub, cnt, sub.L)
     return dt, kv + sk + ap
 
 
+def _sample_sizes(wl):
+    sizes = [1]
+    while sizes[-1] < wl.Hkv:
+        sizes.append(min(wl.Hkv, sizes[-1] * 2))
+    b = 2
+    while b <= wl.B:
+        sizes.append(b * wl.Hkv)
+        b *= 2
+    if sizes[-1] != wl.B * wl.Hkv:
+        sizes.append(wl.B * wl.Hkv)
+    return sizes
+
+
 def cpu_oracle_decode(wl, x, budget_s):
-    """Time the CPU oracle on a bounded sample (a prefix of the batch) for about budget_s seconds.
-    Returns (GB/s, cores, sample text)."""
+    """Time the CPU oracle on a bounded sample (the first groups of the batch) for about budget_s
+    seconds.  Returns (GB/s, cores, sample text)."""
     import oracle
-    dt, _ = oracle_decode_sample(wl, x, 1)
-    nbatch = 1
-    while nbatch < wl.B and dt * 2 < budget_s / 3:
-        nbatch = min(wl.B, nbatch * 2)
-        dt, _ = oracle_decode_sample(wl, x, nbatch)
+    ng = 1
+    dt, _ = oracle_decode_sample(wl, x, ng)
+    for cand in _sample_sizes(wl)[1:]:
+        if dt * cand / ng > budget_s / 3:
+            break
+        ng = cand
+        dt, _ = oracle_decode_sample(wl, x, ng)
     reps = max(1, int(budget_s // max(dt, 1e-3)))
     total_t, total_b = 0.0, 0
     for _ in range(reps):
-        t, b = oracle_decode_sample(wl, x, nbatch)
+        t, b = oracle_decode_sample(wl, x, ng)
         total_t += t
         total_b += b
-    sample = "%d of %d batch entries (%d of %d groups), full context %d, %d rep(s)" % (
-        nbatch, wl.B, nbatch * wl.Hkv, wl.B * wl.Hkv, wl.L, reps)
+    sample = "%d of %d groups, full context %d, %d rep(s)" % (ng, wl.B * wl.Hkv, wl.L, reps)
     return total_b / total_t / 1e9, oracle.threads(), sample
 
 
@@ -190,7 +212,7 @@ def bench_decode(args, wl, rank, world):
             idx=torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device=dev),
             cnt=torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device=dev),
             out=torch.empty_like(q0),
-            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=dev)))
+            ws=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)))
     del k0, v0
 
     def step(s):
@@ -208,20 +230,36 @@ def bench_decode(args, wl, rank, world):
     kv_b, sk_b, ap_b = decode_bytes(wl, cnt_np, wl.L)
     step_bytes = kv_b + sk_b + ap_b
 
-    # one CUDA graph per input set (the step is 4 kernels)
-    graphs = []
-    for r in range(R):
+    def capture(fns):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(sets[r])
-        graphs.append(g)
+            for f in fns:
+                f()
+        return g
+
+    def graph_us(g, calls, reps):
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda._sleep(20_000_000)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (calls * reps)
+
+    # the step as CUDA graphs: R consecutive steps over the R input sets
+    g_full = capture([lambda s=s: step(s) for s in sets])
+    K = args.steps
+    rem = K % R
+    g_rem = capture([lambda s=s: step(s) for s in sets[:rem]]) if rem else None
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
-            graphs[i % R].replay()
+        for _ in range(max(1, args.warmup // R)):
+            g_full.replay()
     torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps
-    K = args.steps
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -231,8 +269,10 @@ def bench_decode(args, wl, rank, world):
     with torch.cuda.stream(stream):
         torch.cuda._sleep(20_000_000)  # keep the device busy while the host queues the replays
         ev0.record(stream)
-        for i in range(K):
-            graphs[i % R].replay()
+        for _ in range(K // R):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
         ev1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -246,19 +286,23 @@ def bench_decode(args, wl, rank, world):
     ms_per_step = t_ms / K
     value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
 
-    # ---- dominant kernel pair (split-KV decode + merge) timed alone, CUDA events on its stream
-    nd = min(K, 3000)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nd)]
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(50_000_000)
-        for i in range(nd):
-            s = sets[i % R]
-            evs[i][0].record(stream)
-            sa.sa_decode(s["q"], s["kc"], s["vc"], s["idx"], s["cnt"], wl.L, wl.Bk, wl.scale, s["out"], s["ws"])
-            evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs[10:] if True) if nd > 20 else \
-        statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # ---- per-kernel times, each from a CUDA graph of 4*R back-to-back calls
+    def dec(s):
+        sa.sa_decode(s["q"], s["kc"], s["vc"], s["idx"], s["cnt"], wl.L, wl.Bk, wl.scale, s["out"], s["ws"])
+
+    def sel(s):
+        sa.sa_select_topk(sa.SA_SELECT_SKETCH, s["q"], s["sk"], None, wl.Hkv, wl.L, wl.L, wl.Bk, 0, False, wl.k, 0,
+                          1, wl.scale, s["idx"], s["cnt"])
+
+    def app(s):
+        sa.sa_append_kv(s["k_new"], s["v_new"], s["kc"], s["vc"], pos, wl.Bk, s["sk"])
+
+    reps = max(10, min(500, K // (4 * R)))
+    kern_us = {}
+    for name, fn in (("append", app), ("select", sel), ("decode", dec)):
+        g = capture([lambda s=s, fn=fn: fn(s) for s in sets * 4])
+        kern_us[name] = round(graph_us(g, 4 * R, reps), 3)
+    dec_ms = kern_us["decode"] * 1e-3
     dec_gbs = kv_b / (dec_ms * 1e-3) / 1e9
 
     # ---- end to end through the C ABI with pinned host buffers
@@ -301,14 +345,15 @@ def bench_decode(args, wl, rank, world):
         "config": {
             "workload": "%s decode: B=%d T=%d Hq=%d Hkv=%d d=%d L=%d block=%d top-k=%d + sink + local" % (
                 wl.name, wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, wl.L, wl.Bk, wl.k),
-            "step": "append+sketch refresh, score+top-k select, split-KV sparse decode (4 kernels, CUDA graph)",
+            "step": "append+sketch refresh, score+top-k select, split-KV sparse decode (CUDA graphs of %d steps)" % R,
             "bytes_per_step": {"selected_kv": kv_b, "sketch_scan": sk_b, "append": ap_b},
             "l2": "%d resident input sets rotated (%.1f GB of K/V); no step reuses L2 from the previous" % (
                 R, R * x.k.nbytes * 2 / 1e9),
         },
         "pct_hbm_peak": round(100 * value / peaks["hbm_gbs"], 2),
         "roofline": {
-            "kernel": "sa_decode (decode_split_kernel + decode_combine_kernel)",
+            "kernel": "sa_decode (decode_mma_kernel, one launch)" if bf and wl.G * wl.T <= 16 else
+                      "sa_decode (decode_split_kernel + decode_combine_kernel)",
             "bound": "hbm",
             "achieved": round(dec_gbs, 2),
             "peak": peaks["hbm_gbs"],
@@ -321,7 +366,8 @@ def bench_decode(args, wl, rank, world):
         },
         "e2e": {"value": round(step_bytes / t_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 4)},
-        "gpu_launches": 4 * K,
+        "kernels_us": kern_us,
+        "gpu_launches": K * (3 if bf and wl.G * wl.T <= 16 else 4),
         "clocks": clocks,
     }
     if rank == 0 and args.cpu_baseline:
@@ -357,22 +403,23 @@ def bench_reference(args, wl, rank, world):
     if rank != 0:
         return None
     x = synth.make_inputs(wl)
-    budget = max(0.005, 150.0 / max(1, args.steps + args.warmup))
-    dt, _ = oracle_decode_sample(wl, x, 1)
-    nbatch = 1
-    while nbatch < wl.B and dt * 2 <= budget:
-        nbatch = min(wl.B, nbatch * 2)
-        dt, _ = oracle_decode_sample(wl, x, nbatch)
+    budget = max(0.002, 150.0 / max(1, args.steps + args.warmup))
+    ng = 1
+    dt, _ = oracle_decode_sample(wl, x, ng)
+    for cand in _sample_sizes(wl)[1:]:
+        if dt * cand / ng > budget:
+            break
+        ng = cand
+        dt, _ = oracle_decode_sample(wl, x, ng)
     for _ in range(max(0, args.warmup - 1)):
-        oracle_decode_sample(wl, x, nbatch)
+        oracle_decode_sample(wl, x, ng)
     tot_t, tot_b = 0.0, 0
     for _ in range(args.steps):
-        t, b = oracle_decode_sample(wl, x, nbatch)
+        t, b = oracle_decode_sample(wl, x, ng)
         tot_t += t
         tot_b += b
     value = tot_b / tot_t / 1e9
-    sample = "%d of %d batch entries (%d of %d groups) per step, full context %d" % (
-        nbatch, wl.B, nbatch * wl.Hkv, wl.B * wl.Hkv, wl.L)
+    sample = "%d of %d groups per step, full context %d" % (ng, wl.B * wl.Hkv, wl.L)
     return {
         "impl": "reference",
         "metric": "sparse-attn decode KV GB/s (% HBM peak)",

@@ -159,7 +159,10 @@ int sa_select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num
  *   out[b,t,h] = sum_j softmax_j(scale * q[b,t,h] . k[g,j]) v[g,j]
  * over keys j in the blocks idx[g, 0:cnt[g]] with j < L and
  * j <= L - T + t.  workspace: >= sa_decode_workspace_bytes(...) bytes of
- * device memory, no initial contents needed, 16-byte aligned.
+ * device memory, 16-byte aligned, ZERO-FILLED before its first use (it holds
+ * per-group arrival counters; every call that completes leaves them zero, so
+ * a workspace is zeroed once, and again after a call that reported an error).
+ * Calls that share a workspace must not overlap on the device.
  * Requires d in {64, 128}; block == 64; G*T <= 32; T <= block;
  * 16-byte-aligned k/v caches.
  */
@@ -207,7 +210,9 @@ sa_status_t sa_oracle_mass(const void* q, const void* k, int dtype, int B, int L
  * area in `workspace`, runs, and copies `out` back, all on `stream`.
  * Otherwise they are device pointers.  sketch, caches, idx, cnt, scores
  * (optional) are device memory as above.  workspace: >=
- * sa_decode_step_workspace_bytes(...) bytes of device memory.
+ * sa_decode_step_workspace_bytes(...) bytes of device memory, zero-filled
+ * before first use exactly as for sa_decode (its head is sa_decode's
+ * workspace).
  */
 size_t sa_decode_step_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int dtype, int kmax);
 sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, int dtype,

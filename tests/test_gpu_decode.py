@@ -84,7 +84,7 @@ def _decode_gpu(sa, wl, x, idx_np, cnt_np, kmax):
     idx = torch.from_numpy(np.ascontiguousarray(idx_np.reshape(wl.B, wl.Hkv, 1, kmax))).cuda()
     cnt = torch.from_numpy(np.ascontiguousarray(cnt_np.reshape(wl.B, wl.Hkv, 1))).cuda()
     out = torch.empty_like(q)
-    ws = torch.empty(sa.sa_decode_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, kmax), dtype=torch.uint8,
+    ws = torch.zeros(sa.sa_decode_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, kmax), dtype=torch.uint8,
                      device="cuda")
     sa.sa_decode(q, k, v, idx, cnt, wl.L, wl.Bk, wl.scale, out, ws)
     torch.cuda.synchronize()
@@ -196,7 +196,7 @@ def test_decode_step_matches_oracle(sa, host_io):
     kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
     idx = torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device="cuda")
     cnt = torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device="cuda")
-    ws = torch.empty(sa.sa_decode_step_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, sa.SA_BF16, kmax),
+    ws = torch.zeros(sa.sa_decode_step_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, sa.SA_BF16, kmax),
                      dtype=torch.uint8, device="cuda")
     q = dev(x.q)
     k_new = kfull[:, :, pos:].permute(0, 2, 1, 3).contiguous()
@@ -212,3 +212,30 @@ def test_decode_step_matches_oracle(sa, host_io):
     assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s)
     ref, _ = oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, pos, wl.Bk, wl.scale, _all_rows(wl), o_idx, o_cnt)
     assert_close(host(out).reshape(ref.shape), ref, what="decode step")
+
+
+def test_workspace_reuse_keeps_counters_clean(sa):
+    """Back-to-back calls on one workspace (different selections) are each exact."""
+    wl = DECODE_CASES["c3"].replace(L=16384, k=20, needles=5)
+    x = synth.make_inputs(wl)
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
+    q, k, v = dev(x.q), dev(x.k), dev(x.v)
+    ws = torch.zeros(sa.sa_decode_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, kmax), dtype=torch.uint8,
+                     device="cuda")
+    o_idx, o_cnt, _, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax)
+    rng = np.random.default_rng(5)
+    alt = o_idx.copy()
+    for g in range(alt.shape[0]):  # a different valid selection: shuffle the non-forced blocks
+        alt[g, 1:-1] = np.sort(rng.choice(np.arange(1, wl.nb - 1), size=kmax - 2, replace=False))
+    rows = _all_rows(wl)
+    for sel in (o_idx, alt, o_idx):
+        idx = torch.from_numpy(np.ascontiguousarray(sel.reshape(wl.B, wl.Hkv, 1, kmax))).cuda()
+        cnt = torch.from_numpy(np.ascontiguousarray(o_cnt.reshape(wl.B, wl.Hkv, 1))).cuda()
+        out = torch.empty_like(q)
+        sa.sa_decode(q, k, v, idx, cnt, wl.L, wl.Bk, wl.scale, out, ws)
+        torch.cuda.synchronize()
+        _check_status(sa)
+        ref, _ = oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, wl.L - wl.T, wl.Bk, wl.scale, rows, sel, o_cnt)
+        assert_close(host(out).reshape(ref.shape), ref, what="reuse")
+    # the arrival counters at the head of the workspace are back to zero
+    assert int(ws[: 4 * wl.B * wl.Hkv].view(torch.int32).abs().sum()) == 0

@@ -270,30 +270,63 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(
 }
 
 // Merge the nsplit partials of each group (exact online-softmax combine).
-// grid (groups), 128 threads.
+// grid (groups), 128 threads; nsplit <= kmax <= 16384 is staged through
+// shared memory in chunks of 64 splits.
 template <typename TE, int D, int RMAX>
 __global__ void __launch_bounds__(kDecThreads) decode_combine_kernel(const float* __restrict__ ws_o,
                                                                      const float* __restrict__ ws_ml, int nsplit,
                                                                      int T, int Hq, int Hkv, TE* __restrict__ out) {
+  constexpr int CH = 64;
+  __shared__ float Ms[RMAX], dens[RMAX], wgt[CH * RMAX];
   const int g = blockIdx.x;
   const int G = Hq / Hkv, R = G * T;
   const int b = g / Hkv, kvh = g % Hkv;
+  const size_t base = static_cast<size_t>(g) * nsplit;
+  if (threadIdx.x < R) {
+    const int r = threadIdx.x;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ws_ml[((base + s) * RMAX + r) * 2]);
+    const float mu = (M == -INFINITY) ? 0.f : M;
+    float den = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const size_t pr = (base + s) * RMAX + r;
+      den = fmaf(ws_ml[pr * 2 + 1], exp2f(ws_ml[pr * 2] - mu), den);
+    }
+    Ms[r] = mu;
+    dens[r] = den > 0.f ? 1.f / den : 0.f;
+  }
+  __syncthreads();
   constexpr int DSPLIT = kDecThreads / D;
   const int dcol = threadIdx.x % D, rsub = threadIdx.x / D;
-  for (int r = rsub; r < R; r += DSPLIT) {
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ws_ml[((static_cast<size_t>(g) * nsplit + s) * RMAX + r) * 2]);
-    const float mu = (M == -INFINITY) ? 0.f : M;
-    float num = 0.f, den = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const size_t part = (static_cast<size_t>(g) * nsplit + s) * RMAX + r;
-      const float w = exp2f(ws_ml[part * 2] - mu);
-      den = fmaf(ws_ml[part * 2 + 1], w, den);
-      num = fmaf(ws_o[part * D + dcol], w, num);
+  float num[RMAX / DSPLIT];
+#pragma unroll
+  for (int k = 0; k < RMAX / DSPLIT; ++k) num[k] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += CH) {
+    const int ns = min(CH, nsplit - s0);
+    for (int i = threadIdx.x; i < ns * R; i += kDecThreads) {
+      const int s = i / R, r = i % R;
+      wgt[s * RMAX + r] = exp2f(ws_ml[((base + s0 + s) * RMAX + r) * 2] - Ms[r]);
     }
-    const float o = den > 0.f ? num / den : 0.f;
-    const int t = r / G, h = kvh * G + r % G;
-    out[((static_cast<size_t>(b) * T + t) * Hq + h) * D + dcol] = static_cast<TE>(o);
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < RMAX / DSPLIT; ++k) {
+      const int r = rsub + DSPLIT * k;
+      if (r < R) {
+        float a = num[k];
+#pragma unroll 4
+        for (int s = 0; s < ns; ++s) a = fmaf(ws_o[((base + s0 + s) * RMAX + r) * D + dcol], wgt[s * RMAX + r], a);
+        num[k] = a;
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < RMAX / DSPLIT; ++k) {
+    const int r = rsub + DSPLIT * k;
+    if (r < R) {
+      const int t = r / G, h = kvh * G + r % G;
+      out[((static_cast<size_t>(b) * T + t) * Hq + h) * D + dcol] = static_cast<TE>(num[k] * dens[r]);
+    }
   }
 }
 

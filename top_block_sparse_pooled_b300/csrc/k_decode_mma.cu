@@ -1,0 +1,399 @@
+// k_decode_mma.cu -- bf16 sparse decode over the selected blocks, tensor-core
+// tile math, HBM-streaming design.
+//
+// "How Much Dense Attention is Necessary?" Sec. 2.1: exact attention with the
+// original q, k, v on the selected support only.  "Faster Than Flash" Sec. 3:
+// only the selected blocks are read from HBM.  "Pulsar Attention" Phase 2:
+// partial softmaxes over disjoint key sets merge exactly (online softmax).
+//
+// Work split: the (group, selected-block) units of all groups are laid end to
+// end and cut into equal contiguous ranges, one per CTA (about two CTAs per
+// SM), so every SM streams the same number of blocks whatever the group
+// count.  A CTA whose range spans several groups emits one partial per group;
+// the partial of (CTA c, group g) is stored at slot c + g (the pieces of two
+// interleaved partitions of a line, counted in order).  The CTA that brings a
+// group's arrival counter to its CTA count merges that group's partials and
+// writes the output, so the whole decode is one launch.
+//
+// Per CTA: warp 4 is the TMA producer (K and V tiles of a block, 64 rows each,
+// 128B-swizzled, into a ring of stages guarded by full/empty mbarriers);
+// warps 0-3 each own 16 of the block's 64 keys and keep their own online
+// softmax state for the group's G*T (<= 16) query rows, so consumers never
+// synchronize per block.  QK^T and PV use mma.m16n8k16 (bf16 in, fp32
+// accumulate) with ldmatrix straight from the swizzled tiles; P stays in
+// registers (the QK accumulator fragment is the PV A fragment).  At the end of
+// a group's range the four warp states merge through shared memory.
+#pragma once
+
+#include "sa_ptx.cuh"
+
+namespace sa {
+
+constexpr int kDmConsumers = 4;
+constexpr int kDmThreads = (kDmConsumers + 1) * 32;
+constexpr int kDmBk = 64;
+constexpr int kDmMaxList = 1024;
+
+template <int D>
+struct DmCfg {
+  static constexpr int ROWB = D * 2;
+  static constexpr int TILEB = kDmBk * ROWB;
+  static constexpr int STAGEB = 2 * TILEB;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int NT = D / 8;
+};
+
+// Shared-memory layout (runtime, from a 1024-aligned base).
+struct DmLayout {
+  int nstages, R, D, per;
+  __host__ __device__ int stage_off(int s) const { return s * 2 * kDmBk * D * 2; }
+  __host__ __device__ int merge_off() const { return nstages * 2 * kDmBk * D * 2; }
+  __host__ __device__ int merge_bytes() const { return kDmConsumers * R * (D + 2) * 4; }
+  __host__ __device__ int list_off() const { return merge_off() + merge_bytes(); }
+  __host__ __device__ int bar_off() const { return list_off() + ((per * 8 + 15) / 16) * 16; }
+  __host__ __device__ int bytes() const { return bar_off() + 2 * nstages * 8 + 1024; }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// c += a * b, m16n8k16, bf16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// address of 16-byte chunk `chunk` of row `row` in a 64-row, 128B-swizzled tile
+__device__ __forceinline__ uint32_t swz_chunk(uint32_t tile, int row, int chunk) {
+  return tile + (chunk >> 3) * (kDmBk * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+struct DmParams {
+  const __nv_bfloat16* q;
+  const int32_t* idx;
+  const int32_t* cnt;
+  int kmax, T, Hq, Hkv, L, Ls, R;
+  float qscale;
+  int per, U;
+  float* part_o;   // [slots][R][D] (unnormalized numerators)
+  float* part_ml;  // [slots][R][2] (max in base-2 units, denominator)
+  int* ctr;        // [groups] arrival counters: zero on entry, left zero on exit
+  int nctas;
+  __nv_bfloat16* out;
+  DmLayout lay;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDmThreads, 2) decode_mma_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                   const __grid_constant__ CUtensorMap vmap,
+                                                                   const DmParams p) {
+  using C = DmCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_dm[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dm) + 1023) & ~uintptr_t(1023));
+  const DmLayout& lay = p.lay;
+  const int NS = lay.nstages;
+  int2* list = reinterpret_cast<int2*>(smem + lay.list_off());
+  float* mw = reinterpret_cast<float*>(smem + lay.merge_off());  // [4][R]
+  float* lw = mw + kDmConsumers * p.R;                            // [4][R]
+  float* ow = lw + kDmConsumers * p.R;                            // [4][R][D]
+  const uint32_t full0 = smem_u32(smem + lay.bar_off());
+  const uint32_t empty0 = full0 + 8 * NS;
+  const uint32_t sbase = smem_u32(smem);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = blockIdx.x;
+  const int u0 = c * p.per;
+  const int nu = min(p.per, p.U - u0);
+  const int G = p.Hq / p.Hkv;
+
+  // unit list: (group, block id or -1 when the unit is past the group's count)
+  for (int i = tid; i < nu; i += kDmThreads) {
+    const int u = u0 + i;
+    const int g = u / p.kmax, s = u % p.kmax;
+    const int n = min(p.cnt[g], p.kmax);
+    int blk = -1;
+    if (s < n) {
+      blk = p.idx[static_cast<size_t>(g) * p.kmax + s];
+      if (blk < 0 || blk * kDmBk >= p.L) blk = -1;
+    }
+    list[i] = make_int2(g, blk);
+  }
+  if (tid == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kDmConsumers);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kDmConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int vi = 0;
+      bool ok = true;
+      for (int i = 0; i < nu && ok; ++i) {
+        const int2 e = list[i];
+        if (e.y < 0) continue;
+        const int st = vi % NS;
+        if (vi >= NS) ok = mbar_wait(empty0 + 8 * st, ((vi / NS) - 1) & 1);
+        if (!ok) break;
+        const uint32_t full = full0 + 8 * st;
+        mbar_arrive_expect_tx(full, C::STAGEB);
+        const uint32_t kt = sbase + lay.stage_off(st);
+        const int row = e.x * p.Ls + e.y * kDmBk;
+#pragma unroll
+        for (int bx = 0; bx < C::ROWB / 128; ++bx) {
+          tma_g2s_2d(kt + bx * kDmBk * 128, &kmap, bx * 64, row, full);
+          tma_g2s_2d(kt + C::TILEB + bx * kDmBk * 128, &vmap, bx * 64, row, full);
+        }
+        ++vi;
+      }
+      // never leave with copies in flight: wait for the last fill of every used stage
+      for (int k = max(0, vi - NS); k < vi; ++k) mbar_wait_drain(full0 + 8 * (k % NS), (k / NS) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
+  const int kb = warp * 16;                  // this warp's keys within the block
+  uint32_t qa[C::KSTEPS][4];
+  float o[C::NT][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int lim0 = -1, lim1 = -1;  // last visible key position of rows gq and gq + 8 (-1: no row)
+  bool dead = false;
+
+  auto start_group = [&](int g) {
+    const int b = g / p.Hkv, kvh = g % p.Hkv;
+    const int r0 = gq, r1 = gq + 8;
+    const __nv_bfloat16* q0 = nullptr;
+    const __nv_bfloat16* q1 = nullptr;
+    lim0 = lim1 = -1;
+    if (r0 < p.R) {
+      q0 = p.q + ((static_cast<size_t>(b) * p.T + r0 / G) * p.Hq + kvh * G + r0 % G) * D;
+      lim0 = p.L - p.T + r0 / G;
+    }
+    if (r1 < p.R) {
+      q1 = p.q + ((static_cast<size_t>(b) * p.T + r1 / G) * p.Hq + kvh * G + r1 % G) * D;
+      lim1 = p.L - p.T + r1 / G;
+    }
+#pragma unroll
+    for (int kk = 0; kk < C::KSTEPS; ++kk) {
+      const int col = kk * 16 + 2 * tq;
+      qa[kk][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col) : 0u;
+      qa[kk][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col) : 0u;
+      qa[kk][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col + 8) : 0u;
+      qa[kk][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col + 8) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < C::NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  };
+
+  auto finish_group = [&](int g) {
+    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+    const int r0 = gq, r1 = gq + 8;
+    if (tq == 0) {
+      if (r0 < p.R) {
+        mw[warp * p.R + r0] = m0;
+        lw[warp * p.R + r0] = l0;
+      }
+      if (r1 < p.R) {
+        mw[warp * p.R + r1] = m1;
+        lw[warp * p.R + r1] = l1;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < C::NT; ++j) {
+      const int col = j * 8 + 2 * tq;
+      if (r0 < p.R) *reinterpret_cast<float2*>(ow + (warp * p.R + r0) * D + col) = make_float2(o[j][0], o[j][1]);
+      if (r1 < p.R) *reinterpret_cast<float2*>(ow + (warp * p.R + r1) * D + col) = make_float2(o[j][2], o[j][3]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+    const size_t slot = static_cast<size_t>(c) + g;
+    for (int i = tid; i < p.R * D; i += kDmConsumers * 32) {
+      const int r = i / D, dd = i % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDmConsumers; ++w) M = fmaxf(M, mw[w * p.R + r]);
+      const float mu = (M == -INFINITY) ? 0.f : M;
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDmConsumers; ++w) {
+        const float wt = exp2f(mw[w * p.R + r] - mu);
+        num = fmaf(ow[(w * p.R + r) * D + dd], wt, num);
+        den = fmaf(lw[w * p.R + r], wt, den);
+      }
+      p.part_o[(slot * p.R + r) * D + dd] = num;
+      if (dd == 0) {
+        p.part_ml[(slot * p.R + r) * 2] = M;
+        p.part_ml[(slot * p.R + r) * 2 + 1] = den;
+      }
+    }
+    // The CTA that completes group g merges its partials (no waiting: the
+    // others just leave).  Writers: stores, fence, count.  Last: count, fence,
+    // loads from L2.
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+    const int cf = (g * p.kmax) / p.per;
+    const int cl = min(p.nctas - 1, ((g + 1) * p.kmax - 1) / p.per);
+    const int np = cl - cf + 1;
+    if (tid == 0) {
+      const int old = atomicAdd(p.ctr + g, 1);
+      lw[0] = (old == np - 1) ? 1.f : 0.f;  // merge buffer is free here; reuse one word as the flag
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+    const bool last = lw[0] != 0.f;
+    asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+    if (last) {
+      __threadfence();
+      // row max and 1/denominator into mw[r], lw[r]
+      if (tid < p.R) {
+        const int r = tid;
+        float M = -INFINITY;
+        for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(p.part_ml + ((static_cast<size_t>(cf + k) + g) * p.R + r) * 2));
+        const float mu = (M == -INFINITY) ? 0.f : M;
+        float den = 0.f;
+        for (int k = 0; k < np; ++k) {
+          const size_t sl = (static_cast<size_t>(cf + k) + g) * p.R + r;
+          den = fmaf(__ldcg(p.part_ml + sl * 2 + 1), exp2f(__ldcg(p.part_ml + sl * 2) - mu), den);
+        }
+        mw[r] = mu;
+        lw[r] = den > 0.f ? 1.f / den : 0.f;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+      const int b = g / p.Hkv, kvh = g % p.Hkv;
+      for (int i = tid; i < p.R * D; i += kDmConsumers * 32) {
+        const int r = i / D, dd = i % D;
+        const float mu = mw[r];
+        float num = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < np; ++k) {
+          const size_t sl = (static_cast<size_t>(cf + k) + g) * p.R + r;
+          num = fmaf(__ldcg(p.part_o + sl * D + dd), exp2f(__ldcg(p.part_ml + sl * 2) - mu), num);
+        }
+        const int t = r / G, h = kvh * G + r % G;
+        p.out[((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * D + dd] = __float2bfloat16_rn(num * lw[r]);
+      }
+      if (tid == 0) p.ctr[g] = 0;  // ready for the next call on this workspace
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+  };
+
+  int vi = 0, cur = -1;
+  for (int i = 0; i < nu; ++i) {
+    const int2 e = list[i];
+    if (e.x != cur) {
+      if (cur >= 0) finish_group(cur);
+      start_group(e.x);
+      cur = e.x;
+    }
+    if (e.y < 0) continue;
+    const int st = vi % NS;
+    const uint32_t full = full0 + 8 * st;
+    if (!dead) dead = !mbar_wait(full, (vi / NS) & 1);
+    ++vi;
+    if (dead) continue;
+    const uint32_t kt = sbase + lay.stage_off(st);
+    const uint32_t vt = kt + C::TILEB;
+
+    // S = Q K^T for this warp's 16 keys (two n-tiles of 8)
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const int key = kb + (mi >> 1) * 8 + ri;
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(swz_chunk(kt, key, 2 * kk + (mi & 1)), b00, b01, b10, b11);
+        mma_bf16(s[0], qa[kk], b00, b01);
+        mma_bf16(s[1], qa[kk], b10, b11);
+      }
+    }
+    __syncwarp();
+    // scale, causal / validity mask, online softmax (base 2)
+    const int base = e.y * kDmBk + kb + 2 * tq;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int key = base + nt * 8 + (x & 1);
+        const int lim = (x < 2) ? lim0 : lim1;
+        s[nt][x] = (key <= lim) ? s[nt][x] * p.qscale : -INFINITY;
+      }
+    float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+    const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float c0 = exp2f(m0 - mu0), c1 = exp2f(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - mu0);
+      s[nt][1] = exp2f(s[nt][1] - mu0);
+      s[nt][2] = exp2f(s[nt][2] - mu1);
+      s[nt][3] = exp2f(s[nt][3] - mu1);
+    }
+    l0 = l0 * c0 + (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
+    l1 = l1 * c1 + (s[0][2] + s[0][3]) + (s[1][2] + s[1][3]);
+    uint32_t pa[4];
+    pa[0] = pack_bf16(s[0][0], s[0][1]);
+    pa[1] = pack_bf16(s[0][2], s[0][3]);
+    pa[2] = pack_bf16(s[1][0], s[1][1]);
+    pa[3] = pack_bf16(s[1][2], s[1][3]);
+#pragma unroll
+    for (int j = 0; j < C::NT; ++j) {
+      o[j][0] *= c0;
+      o[j][1] *= c0;
+      o[j][2] *= c1;
+      o[j][3] *= c1;
+    }
+    // O += P V for this warp's 16 keys
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const int key = kb + (mi & 1) * 8 + ri;
+#pragma unroll
+      for (int jj = 0; jj < C::NT / 2; ++jj) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(swz_chunk(vt, key, 2 * jj + (mi >> 1)), v0, v1, v2, v3);
+        mma_bf16(o[2 * jj], pa, v0, v1);
+        mma_bf16(o[2 * jj + 1], pa, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+  }
+  if (cur >= 0) finish_group(cur);
+}
+
+}  // namespace sa

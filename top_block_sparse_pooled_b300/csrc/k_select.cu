@@ -66,10 +66,17 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += kSelThreads) S.hist[i] = 0;
       __syncthreads();
-      for (int b = tid; b < n; b += kSelThreads) {
-        if (b == 0 || b == f1) continue;
-        const uint32_t key = float_key(sc[b]);
-        if ((key & mask) == prefix) atomicAdd(&S.hist[(key >> shift) & 255u], 1u);
+      // warp-aggregated histogram: lanes with equal digits add once (the top
+      // digits of similar scores coincide, so plain atomics would serialize)
+      for (int base = 0; base < n; base += kSelThreads) {
+        const int b = base + tid;
+        uint32_t bin = 256u + (tid & 31);  // unique sentinel: no peers
+        if (b < n && b != 0 && b != f1) {
+          const uint32_t key = float_key(sc[b]);
+          if ((key & mask) == prefix) bin = (key >> shift) & 255u;
+        }
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+        if (bin < 256u && (tid & 31) == (__ffs(peers) - 1)) atomicAdd(&S.hist[bin], __popc(peers));
       }
       __syncthreads();
       if (tid < 32) {
@@ -189,8 +196,8 @@ struct SelDecodeSmem {
 template <typename TE, int D, int RMAX>
 __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
     const __grid_constant__ CUtensorMap sk_map, const TE* __restrict__ q, int T, int Hq, int Hkv, int nb,
-    int nb_cap, float scale, int per, int k, float* __restrict__ scores_out, int32_t* __restrict__ idx,
-    int32_t* __restrict__ cnt, int kmax) {
+    int nb_cap, float scale, int per, int tile_rows, int k, float* __restrict__ scores_out,
+    int32_t* __restrict__ idx, int32_t* __restrict__ cnt, int kmax) {
   using SM = SelDecodeSmem<D, RMAX>;
   extern __shared__ __align__(1024) uint8_t smem_sel_dec[];
   uint8_t* smem_raw = smem_sel_dec;
@@ -226,25 +233,28 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
 
   bool ok = true;
   uint32_t phase = 0;
-  for (int t0 = b0; t0 < b1; t0 += kSelTileRows) {
+  // tile_rows (a multiple of 8, <= kSelTileRows) is the TMA box height: the
+  // CTA's range is fetched without over-reading the next group's sketch
+  const uint32_t tile_bytes = static_cast<uint32_t>(SM::kBoxes * tile_rows * 128);
+  for (int t0 = b0; t0 < b1; t0 += tile_rows) {
     if (tid == 0) {
-      mbar_arrive_expect_tx(bar, SM::kTileBytes);
+      mbar_arrive_expect_tx(bar, tile_bytes);
 #pragma unroll
       for (int bx = 0; bx < SM::kBoxes; ++bx)
-        tma_g2s_2d(smem_u32(smem + bx * kSelTileRows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
+        tma_g2s_2d(smem_u32(smem + bx * tile_rows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
     }
     ok = mbar_wait(bar, phase);
     phase ^= 1;
     if (__syncthreads_or(!ok)) break;
     const int row = t0 + tid;
-    if (row < b1) {
+    if (tid < tile_rows && row < b1) {
       float acc[RMAX];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
 #pragma unroll 4
       for (int c = 0; c < D / 4; ++c) {
         const int bx = c >> 3, cc = c & 7;
-        const float4 kv = *reinterpret_cast<const float4*>(smem + bx * kSelTileRows * 128 + tid * 128 +
+        const float4 kv = *reinterpret_cast<const float4*>(smem + bx * tile_rows * 128 + tid * 128 +
                                                            ((cc ^ (tid & 7)) << 4));
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {

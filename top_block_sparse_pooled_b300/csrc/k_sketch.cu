@@ -73,15 +73,16 @@ __device__ __forceinline__ void block_mean_rows(const TE* __restrict__ rows, int
 }
 
 // grid (nb, groups): one CTA per (group, block).
+// The sketch's group stride is nb_cap = ceil(Ls / Bk) blocks (the cache capacity).
 template <typename TE, int D>
 __global__ void __launch_bounds__(kSketchThreads) build_sketch_kernel(const TE* __restrict__ k, int L, int Ls,
-                                                                      int Bk, float* __restrict__ sketch) {
+                                                                      int Bk, int nb_cap, float* __restrict__ sketch) {
   __shared__ __align__(16) float red[kSketchThreads * 8];
-  const int blk = blockIdx.x, g = blockIdx.y, nb = gridDim.x;
+  const int blk = blockIdx.x, g = blockIdx.y;
   const int j0 = blk * Bk;
   const int j1 = min(j0 + Bk, L);
   block_mean_rows<TE, D>(k + (static_cast<size_t>(g) * Ls + j0) * D, j1 - j0,
-                         sketch + (static_cast<size_t>(g) * nb + blk) * D, red);
+                         sketch + (static_cast<size_t>(g) * nb_cap + blk) * D, red);
 }
 
 // grid (groups): copy T new rows of K and V into the cache, then rewrite the

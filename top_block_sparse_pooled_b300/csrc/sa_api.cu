@@ -14,6 +14,7 @@
 #include "sparse_attn.h"
 
 #include "k_decode.cu"
+#include "k_decode_mma.cu"
 #include "k_select.cu"
 #include "k_sketch.cu"
 
@@ -145,13 +146,14 @@ template <typename TE>
 sa_status_t launch_build_sketch(const void* k, int groups, int L, int Ls, int d, int block, float* sketch,
                                 cudaStream_t st) {
   const int nb = cdiv(L, block);
+  const int nb_cap = cdiv(Ls, block);
   const dim3 grid(nb, groups);
   if (d == 128)
     sa::build_sketch_kernel<TE, 128><<<grid, sa::kSketchThreads, 0, st>>>(static_cast<const TE*>(k), L, Ls, block,
-                                                                           sketch);
+                                                                           nb_cap, sketch);
   else
     sa::build_sketch_kernel<TE, 64><<<grid, sa::kSketchThreads, 0, st>>>(static_cast<const TE*>(k), L, Ls, block,
-                                                                          sketch);
+                                                                          nb_cap, sketch);
   SA_CUDA(cudaGetLastError());
   return SA_OK;
 }
@@ -228,9 +230,10 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
   cs = std::min(cs, nb);
   const int per = cdiv(nb, cs);
   cs = cdiv(nb, per);
+  const int tile_rows = std::min(sa::kSelTileRows, cdiv(per, 8) * 8);
   CUtensorMap map;
   SA_TRY(make_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.sketch, D, static_cast<uint64_t>(groups) * nb_cap,
-                     D * 4, 32, sa::kSelTileRows, CU_TENSOR_MAP_SWIZZLE_128B));
+                     D * 4, 32, tile_rows, CU_TENSOR_MAP_SWIZZLE_128B));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, groups);
   cfg.blockDim = dim3(sa::kSelThreads);
@@ -244,7 +247,7 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   SA_CUDA(cudaLaunchKernelEx(&cfg, kern, map, static_cast<const TE*>(a.q), a.Tq, a.Hq, a.Hkv, nb, nb_cap, a.scale,
-                             per, a.k, a.scores, a.idx, a.cnt, a.kmax));
+                             per, tile_rows, a.k, a.scores, a.idx, a.cnt, a.kmax));
   return SA_OK;
 }
 
@@ -315,10 +318,68 @@ struct DecodeArgs {
 };
 
 size_t decode_ws_bytes(int groups, int R, int d, int kmax) {
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  // CUDA-core path: [groups][nsplit <= kmax][RMAX] partials
   const size_t rm = static_cast<size_t>(rmax_for(R));
-  const size_t o = static_cast<size_t>(groups) * kmax * rm * d * 4;
-  const size_t ml = static_cast<size_t>(groups) * kmax * rm * 2 * 4;
-  return ((o + 255) / 256) * 256 + ((ml + 255) / 256) * 256;
+  const size_t v1 = up(static_cast<size_t>(groups) * kmax * rm * d * 4) + up(static_cast<size_t>(groups) * kmax * rm * 8);
+  // tensor-core path: arrival counters, then (CTAs + groups) <= groups * (kmax + 1)
+  // partial slots of R rows
+  const size_t slots = static_cast<size_t>(groups) * (kmax + 1);
+  const size_t v2 = up(static_cast<size_t>(groups) * 4) + up(slots * R * d * 4) + up(slots * R * 8);
+  return v1 > v2 ? v1 : v2;
+}
+
+template <int D>
+sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream_t st) {
+  using Cfg = sa::DmCfg<D>;
+  const int groups = a.B * a.Hkv;
+  const int R = (a.Hq / a.Hkv) * a.T;
+  const long long U = static_cast<long long>(groups) * a.kmax;
+  SA_ARG(U < (1LL << 31), "too many (group, block) units");
+  // two CTAs per SM; equal contiguous ranges of units
+  const long long target = 2LL * di.sms;
+  long long per = (U + target - 1) / target;
+  per = std::min<long long>(std::max<long long>(per, 1), sa::kDmMaxList);
+  const int nctas = static_cast<int>((U + per - 1) / per);
+  sa::DmLayout lay{2, R, D, static_cast<int>(per)};
+  const int budget = 113 * 1024;  // two CTAs in the 228 KB of shared memory per SM
+  const int fixed = lay.bytes() - 2 * Cfg::STAGEB;
+  lay.nstages = std::max(2, std::min(6, (budget - fixed) / Cfg::STAGEB));
+  const int smem = lay.bytes();
+  auto kern = sa::decode_mma_kernel<D>;
+  SA_TRY(set_smem(kern, smem));
+  const size_t slots = static_cast<size_t>(nctas) + groups;
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  sa::DmParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.idx = a.idx;
+  p.cnt = a.cnt;
+  p.kmax = a.kmax;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.L = a.L;
+  p.Ls = a.Ls;
+  p.R = R;
+  p.qscale = a.scale * 1.4426950408889634f;
+  p.per = static_cast<int>(per);
+  p.U = static_cast<int>(U);
+  char* w = static_cast<char*>(a.ws);
+  p.ctr = reinterpret_cast<int*>(w);
+  p.part_o = reinterpret_cast<float*>(w + up(static_cast<size_t>(groups) * 4));
+  p.part_ml = reinterpret_cast<float*>(w + up(static_cast<size_t>(groups) * 4) + up(slots * R * D * 4));
+  p.nctas = nctas;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lay = lay;
+  CUtensorMap km, vm;
+  const uint64_t rows = static_cast<uint64_t>(groups) * a.Ls;
+  SA_TRY(make_map_2d(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kc, D, rows, D * 2, 64, sa::kDmBk,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  SA_TRY(make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.vc, D, rows, D * 2, 64, sa::kDmBk,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  kern<<<nctas, sa::kDmThreads, smem, st>>>(km, vm, p);
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
 }
 
 template <typename TE, int D, int RMAX>
@@ -369,6 +430,8 @@ sa_status_t dispatch_decode_r(const DecodeArgs& a, const DevInfo& di, cudaStream
 sa_status_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   DevInfo di;
   SA_TRY(dev_info(&di));
+  if (a.dtype == SA_BF16 && (a.Hq / a.Hkv) * a.T <= 16)
+    return a.d == 128 ? launch_decode_mma<128>(a, di, st) : launch_decode_mma<64>(a, di, st);
   if (a.dtype == SA_F32)
     return a.d == 128 ? dispatch_decode_r<float, 128>(a, di, st) : dispatch_decode_r<float, 64>(a, di, st);
   return a.d == 128 ? dispatch_decode_r<__nv_bfloat16, 128>(a, di, st) : dispatch_decode_r<__nv_bfloat16, 64>(a, di, st);

@@ -67,17 +67,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false (and records SA_ERR_TIMEOUT) on give-up.
+// kWaitLimitNs.  Returns false (and records SA_ERR_TIMEOUT) on give-up.  Once
+// any wait in any kernel has given up (status word set), later waits return
+// false at once instead of spinning out their own limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&g_device_status) != 0) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       record_error(kErrTimeout);
       return false;
     }
   }
+}
+
+// Bounded wait used before a thread exits, so that no copy it issued is still
+// landing in shared memory; it does not stop early on a recorded error.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(kErrTimeout);
+      return false;
+    }
+  }
+  return true;
 }
 
 // ------------------------------------------------------------- bulk copies
