@@ -33,6 +33,7 @@ constexpr int kDmConsumers = 4;
 constexpr int kDmThreads = (kDmConsumers + 1) * 32;
 constexpr int kDmBk = 64;
 constexpr int kDmMaxList = 1024;
+constexpr int kDmMaxParts = 64;  // partials per group (CTAs touching one group)
 
 template <int D>
 struct DmCfg {
@@ -48,7 +49,11 @@ struct DmLayout {
   int nstages, R, D, per;
   __host__ __device__ int stage_off(int s) const { return s * 2 * kDmBk * D * 2; }
   __host__ __device__ int merge_off() const { return nstages * 2 * kDmBk * D * 2; }
-  __host__ __device__ int merge_bytes() const { return kDmConsumers * R * (D + 2) * 4; }
+  __host__ __device__ int merge_bytes() const {
+    const int warps = kDmConsumers * R * (D + 2) * 4;  // per-warp states
+    const int parts = (8 + 2 * kDmMaxParts) * R * 4;  // mw, lw, then staged partial maxima / denominators
+    return warps > parts ? warps : parts;
+  }
   __host__ __device__ int list_off() const { return merge_off() + merge_bytes(); }
   __host__ __device__ int bar_off() const { return list_off() + ((per * 8 + 15) / 16) * 16; }
   __host__ __device__ int bytes() const { return bar_off() + 2 * nstages * 8 + 1024; }
@@ -271,33 +276,74 @@ __global__ void __launch_bounds__(kDmThreads, 2) decode_mma_kernel(const __grid_
     asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
     if (last) {
       __threadfence();
-      // row max and 1/denominator into mw[r], lw[r]
+      // stage every partial's (max, denominator) per row; np <= kDmMaxParts
+      float* pm = ow;                          // [np][R] maxima, then weights
+      float* pl = ow + kDmMaxParts * p.R;      // [np][R] denominators
+      for (int i = tid; i < np * p.R; i += kDmConsumers * 32) {
+        const int k = i / p.R, r = i % p.R;
+        const size_t sl = (static_cast<size_t>(cf + k) + g) * p.R + r;
+        pm[i] = __ldcg(p.part_ml + sl * 2);
+        pl[i] = __ldcg(p.part_ml + sl * 2 + 1);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
       if (tid < p.R) {
-        const int r = tid;
         float M = -INFINITY;
-        for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(p.part_ml + ((static_cast<size_t>(cf + k) + g) * p.R + r) * 2));
+        for (int k = 0; k < np; ++k) M = fmaxf(M, pm[k * p.R + tid]);
         const float mu = (M == -INFINITY) ? 0.f : M;
         float den = 0.f;
         for (int k = 0; k < np; ++k) {
-          const size_t sl = (static_cast<size_t>(cf + k) + g) * p.R + r;
-          den = fmaf(__ldcg(p.part_ml + sl * 2 + 1), exp2f(__ldcg(p.part_ml + sl * 2) - mu), den);
+          const float w = exp2f(pm[k * p.R + tid] - mu);
+          pm[k * p.R + tid] = w;
+          den = fmaf(pl[k * p.R + tid], w, den);
         }
-        mw[r] = mu;
-        lw[r] = den > 0.f ? 1.f / den : 0.f;
+        lw[tid] = den > 0.f ? 1.f / den : 0.f;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+      // out[r, d:d+4] = sum_k w[k, r] * part_o[k, r, d:d+4] / den[r]; up to 4 float4 slots per thread,
+      // all of a partial's loads issued together
       const int b = g / p.Hkv, kvh = g % p.Hkv;
-      for (int i = tid; i < p.R * D; i += kDmConsumers * 32) {
-        const int r = i / D, dd = i % D;
-        const float mu = mw[r];
-        float num = 0.f;
-#pragma unroll 4
-        for (int k = 0; k < np; ++k) {
-          const size_t sl = (static_cast<size_t>(cf + k) + g) * p.R + r;
-          num = fmaf(__ldcg(p.part_o + sl * D + dd), exp2f(__ldcg(p.part_ml + sl * 2) - mu), num);
+      const int nq4 = p.R * D / 4;
+      for (int j0 = tid; j0 < nq4; j0 += 4 * kDmConsumers * 32) {
+        float4 acc[4];
+        int rr[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          rr[j] = (j0 + j * kDmConsumers * 32) * 4 / D;
         }
-        const int t = r / G, h = kvh * G + r % G;
-        p.out[((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * D + dd] = __float2bfloat16_rn(num * lw[r]);
+#pragma unroll 2
+        for (int k = 0; k < np; ++k) {
+          const size_t sl0 = (static_cast<size_t>(cf + k) + g) * p.R;
+          float4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int q4 = j0 + j * kDmConsumers * 32;
+            v[j] = q4 < nq4 ? __ldcg(reinterpret_cast<const float4*>(p.part_o + sl0 * D) + q4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int q4 = j0 + j * kDmConsumers * 32;
+            const float w = q4 < nq4 ? pm[k * p.R + rr[j]] : 0.f;
+            acc[j].x = fmaf(v[j].x, w, acc[j].x);
+            acc[j].y = fmaf(v[j].y, w, acc[j].y);
+            acc[j].z = fmaf(v[j].z, w, acc[j].z);
+            acc[j].w = fmaf(v[j].w, w, acc[j].w);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q4 = j0 + j * kDmConsumers * 32;
+          if (q4 < nq4) {
+            const int r = rr[j], dd = (q4 * 4) % D;
+            const float inv = lw[r];
+            const int t = r / G, h = kvh * G + r % G;
+            uint2 pk;
+            pk.x = pack_bf16(acc[j].x * inv, acc[j].y * inv);
+            pk.y = pack_bf16(acc[j].z * inv, acc[j].w * inv);
+            *reinterpret_cast<uint2*>(p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * D + dd) = pk;
+          }
+        }
       }
       if (tid == 0) p.ctr[g] = 0;  // ready for the next call on this workspace
     }

@@ -18,11 +18,15 @@ namespace sa {
 
 constexpr int kSelThreads = 256;
 
+constexpr int kTopkMaxN = 16384;  // candidates per selection (blocks per sequence)
+
 struct TopkShared {
-  uint32_t hist[256];
+  uint32_t hist[kSelThreads / 32][256];  // per-warp digit histograms
+  uint32_t tot[256];
   uint32_t warp_tot[kSelThreads / 32];
-  uint32_t dsel;
-  uint32_t rem_next;
+  uint32_t dsel, rem_next, cnt_dsel;
+  uint32_t bits[kTopkMaxN / 32];    // selection bitmap, index order
+  uint32_t eqbits[kTopkMaxN / 32];  // candidates tied with the threshold key
 };
 
 // Exclusive block-wide prefix sum of v (all kSelThreads threads); *total gets the sum.
@@ -48,49 +52,53 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, TopkShared& S, u
   return before + inc - v;
 }
 
-// Select from scores sc[0:n) (shared memory): forced {0, f1}; candidates the
-// rest; keep min(budget, #candidates) highest (ties -> lower index).  Writes
-// idx_out[0:kmax] (ascending, -1 padded) and *cnt_out.  All threads call.
+// Select from scores sc[0:n) (shared memory, n <= kTopkMaxN): forced {0, f1};
+// candidates the rest; keep min(budget, #candidates) highest, ties -> lower
+// index.  Writes idx_out[0:kmax] (ascending, -1 padded) and *cnt_out.  All
+// kSelThreads threads call.
+//
+// Exact radix select of the threshold key (4 x 8-bit digits, per-warp
+// histograms), then a selection bitmap built with warp ballots (keys above the
+// threshold, plus the lowest-index ties at it), compacted in index order.
 __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax, int32_t* __restrict__ idx_out,
                            int32_t* __restrict__ cnt_out, TopkShared& S) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool has_f1 = (f1 > 0 && f1 < n);
   const int ncand = n - (n > 0 ? 1 : 0) - (has_f1 ? 1 : 0);
   int take = budget < ncand ? budget : ncand;
   if (take < 0) take = 0;
   const bool take_all = (take == ncand);
-  uint32_t thr = 0xFFFFFFFFu;
-  uint32_t need_eq = 0;
+  uint32_t thr = 0xFFFFFFFFu, need_eq = 0, cnt_eq = 0;
   if (!take_all && take > 0) {
     uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(take);
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kSelThreads) S.hist[i] = 0;
+      for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&S.hist[0][0])[i] = 0;
       __syncthreads();
-      // warp-aggregated histogram: lanes with equal digits add once (the top
-      // digits of similar scores coincide, so plain atomics would serialize)
-      for (int base = 0; base < n; base += kSelThreads) {
-        const int b = base + tid;
-        uint32_t bin = 256u + (tid & 31);  // unique sentinel: no peers
-        if (b < n && b != 0 && b != f1) {
-          const uint32_t key = float_key(sc[b]);
-          if ((key & mask) == prefix) bin = (key >> shift) & 255u;
-        }
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
-        if (bin < 256u && (tid & 31) == (__ffs(peers) - 1)) atomicAdd(&S.hist[bin], __popc(peers));
+      for (int b = tid; b < n; b += kSelThreads) {
+        if (b == 0 || b == f1) continue;
+        const uint32_t key = float_key(sc[b]);
+        if ((key & mask) == prefix) atomicAdd(&S.hist[warp][(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid < 32) {
+      {
+        uint32_t t = 0;
+#pragma unroll
+        for (int w = 0; w < kSelThreads / 32; ++w) t += S.hist[w][tid];
+        S.tot[tid] = t;
+      }
+      __syncthreads();
+      if (warp == 0) {
         uint32_t c[8], s = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          c[e] = S.hist[255 - 8 * tid - e];
+          c[e] = S.tot[255 - 8 * lane - e];
           s += c[e];
         }
         uint32_t inc = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-          if (tid >= o) inc += y;
+          if (lane >= o) inc += y;
         }
         const uint32_t exc = inc - s;
         if (exc < remaining && remaining <= inc) {
@@ -98,8 +106,9 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             if (run + c[e] >= remaining) {
-              S.dsel = 255u - 8u * tid - e;
+              S.dsel = 255u - 8u * lane - e;
               S.rem_next = remaining - run;
+              S.cnt_dsel = c[e];
               break;
             }
             run += c[e];
@@ -110,65 +119,63 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
       prefix |= S.dsel << shift;
       mask |= 255u << shift;
       remaining = S.rem_next;
-      __syncthreads();
+      cnt_eq = S.cnt_dsel;
     }
     thr = prefix;
-    need_eq = remaining;
+    need_eq = remaining;  // ties at the threshold still to take (lowest indices first)
   }
-  // contiguous index range per thread, so that ranks follow index order
-  const int per = (n + kSelThreads - 1) / kSelThreads;
-  const int lo = tid * per, hi = min(n, lo + per);
-  uint32_t eq_before = 0, tot;
-  if (!take_all && take > 0) {
-    uint32_t eqc = 0;
-    for (int b = lo; b < hi; ++b)
-      if (b != 0 && b != f1 && float_key(sc[b]) == thr) ++eqc;
-    eq_before = block_excl_scan(eqc, S, &tot);
-  }
-  uint32_t nsel = 0;
-  {
-    uint32_t eqr = eq_before;
-    for (int b = lo; b < hi; ++b) {
-      bool sel;
-      if (b == 0 || b == f1) {
+  const bool surplus = cnt_eq > need_eq;  // more ties than places: resolve by index
+  const int nwords = (n + 31) >> 5;
+  for (int base = 0; base < n; base += kSelThreads) {
+    const int b = base + tid;
+    bool sel = false, eq = false;
+    if (b < n) {
+      if (b == 0 || b == f1 || take_all) {
         sel = true;
-      } else if (take_all) {
-        sel = true;
-      } else if (take == 0) {
-        sel = false;
-      } else {
+      } else if (take > 0) {
         const uint32_t key = float_key(sc[b]);
-        sel = key > thr || (key == thr && eqr < need_eq);
-        if (key == thr) ++eqr;
+        sel = key > thr || (key == thr && !surplus);
+        eq = surplus && key == thr;
       }
-      nsel += sel ? 1u : 0u;
+    }
+    const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
+    const uint32_t be = __ballot_sync(0xFFFFFFFFu, eq);
+    const int word = (base >> 5) + warp;
+    if (lane == 0 && word < nwords) {
+      S.bits[word] = bs;
+      S.eqbits[word] = be;
     }
   }
-  uint32_t total;
-  uint32_t pos = block_excl_scan(nsel, S, &total);
-  {
-    uint32_t eqr = eq_before;
-    for (int b = lo; b < hi; ++b) {
-      bool sel;
-      if (b == 0 || b == f1) {
-        sel = true;
-      } else if (take_all) {
-        sel = true;
-      } else if (take == 0) {
-        sel = false;
-      } else {
-        const uint32_t key = float_key(sc[b]);
-        sel = key > thr || (key == thr && eqr < need_eq);
-        if (key == thr) ++eqr;
-      }
-      if (sel) {
-        if (pos < static_cast<uint32_t>(kmax)) idx_out[pos] = b;
-        ++pos;
+  __syncthreads();
+  if (surplus && tid == 0) {
+    uint32_t need = need_eq;
+    for (int w = 0; w < nwords && need > 0; ++w) {
+      uint32_t e = S.eqbits[w];
+      while (e && need > 0) {
+        const uint32_t lo = e & (~e + 1u);
+        S.bits[w] |= lo;
+        e ^= lo;
+        --need;
       }
     }
   }
-  for (int i = static_cast<int>(total) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
-  if (tid == 0) *cnt_out = static_cast<int32_t>(total);
+  __syncthreads();
+  uint32_t running = 0;
+  for (int wb = 0; wb < nwords; wb += kSelThreads) {
+    const int w = wb + tid;
+    uint32_t word = w < nwords ? S.bits[w] : 0u;
+    uint32_t total;
+    uint32_t pos = running + block_excl_scan(static_cast<uint32_t>(__popc(word)), S, &total);
+    while (word) {
+      const int bit = __ffs(word) - 1;
+      if (pos < static_cast<uint32_t>(kmax)) idx_out[pos] = w * 32 + bit;
+      ++pos;
+      word &= word - 1u;
+    }
+    running += total;
+  }
+  for (int i = static_cast<int>(running) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
+  if (tid == 0) *cnt_out = static_cast<int32_t>(running);
 }
 
 // --------------------------------------------------------------------------
@@ -179,34 +186,47 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
 // distributed shared memory and runs the top-k.
 constexpr int kSelTileRows = 256;
 
-template <int D, int RMAX>
-struct SelDecodeSmem {
-  static constexpr int kBoxes = D * 4 / 128;                      // 128-byte column boxes
-  static constexpr int kTileBytes = kBoxes * kSelTileRows * 128;  // one staged tile
-  static constexpr int kMaxScores = 16384;                        // gathered scores (rank 0)
-  static constexpr int kRegion = kTileBytes > kMaxScores * 4 ? kTileBytes : kMaxScores * 4;
-  static constexpr int kQOff = kRegion;
-  static constexpr int kScOff = kQOff + RMAX * D * 4;
-  static constexpr int kMaxPer = 1024;
-  static constexpr int kTopkOff = kScOff + kMaxPer * 4;
-  static constexpr int kBarOff = kTopkOff + ((sizeof(TopkShared) + 15) / 16) * 16;
-  static constexpr int kBytes = kBarOff + 16;
+// Shared layout (runtime): staged sketch tile | q rows | gathered scores (rank 0) | top-k scratch | mbarrier
+struct SelDecodeLayout {
+  int tile_bytes, q_bytes, nb;
+  __host__ __device__ int q_off() const { return tile_bytes; }
+  __host__ __device__ int all_off() const { return tile_bytes + q_bytes; }
+  __host__ __device__ int topk_off() const { return all_off() + ((nb * 4 + 15) / 16) * 16; }
+  __host__ __device__ int bar_off() const { return topk_off() + static_cast<int>(((sizeof(TopkShared) + 15) / 16) * 16); }
+  __host__ __device__ int bytes() const { return bar_off() + 16 + 1024; }
 };
 
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// grid (CS, groups), cluster (CS, 1, 1), kSelThreads threads.  CTA rank r of
+// group g's cluster scores blocks [r*per, r*per + per): its sketch rows come in
+// by TMA (128B-swizzled tiles of tile_rows rows), one thread per block, q rows
+// broadcast from shared memory.  Each score is stored straight into CTA rank
+// 0's gather array (distributed shared memory); after one cluster barrier rank
+// 0 holds all nb scores and runs the top-k.
 template <typename TE, int D, int RMAX>
 __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
     const __grid_constant__ CUtensorMap sk_map, const TE* __restrict__ q, int T, int Hq, int Hkv, int nb,
     int nb_cap, float scale, int per, int tile_rows, int k, float* __restrict__ scores_out,
     int32_t* __restrict__ idx, int32_t* __restrict__ cnt, int kmax) {
-  using SM = SelDecodeSmem<D, RMAX>;
+  constexpr int kBoxes = D * 4 / 128;
   extern __shared__ __align__(1024) uint8_t smem_sel_dec[];
-  uint8_t* smem_raw = smem_sel_dec;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* q_s = reinterpret_cast<float*>(smem + SM::kQOff);
-  float* sc = reinterpret_cast<float*>(smem + SM::kScOff);
-  TopkShared& S = *reinterpret_cast<TopkShared*>(smem + SM::kTopkOff);
-  const uint32_t bar = smem_u32(smem + SM::kBarOff);
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_sel_dec) + 1023) & ~uintptr_t(1023));
+  const SelDecodeLayout lay{kBoxes * tile_rows * 128, RMAX * D * 4, nb};
+  float* q_s = reinterpret_cast<float*>(smem + lay.q_off());
+  float* all = reinterpret_cast<float*>(smem + lay.all_off());
+  TopkShared& S = *reinterpret_cast<TopkShared*>(smem + lay.topk_off());
+  const uint32_t bar = smem_u32(smem + lay.bar_off());
 
+  cluster_arrive_relaxed();  // paired with the wait before the first remote store
   const int tid = threadIdx.x;
   const int g = blockIdx.y;
   const uint32_t rank = cluster_ctarank();
@@ -230,23 +250,23 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
     q_s[i] = v;
   }
   __syncthreads();
+  const uint32_t all0 = map_cluster(smem_u32(all), 0);  // rank 0's gather array
+  bool waited = false;
 
   bool ok = true;
   uint32_t phase = 0;
-  // tile_rows (a multiple of 8, <= kSelTileRows) is the TMA box height: the
-  // CTA's range is fetched without over-reading the next group's sketch
-  const uint32_t tile_bytes = static_cast<uint32_t>(SM::kBoxes * tile_rows * 128);
   for (int t0 = b0; t0 < b1; t0 += tile_rows) {
     if (tid == 0) {
-      mbar_arrive_expect_tx(bar, tile_bytes);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(lay.tile_bytes));
 #pragma unroll
-      for (int bx = 0; bx < SM::kBoxes; ++bx)
+      for (int bx = 0; bx < kBoxes; ++bx)
         tma_g2s_2d(smem_u32(smem + bx * tile_rows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
     }
     ok = mbar_wait(bar, phase);
     phase ^= 1;
     if (__syncthreads_or(!ok)) break;
     const int row = t0 + tid;
+    float s = -INFINITY;
     if (tid < tile_rows && row < b1) {
       float acc[RMAX];
 #pragma unroll
@@ -254,8 +274,8 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
 #pragma unroll 4
       for (int c = 0; c < D / 4; ++c) {
         const int bx = c >> 3, cc = c & 7;
-        const float4 kv = *reinterpret_cast<const float4*>(smem + bx * tile_rows * 128 + tid * 128 +
-                                                           ((cc ^ (tid & 7)) << 4));
+        const float4 kv =
+            *reinterpret_cast<const float4*>(smem + bx * tile_rows * 128 + tid * 128 + ((cc ^ (tid & 7)) << 4));
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
           const float4 qv = *reinterpret_cast<const float4*>(q_s + r * D + c * 4);
@@ -265,29 +285,21 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
           acc[r] = fmaf(qv.w, kv.w, acc[r]);
         }
       }
-      float s = -INFINITY;
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
         if (r < R) s = fmaxf(s, acc[r]);
-      sc[row - b0] = s;
       if (scores_out) scores_out[static_cast<size_t>(g) * nb + row] = s;
     }
-    __syncthreads();
-  }
-  if (!ok) {
-    // a TMA wait gave up: leave the selection untouched; the host sees SA_ERR_TIMEOUT
-  }
-  cluster_sync();
-  float* all = reinterpret_cast<float*>(smem);  // reuses the tile region
-  if (rank == 0) {
-    for (int bb = tid; bb < nb; bb += kSelThreads) {
-      const uint32_t owner = static_cast<uint32_t>(bb / per);
-      all[bb] = ld_cluster_f32(map_cluster(smem_u32(sc + (bb - static_cast<int>(owner) * per)), owner));
+    if (!waited) {
+      cluster_wait();  // every CTA of the cluster is running: remote stores are safe
+      waited = true;
     }
+    if (tid < tile_rows && row < b1) st_cluster_f32(all0 + 4u * static_cast<uint32_t>(row), s);
+    __syncthreads();  // the tile buffer is refilled next iteration
   }
-  cluster_sync();
+  if (!waited) cluster_wait();
+  cluster_sync();  // all scores have landed in rank 0
   if (rank != 0) return;
-  __syncthreads();
   block_topk(all, nb, nb - 1, k, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, S);
 }
 

@@ -211,26 +211,29 @@ int max_cluster_size(const void* fn, int smem, int groups, cudaStream_t st) {
 
 template <typename TE, int D, int RMAX>
 sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStream_t st) {
-  using SM = sa::SelDecodeSmem<D, RMAX>;
   const int groups = a.B * a.Hkv;
   const int nb = cdiv(a.L, a.block);
   const int nb_cap = cdiv(a.Ls, a.block);
   auto kern = sa::select_decode_kernel<TE, D, RMAX>;
-  const int smem = SM::kBytes + 1024;
-  SA_TRY(set_smem(kern, smem));
   static int max_cs = 0;  // per instantiation
   if (max_cs == 0) {
+    sa::SelDecodeLayout big{(D * 4 / 128) * sa::kSelTileRows * 128, RMAX * D * 4, sa::kTopkMaxN};
+    SA_TRY(set_smem(kern, big.bytes()));
     cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    max_cs = std::max(1, std::min(16, max_cluster_size(reinterpret_cast<const void*>(kern), smem, groups, st)));
+    max_cs = std::max(1, std::min(16, max_cluster_size(reinterpret_cast<const void*>(kern), big.bytes(), groups, st)));
   }
+  // about one CTA per SM in total, at most 1024 blocks per CTA
   int cs = std::min(max_cs, std::max(1, cdiv(di.sms, groups)));
-  cs = std::max(cs, cdiv(nb, SM::kMaxPer));
+  cs = std::max(cs, cdiv(nb, 1024));
   SA_SUP(cs <= max_cs, "decode selection over %d blocks needs a cluster of %d CTAs (device allows %d)", nb, cs,
          max_cs);
   cs = std::min(cs, nb);
   const int per = cdiv(nb, cs);
   cs = cdiv(nb, per);
   const int tile_rows = std::min(sa::kSelTileRows, cdiv(per, 8) * 8);
+  const sa::SelDecodeLayout lay{(D * 4 / 128) * tile_rows * 128, RMAX * D * 4, nb};
+  const int smem = lay.bytes();
+  SA_TRY(set_smem(kern, smem));
   CUtensorMap map;
   SA_TRY(make_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.sketch, D, static_cast<uint64_t>(groups) * nb_cap,
                      D * 4, 32, tile_rows, CU_TENSOR_MAP_SWIZZLE_128B));
@@ -339,6 +342,7 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
   // two CTAs per SM; equal contiguous ranges of units
   const long long target = 2LL * di.sms;
   long long per = (U + target - 1) / target;
+  per = std::max<long long>(per, (a.kmax + sa::kDmMaxParts - 2) / (sa::kDmMaxParts - 1));  // <= 64 partials per group
   per = std::min<long long>(std::max<long long>(per, 1), sa::kDmMaxList);
   const int nctas = static_cast<int>((U + per - 1) / per);
   sa::DmLayout lay{2, R, D, static_cast<int>(per)};
@@ -493,7 +497,7 @@ sa_status_t validate_select(const SelectArgs& a) {
   SA_ARG(need >= 1, "bad selection parameters");
   SA_ARG(a.kmax >= need, "kmax (%d) too small: the selection needs %d", a.kmax, need);
   const int nb = cdiv(a.L, a.block);
-  SA_SUP(nb <= 16384, "at most 16384 blocks per sequence (got %d)", nb);
+  SA_SUP(nb <= sa::kTopkMaxN, "at most %d blocks per sequence (got %d)", sa::kTopkMaxN, nb);
   if (a.prefill) SA_ARG(a.qtile >= 1 && a.Tq == a.L, "prefill: qtile >= 1 and Tq == L required");
   if (a.mode == SA_SELECT_MASS) {
     SA_ARG(a.scores != nullptr, "MASS mode needs the scores array");
