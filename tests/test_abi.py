@@ -14,8 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def sa():
-    from top_block_sparse_pooled_b300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._load_builder().build()
     import top_block_sparse_pooled_b300 as m
     return m
 
