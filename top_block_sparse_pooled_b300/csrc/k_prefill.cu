@@ -1,0 +1,367 @@
+// k_prefill.cu -- causal sparse prefill over the selected KV blocks on the
+// fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// "How Much Dense Attention is Necessary?" Sec. 2.1: attention is recomputed
+// exactly, with the original q, k, v, on the selected support only, the
+// support being shared by a run of consecutive queries (here a 128-row query
+// tile).  "The Sparse Frontier" RQ2: block-by-block selection for prefill.
+//
+// Work unit: (group g = (b, kv-head), query tile i, head pair).  The two heads
+// of a pair share every K/V tile the CTA loads (GQA), each head being one
+// 128-row M tile.  Units are ordered longest first (tile i descending: tile i
+// has up to i + 1 causal blocks) and dealt round-robin to a persistent grid of
+// one CTA per SM.
+//
+// Roles (384 threads):
+//   warp 0    TMA producer: the unit's Q tiles (3-D map: d, head, row), then
+//             the K and V tiles of each selected block into 2-stage rings.
+//   warp 1    TMEM allocator and MMA issuer (one thread):
+//               S_t = Q_t K^T  (M=128, N=128 keys, K=d; both K-major in smem)
+//               O_t += P_t V   (A = P_t from TMEM, B = V MN-major in smem)
+//   warps 4-7, 8-11  softmax warpgroup t = 0, 1: thread r owns query row r of
+//             M tile t (= TMEM lane r).  It reads its S row from TMEM, masks
+//             (causal on the diagonal block, keys past L), keeps the running
+//             max m and sum l (base 2), writes P = exp2(S - m) as bf16 pairs
+//             over the first 64 columns of S in TMEM, and rescales its O row
+//             only when the running max grows by more than 8 (so P <= 2^8; the
+//             result is the same exact softmax, normalised once at the end).
+//             At the end of a unit it normalises O, stores it and the lse.
+// TMEM: S_0 cols 0-127, S_1 128-255, O_0 256-383, O_1 384-511.
+//
+// Every mbarrier wait is bounded (sa_ptx.cuh); after a give-up all later
+// waits return at once, every role runs out its loops, the producer and the
+// MMA issuer drain what they issued, and TMEM is freed before exit.
+#pragma once
+
+#include "sa_tc.cuh"
+
+namespace sa {
+
+constexpr int kPfRows = 128;            // query rows per M tile (= qtile)
+constexpr int kPfKeys = 128;            // keys per KV block
+constexpr int kPfTile = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 operand (two 64-column boxes)
+constexpr int kPfBox = 128 * 128;       // bytes of one 64-column box of 128 rows
+constexpr int kPfStages = 2;
+constexpr int kPfThreads = 384;
+constexpr float kPfRescale = 8.0f;  // log2 growth of the running max that forces an O rescale
+
+struct PfSmem {
+  static constexpr int kQ = 0;                         // [2] M tiles
+  static constexpr int kK = kQ + 2 * kPfTile;          // [kPfStages]
+  static constexpr int kV = kK + kPfStages * kPfTile;  // [kPfStages]
+  static constexpr int kBar = kV + kPfStages * kPfTile;
+  // mbarrier slots (8 bytes each)
+  static constexpr int Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = 4, V_FULL = 6, V_EMPTY = 8, S_FULL = 10,
+                       P_FULL = 12, O_BAR = 14, O_FREE = 16, DONE = 18, NBARS = 19;
+  static constexpr int kSlot = kBar + NBARS * 8;
+  static constexpr int kBytes = kSlot + 16 + 1024;  // + slack for 1024-byte alignment
+};
+
+struct PfParams {
+  const int32_t* idx;  // [groups, nq, kmax]
+  const int32_t* cnt;  // [groups, nq]
+  int kmax;
+  int L, Hq, Hkv, G, groups, nq, nb, npairs, units;
+  float qscale;  // softmax scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;  // optional [B, Hq, L]
+};
+
+struct PfUnit {
+  int g, i, nt, b, kvh, h0, n;
+  const int32_t* ids;
+};
+
+// Unit u -> (tile, group, head pair), tiles in descending order.
+__device__ __forceinline__ PfUnit pf_unit(const PfParams& p, int u) {
+  PfUnit w;
+  const int per_i = p.groups * p.npairs;
+  w.i = p.nq - 1 - u / per_i;
+  const int r = u % per_i;
+  w.g = r / p.npairs;
+  const int pair = r % p.npairs;
+  w.nt = min(2, p.G - 2 * pair);
+  w.b = w.g / p.Hkv;
+  w.kvh = w.g % p.Hkv;
+  w.h0 = w.kvh * p.G + 2 * pair;
+  const size_t sel = static_cast<size_t>(w.g) * p.nq + w.i;
+  w.n = min(p.cnt[sel], p.kmax);
+  w.ids = p.idx + sel * p.kmax;
+  return w;
+}
+
+__device__ __forceinline__ bool pf_valid(int blk, int nb) { return blk >= 0 && blk < nb; }
+
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                                                                 const __grid_constant__ CUtensorMap kmap,
+                                                                 const __grid_constant__ CUtensorMap vmap,
+                                                                 const PfParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_pf[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_pf) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + PfSmem::kBar;
+  auto bar = [&](int slot) { return bar0 + 8u * slot; };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + PfSmem::kSlot);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+    mbar_init(bar(PfSmem::Q_FULL), 1);
+    mbar_init(bar(PfSmem::Q_EMPTY), 1);
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(bar(PfSmem::K_FULL + s), 1);
+      mbar_init(bar(PfSmem::K_EMPTY + s), 1);
+      mbar_init(bar(PfSmem::V_FULL + s), 1);
+      mbar_init(bar(PfSmem::V_EMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(PfSmem::S_FULL + t), 1);
+      mbar_init(bar(PfSmem::P_FULL + t), kPfRows);
+      mbar_init(bar(PfSmem::O_BAR + t), 1);
+      mbar_init(bar(PfSmem::O_FREE + t), kPfRows);
+    }
+    mbar_init(bar(PfSmem::DONE), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(tslot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;  // K/V ring iteration (valid blocks, across units)
+      int nu = 0;       // units processed
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+        const PfUnit w = pf_unit(p, u);
+        if (nu > 0 && ok) ok = mbar_wait(bar(PfSmem::Q_EMPTY), (nu - 1) & 1);
+        mbar_arrive_expect_tx(bar(PfSmem::Q_FULL), w.nt * kPfTile);
+        for (int t = 0; t < w.nt; ++t)
+          for (int bx = 0; bx < 2; ++bx)
+            tma_g2s_3d(sbase + PfSmem::kQ + t * kPfTile + bx * kPfBox, &qmap, bx * 64, w.h0 + t,
+                       w.b * p.L + w.i * kPfRows, bar(PfSmem::Q_FULL));
+        for (int j = 0; j < w.n; ++j) {
+          const int blk = w.ids[j];
+          if (!pf_valid(blk, p.nb)) continue;
+          const int s = it % kPfStages;
+          const uint32_t ph = (it / kPfStages) & 1;
+          const int row = w.g * p.L + blk * kPfKeys;
+          if (it >= kPfStages && ok) ok = mbar_wait(bar(PfSmem::K_EMPTY + s), ph ^ 1);
+          mbar_arrive_expect_tx(bar(PfSmem::K_FULL + s), kPfTile);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_g2s_2d(sbase + PfSmem::kK + s * kPfTile + bx * kPfBox, &kmap, bx * 64, row, bar(PfSmem::K_FULL + s));
+          if (it >= kPfStages && ok) ok = mbar_wait(bar(PfSmem::V_EMPTY + s), ph ^ 1);
+          mbar_arrive_expect_tx(bar(PfSmem::V_FULL + s), kPfTile);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_g2s_2d(sbase + PfSmem::kV + s * kPfTile + bx * kPfBox, &vmap, bx * 64, row, bar(PfSmem::V_FULL + s));
+          ++it;
+        }
+      }
+      // never exit with copies in flight: wait for the last fill of each stage and of Q
+      for (uint32_t k = it > kPfStages ? it - kPfStages : 0; k < it; ++k) {
+        mbar_wait_drain(bar(PfSmem::K_FULL + k % kPfStages), (k / kPfStages) & 1);
+        mbar_wait_drain(bar(PfSmem::V_FULL + k % kPfStages), (k / kPfStages) & 1);
+      }
+      if (nu > 0) mbar_wait_drain(bar(PfSmem::Q_FULL), (nu - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdPV = tc::idesc_bf16(128, 128, false, true);
+      uint32_t it = 0;
+      int nu = 0;
+      uint32_t o_commits[2] = {0, 0};  // commits to O_BAR[t]
+      uint32_t p_waits[2] = {0, 0};    // completed P_FULL[t] phases consumed
+      uint32_t units_t[2] = {0, 0};    // earlier units in which M tile t was active
+      bool pv_pending[2] = {false, false};
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+        const PfUnit w = pf_unit(p, u);
+        if (ok) ok = mbar_wait(bar(PfSmem::Q_FULL), nu & 1);
+        tc::fence_after_sync();
+        int jj = 0;
+        for (int j = 0; j < w.n; ++j) {
+          const int blk = w.ids[j];
+          if (!pf_valid(blk, p.nb)) continue;
+          const int s = it % kPfStages;
+          const uint32_t ph = (it / kPfStages) & 1;
+          if (ok) ok = mbar_wait(bar(PfSmem::K_FULL + s), ph);
+          tc::fence_after_sync();
+          const uint32_t kst = sbase + PfSmem::kK + s * kPfTile;
+          for (int t = 0; t < w.nt; ++t) {
+            if (pv_pending[t]) {  // P_t (aliasing S_t) must be consumed before S_t is rewritten
+              if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), (o_commits[t] - 1) & 1);
+              tc::fence_after_sync();
+              pv_pending[t] = false;
+            }
+            const uint32_t qt = sbase + PfSmem::kQ + t * kPfTile;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t off = (k >> 2) * kPfBox + (k & 3) * 32;
+              tc::mma_ss(tmem + t * 128, tc::desc_kmajor(qt + off), tc::desc_kmajor(kst + off), kIdQK, k > 0);
+            }
+            tc::mma_commit(bar(PfSmem::S_FULL + t));
+          }
+          tc::mma_commit(bar(PfSmem::K_EMPTY + s));
+          if (ok) ok = mbar_wait(bar(PfSmem::V_FULL + s), ph);
+          tc::fence_after_sync();
+          const uint32_t vst = sbase + PfSmem::kV + s * kPfTile;
+          for (int t = 0; t < w.nt; ++t) {
+            if (ok) ok = mbar_wait(bar(PfSmem::P_FULL + t), p_waits[t] & 1);
+            ++p_waits[t];
+            if (jj == 0 && units_t[t] > 0) {  // O_t of the previous unit has been read out
+              if (ok) ok = mbar_wait(bar(PfSmem::O_FREE + t), (units_t[t] - 1) & 1);
+            }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              tc::mma_ts(tmem + 256 + t * 128, tmem + t * 128 + 8 * k,
+                         tc::desc_mnmajor(vst + k * 2048, kPfBox), kIdPV, (jj > 0 || k > 0) ? 1u : 0u);
+            tc::mma_commit(bar(PfSmem::O_BAR + t));
+            ++o_commits[t];
+            pv_pending[t] = true;
+          }
+          tc::mma_commit(bar(PfSmem::V_EMPTY + s));
+          ++it;
+          ++jj;
+        }
+        tc::mma_commit(bar(PfSmem::Q_EMPTY));
+        for (int t = 0; t < w.nt; ++t) ++units_t[t];
+      }
+      // drain: every MMA issued has completed before TMEM is freed
+      tc::mma_commit(bar(PfSmem::DONE));
+      mbar_wait_drain(bar(PfSmem::DONE), 0);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax
+    const int t = (warp - 4) >> 2;           // M tile of this warpgroup
+    const int r = ((warp & 3) << 5) | lane;  // row within the tile = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_addr = lane_base + t * 128;
+    const uint32_t o_addr = lane_base + 256 + t * 128;
+    uint32_t s_waits = 0, o_waits = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      const PfUnit w = pf_unit(p, u);
+      if (t >= w.nt) continue;
+      const int qpos = w.i * kPfRows + r;  // query position of this row
+      float m_run = -INFINITY, l_run = 0.f;
+      int jj = 0;
+      for (int j = 0; j < w.n; ++j) {
+        const int blk = w.ids[j];
+        if (!pf_valid(blk, p.nb)) continue;
+        if (ok) ok = mbar_wait(bar(PfSmem::S_FULL + t), s_waits & 1);
+        ++s_waits;
+        tc::fence_after_sync();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_addr + 32 * c, s + 32 * c);
+        tc::tmem_wait_ld();
+        const int kbase = blk * kPfKeys;
+        float mx = -INFINITY;
+        if (kbase + kPfKeys - 1 <= qpos && kbase + kPfKeys <= p.L) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            s[c] *= p.qscale;
+            mx = fmaxf(mx, s[c]);
+          }
+        } else {
+          const int lim = min(qpos, p.L - 1) - kbase;  // last visible key column
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            s[c] = (c <= lim) ? s[c] * p.qscale : -INFINITY;
+            mx = fmaxf(mx, s[c]);
+          }
+        }
+        if (jj > 0) {  // PV_t of the previous block has completed: O_t is stable
+          if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), o_waits & 1);
+          ++o_waits;
+          tc::fence_after_sync();
+        }
+        if (mx > m_run + kPfRescale) {
+          if (jj > 0 && m_run != -INFINITY) {
+            const float corr = exp2f(m_run - mx);
+            l_run *= corr;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float o[32];
+              tc::tmem_ld32(o_addr + 32 * c, o);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= corr;
+              tc::tmem_st32(o_addr + 32 * c, o);
+            }
+          }
+          m_run = mx;
+        }
+        const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+        float pk[64];
+        float ls = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float a = exp2f(s[2 * c] - mu), b2 = exp2f(s[2 * c + 1] - mu);
+          ls += a + b2;
+          __nv_bfloat162 h = __floats2bfloat162_rn(a, b2);
+          pk[c] = *reinterpret_cast<float*>(&h);
+        }
+        l_run += ls;
+        tc::tmem_st32(s_addr, pk);
+        tc::tmem_st32(s_addr + 32, pk + 32);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        mbar_arrive(bar(PfSmem::P_FULL + t));
+        ++jj;
+      }
+      // ---- epilogue: O / l, lse
+      float o[128];
+      if (jj > 0) {
+        if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), o_waits & 1);
+        ++o_waits;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(o_addr + 32 * c, o + 32 * c);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) o[c] = 0.f;
+      }
+      tc::fence_before_sync();
+      mbar_arrive(bar(PfSmem::O_FREE + t));
+      if (qpos < p.L) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const int h = w.h0 + t;
+        __nv_bfloat16* dst = p.out + ((static_cast<size_t>(w.b) * p.L + qpos) * p.Hq + h) * kPfRows;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          uint4 v;
+          uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 hh = __floats2bfloat162_rn(o[8 * c + 2 * e] * inv, o[8 * c + 2 * e + 1] * inv);
+            vw[e] = *reinterpret_cast<uint32_t*>(&hh);
+          }
+          reinterpret_cast<uint4*>(dst)[c] = v;
+        }
+        if (p.lse)
+          p.lse[(static_cast<size_t>(w.b) * p.Hq + h) * p.L + qpos] =
+              l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace sa

@@ -117,6 +117,15 @@ __device__ __forceinline__ void tma_g2s_2d(uint32_t dst, const CUtensorMap* map,
       : "memory");
 }
 
+// 3-D tensor copy (TMA) global -> shared; x innermost (same alignment rule).
+__device__ __forceinline__ void tma_g2s_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
