@@ -55,7 +55,9 @@ def assert_selection(g_idx, g_cnt, o_idx, o_cnt, o_scores, rel=SEL_REL, what="")
     swaps = 0
     for u in range(len(o_cnt)):
         n = int(g_cnt[u])
-        assert n == int(o_cnt[u]), "%s unit %d: count %d vs oracle %d" % (what, u, n, o_cnt[u])
+        assert n == int(o_cnt[u]), "%s unit %d: count %d vs oracle %d (gpu %s, oracle %s, scores %s)" % (
+            what, u, n, o_cnt[u], g_idx[u, :n].tolist(), o_idx[u, : o_cnt[u]].tolist(),
+            np.asarray(o_scores[u])[:16].tolist())
         row = g_idx[u, :n].tolist()
         assert row == sorted(set(row)), "%s unit %d: not ascending/unique: %s" % (what, u, row)
         assert np.all(g_idx[u, n:] == -1), "%s unit %d: padding" % (what, u)

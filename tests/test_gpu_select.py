@@ -1,0 +1,64 @@
+"""GPU top-k selection against the oracle's brute-force-pinned selection, over
+many sizes, budgets and tie patterns (mass mode: scores given), and the decode
+sketch selection at small block counts."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import assert_selection, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sa():
+    import top_block_sparse_pooled_b300 as m
+    return m
+
+
+@pytest.mark.parametrize("n", [3, 4, 5, 7, 31, 32, 33, 64, 100, 257, 1000, 4096, 16384])
+def test_select_given_scores_brute_force(sa, n):
+    """One selection per group over n blocks (block = 1 key), forced {0, n-1}."""
+    rng = np.random.default_rng(n)
+    groups = 6
+    budgets = [0, 1, 2, max(0, n // 3), max(0, n - 3), n]
+    for trial, k in enumerate(budgets):
+        # coarse values make many exact ties; the last group has all-equal scores
+        s = rng.integers(-4, 5, size=(groups, n)).astype(np.float32) * 0.25
+        s[-1] = 1.0
+        kmax = sa.sa_select_kmax(n, 1, 0, False, k)
+        scores = torch.from_numpy(s.reshape(1, groups, 1, n)).cuda()
+        idx = torch.full((1, groups, 1, kmax), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((1, groups, 1), -7, dtype=torch.int32, device="cuda")
+        sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, scores, groups, n, n, 1, 0, False, k, 0, 1, 1.0,
+                          idx, cnt, d=128, dtype=sa.SA_BF16, B=1, Tq=1, Hq=groups)
+        torch.cuda.synchronize()
+        assert sa.sa_device_status(clear=True) == 0
+        o_idx, o_cnt = oracle.select(s.astype(np.float64), n, n - 1, k, kmax)
+        # exact ties must resolve to the lower index: bit-exact, no swaps
+        g_idx = idx.cpu().numpy().reshape(groups, kmax)
+        g_cnt = cnt.cpu().numpy().reshape(groups)
+        for g in range(groups):
+            assert g_cnt[g] == o_cnt[g] and np.array_equal(g_idx[g], o_idx[g]), (
+                "n=%d k=%d group %d: gpu %s (cnt %d), oracle %s (cnt %d)" % (
+                    n, k, g, g_idx[g][:12].tolist(), g_cnt[g], o_idx[g][:12].tolist(), o_cnt[g]))
+
+
+@pytest.mark.parametrize("nb", [3, 4, 5, 9, 33])
+def test_decode_select_small_block_counts(sa, nb):
+    wl = synth.WORKLOADS["c2"].replace(B=2, L=64 * nb - 5, k=2, needles=1, seed=400 + nb)
+    x = synth.make_inputs(wl)
+    q, k = dev(x.q), dev(x.k)
+    sk = torch.empty((wl.B, wl.Hkv, wl.nb, wl.d), dtype=torch.float32, device="cuda")
+    sa.sa_build_sketch(k, wl.L, wl.Bk, sk)
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
+    idx = torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device="cuda")
+    sa.sa_select_topk(sa.SA_SELECT_SKETCH, q, sk, None, wl.Hkv, wl.L, wl.L, wl.Bk, 0, False, wl.k, 0, 1, wl.scale,
+                      idx, cnt)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status(clear=True) == 0
+    o_idx, o_cnt, o_s, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax)
+    assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s, what="nb=%d" % nb)

@@ -261,107 +261,119 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         const int blk = w.ids[j];
         if (!pf_valid(blk, p.nb)) continue;
         if (ok) ok = mbar_wait(bar(PfSmem::S_FULL + t), s_waits & 1);
+        ok = __all_sync(0xFFFFFFFFu, ok);  // keep the warp converged for its TMEM accesses
         ++s_waits;
         tc::fence_after_sync();
-        float s[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_addr + 32 * c, s + 32 * c);
-        tc::tmem_wait_ld();
+        // pass 1: row max over the visible keys (raw dot products; qscale > 0)
         const int kbase = blk * kPfKeys;
+        const bool full = kbase + kPfKeys - 1 <= qpos && kbase + kPfKeys <= p.L;
+        const int lim = full ? kPfKeys - 1 : min(qpos, p.L - 1) - kbase;  // last visible key column
         float mx = -INFINITY;
-        if (kbase + kPfKeys - 1 <= qpos && kbase + kPfKeys <= p.L) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            s[c] *= p.qscale;
-            mx = fmaxf(mx, s[c]);
-          }
-        } else {
-          const int lim = min(qpos, p.L - 1) - kbase;  // last visible key column
+        for (int c = 0; c < 4; ++c) {
+          float s[32];
+          tc::tmem_ld32(s_addr + 32 * c, s);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            s[c] = (c <= lim) ? s[c] * p.qscale : -INFINITY;
-            mx = fmaxf(mx, s[c]);
-          }
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, (32 * c + e <= lim) ? s[e] : -INFINITY);
         }
+        mx = (mx == -INFINITY) ? -INFINITY : mx * p.qscale;
         if (jj > 0) {  // PV_t of the previous block has completed: O_t is stable
           if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), o_waits & 1);
+          ok = __all_sync(0xFFFFFFFFu, ok);
           ++o_waits;
           tc::fence_after_sync();
         }
-        if (mx > m_run + kPfRescale) {
-          if (jj > 0 && m_run != -INFINITY) {
-            const float corr = exp2f(m_run - mx);
-            l_run *= corr;
+        // lazy rescale; TMEM accesses are warp-wide, so a warp rescales when any
+        // of its rows needs it (the others use a factor of 1)
+        const bool need = mx > m_run + kPfRescale;
+        if (jj > 0 && __any_sync(0xFFFFFFFFu, need)) {
+          const float corr = (need && m_run != -INFINITY) ? exp2f(m_run - mx) : 1.f;
+          l_run *= corr;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float o[32];
-              tc::tmem_ld32(o_addr + 32 * c, o);
-              tc::tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tc::tmem_ld32(o_addr + 32 * c, o);
+            tc::tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= corr;
-              tc::tmem_st32(o_addr + 32 * c, o);
-            }
+            for (int e = 0; e < 32; ++e) o[e] *= corr;
+            tc::tmem_st32(o_addr + 32 * c, o);
           }
-          m_run = mx;
         }
+        if (need) m_run = mx;
+        // pass 2: P = exp2(S * qscale - m) as bf16 pairs into columns 0-63 of S_t
+        // (chunk c's pairs land on columns 16c..16c+15, already read)
         const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-        float pk[64];
         float ls = 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float a = exp2f(s[2 * c] - mu), b2 = exp2f(s[2 * c + 1] - mu);
-          ls += a + b2;
-          __nv_bfloat162 h = __floats2bfloat162_rn(a, b2);
-          pk[c] = *reinterpret_cast<float*>(&h);
+        for (int c = 0; c < 4; ++c) {
+          float s[32];
+          tc::tmem_ld32(s_addr + 32 * c, s);
+          tc::tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = 32 * c + 2 * e;
+            const float a0 = (c0 <= lim) ? exp2f(fmaf(s[2 * e], p.qscale, -mu)) : 0.f;
+            const float a1 = (c0 + 1 <= lim) ? exp2f(fmaf(s[2 * e + 1], p.qscale, -mu)) : 0.f;
+            ls += a0 + a1;
+            __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+            pk[e] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          tc::tmem_st16(s_addr + 16 * c, pk);
         }
         l_run += ls;
-        tc::tmem_st32(s_addr, pk);
-        tc::tmem_st32(s_addr + 32, pk + 32);
         tc::tmem_wait_st();
         tc::fence_before_sync();
         mbar_arrive(bar(PfSmem::P_FULL + t));
         ++jj;
       }
       // ---- epilogue: O / l, lse
-      float o[128];
       if (jj > 0) {
         if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), o_waits & 1);
+        ok = __all_sync(0xFFFFFFFFu, ok);
         ++o_waits;
         tc::fence_after_sync();
+      }
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int h = w.h0 + t;
+      __nv_bfloat16* dst = p.out + ((static_cast<size_t>(w.b) * p.L + qpos) * p.Hq + h) * kPfRows;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32(o_addr + 32 * c, o + 32 * c);
-        tc::tmem_wait_ld();
-      } else {
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        if (jj > 0) {
+          tc::tmem_ld32(o_addr + 32 * c, o);
+          tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) o[c] = 0.f;
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          __nv_bfloat162 hh = __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
+          pk[e] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+        if (qpos < p.L) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            reinterpret_cast<uint4*>(dst)[4 * c + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
       }
       tc::fence_before_sync();
       mbar_arrive(bar(PfSmem::O_FREE + t));
-      if (qpos < p.L) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const int h = w.h0 + t;
-        __nv_bfloat16* dst = p.out + ((static_cast<size_t>(w.b) * p.L + qpos) * p.Hq + h) * kPfRows;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          uint4 v;
-          uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 hh = __floats2bfloat162_rn(o[8 * c + 2 * e] * inv, o[8 * c + 2 * e + 1] * inv);
-            vw[e] = *reinterpret_cast<uint32_t*>(&hh);
-          }
-          reinterpret_cast<uint4*>(dst)[c] = v;
-        }
-        if (p.lse)
-          p.lse[(static_cast<size_t>(w.b) * p.Hq + h) * p.L + qpos] =
-              l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-      }
+      if (p.lse && qpos < p.L)
+        p.lse[(static_cast<size_t>(w.b) * p.Hq + h) * p.L + qpos] =
+            l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
     }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, 512);
+  }
 }
 
 }  // namespace sa

@@ -52,30 +52,29 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, TopkShared& S, u
   return before + inc - v;
 }
 
-// Select from scores sc[0:n) (shared memory, n <= kTopkMaxN): forced {0, f1};
-// candidates the rest; keep min(budget, #candidates) highest, ties -> lower
-// index.  Writes idx_out[0:kmax] (ascending, -1 padded) and *cnt_out.  All
-// kSelThreads threads call.
+// Select from scores sc[0:n) (shared memory, n <= kTopkMaxN): the forced blocks
+// are the first and the last (0 and n-1, one block when n == 1); the candidates
+// are 1..n-2; keep min(budget, n-2) of them with the highest scores, ties to the
+// lower index.  Writes idx_out[0:kmax] (ascending, -1 padded) and *cnt_out.
+// All kSelThreads threads call.
 //
 // Exact radix select of the threshold key (4 x 8-bit digits, per-warp
 // histograms), then a selection bitmap built with warp ballots (keys above the
 // threshold, plus the lowest-index ties at it), compacted in index order.
-__device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax, int32_t* __restrict__ idx_out,
+__device__ void block_topk(const float* sc, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
                            int32_t* __restrict__ cnt_out, TopkShared& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool has_f1 = (f1 > 0 && f1 < n);
-  const int ncand = n - (n > 0 ? 1 : 0) - (has_f1 ? 1 : 0);
-  int take = budget < ncand ? budget : ncand;
-  if (take < 0) take = 0;
-  const bool take_all = (take == ncand);
+  const int last = n - 1;                      // forced local / diagonal block
+  const int ncand = n > 2 ? n - 2 : 0;         // candidates 1 .. n-2
+  const int take = budget <= 0 ? 0 : (budget < ncand ? budget : ncand);
+  const int take_all = take == ncand ? 1 : 0;
   uint32_t thr = 0xFFFFFFFFu, need_eq = 0, cnt_eq = 0;
-  if (!take_all && take > 0) {
+  if (take_all == 0 && take > 0) {
     uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(take);
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&S.hist[0][0])[i] = 0;
       __syncthreads();
-      for (int b = tid; b < n; b += kSelThreads) {
-        if (b == 0 || b == f1) continue;
+      for (int b = 1 + tid; b < last; b += kSelThreads) {
         const uint32_t key = float_key(sc[b]);
         if ((key & mask) == prefix) atomicAdd(&S.hist[warp][(key >> shift) & 255u], 1u);
       }
@@ -88,6 +87,8 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
       }
       __syncthreads();
       if (warp == 0) {
+        // lane l holds digits 255-8l .. 248-8l (descending); find the digit at
+        // which the count of keys above it, plus its own, reaches `remaining`
         uint32_t c[8], s = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -100,19 +101,15 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
           const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
           if (lane >= o) inc += y;
         }
-        const uint32_t exc = inc - s;
-        if (exc < remaining && remaining <= inc) {
-          uint32_t run = exc;
+        uint32_t run = inc - s;  // keys in higher digits than this lane's first
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (run + c[e] >= remaining) {
-              S.dsel = 255u - 8u * lane - e;
-              S.rem_next = remaining - run;
-              S.cnt_dsel = c[e];
-              break;
-            }
-            run += c[e];
+        for (int e = 0; e < 8; ++e) {
+          if (run < remaining && remaining <= run + c[e]) {  // exactly one (lane, e) matches
+            S.dsel = 255u - 8u * static_cast<uint32_t>(lane) - static_cast<uint32_t>(e);
+            S.rem_next = remaining - run;
+            S.cnt_dsel = c[e];
           }
+          run += c[e];
         }
       }
       __syncthreads();
@@ -120,22 +117,23 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
       mask |= 255u << shift;
       remaining = S.rem_next;
       cnt_eq = S.cnt_dsel;
+      __syncthreads();  // S.dsel is rewritten by the next pass
     }
     thr = prefix;
     need_eq = remaining;  // ties at the threshold still to take (lowest indices first)
   }
-  const bool surplus = cnt_eq > need_eq;  // more ties than places: resolve by index
+  const int surplus = (cnt_eq > need_eq) ? 1 : 0;  // more ties than places: resolve by index
   const int nwords = (n + 31) >> 5;
   for (int base = 0; base < n; base += kSelThreads) {
     const int b = base + tid;
     bool sel = false, eq = false;
     if (b < n) {
-      if (b == 0 || b == f1 || take_all) {
+      if (b == 0 || b == last || take_all != 0) {
         sel = true;
       } else if (take > 0) {
         const uint32_t key = float_key(sc[b]);
-        sel = key > thr || (key == thr && !surplus);
-        eq = surplus && key == thr;
+        sel = key > thr || (key == thr && surplus == 0);
+        eq = surplus != 0 && key == thr;
       }
     }
     const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
@@ -147,7 +145,7 @@ __device__ void block_topk(const float* sc, int n, int f1, int budget, int kmax,
     }
   }
   __syncthreads();
-  if (surplus && tid == 0) {
+  if (surplus != 0 && tid == 0) {
     uint32_t need = need_eq;
     for (int w = 0; w < nwords && need > 0; ++w) {
       uint32_t e = S.eqbits[w];
@@ -300,7 +298,7 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
   if (!waited) cluster_wait();
   cluster_sync();  // all scores have landed in rank 0
   if (rank != 0) return;
-  block_topk(all, nb, nb - 1, k, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, S);
+  block_topk(all, nb, k, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, S);
 }
 
 // --------------------------------------------------------------------------
@@ -326,7 +324,7 @@ __global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* 
   const size_t u = static_cast<size_t>(g) * nq + i;
   for (int bb = threadIdx.x; bb < nvalid; bb += kSelThreads) sc[bb] = scores[u * nb + bb];
   __syncthreads();
-  block_topk(sc, nvalid, nvalid - 1, budget, kmax, idx + u * kmax, cnt + u, S);
+  block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, S);
 }
 
 // --------------------------------------------------------------------------
@@ -450,7 +448,7 @@ __global__ void __launch_bounds__(kSelThreads) select_prefill_sketch_kernel(
   int budget = k;
   if (frac_num > 0) budget = k + (frac_num * nvalid + frac_den - 1) / frac_den;
   __syncthreads();
-  block_topk(sc, nvalid, nvalid - 1, budget, kmax, idx + u * kmax, cnt + u, S);
+  block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, S);
 }
 
 }  // namespace sa

@@ -15,6 +15,8 @@
 
 #include "k_decode.cu"
 #include "k_decode_mma.cu"
+#include "k_prefill.cu"
+#include "k_mass.cu"
 #include "k_select.cu"
 #include "k_sketch.cu"
 
@@ -127,6 +129,24 @@ sa_status_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
     return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d): inner=%llu rows=%llu stride=%llu box=%ux%u", (int)r,
                 (unsigned long long)inner, (unsigned long long)rows, (unsigned long long)row_stride_bytes, box_inner,
                 box_rows);
+  return SA_OK;
+}
+
+// 3-D tiled map: dims {d0 (contiguous), d1, d2}, byte strides of dims 1 and 2.
+sa_status_t make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                        CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc;
+  SA_TRY(get_encode(&enc));
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d): dims %llu x %llu x %llu", (int)r,
+                (unsigned long long)d0, (unsigned long long)d1, (unsigned long long)d2);
   return SA_OK;
 }
 
@@ -519,13 +539,78 @@ sa_status_t validate_select(const SelectArgs& a) {
 }
 
 // ---------------------------------------------------------- prefill / mass
-sa_status_t prefill_impl(const void*, const void*, const void*, const int32_t*, const int32_t*, int, int, int, int,
-                         int, float, void*, float*, cudaStream_t) {
-  return fail(SA_ERR_UNSUPPORTED, "sa_prefill: not built yet");
+sa_status_t prefill_impl(const void* q, const void* k, const void* v, const int32_t* idx, const int32_t* cnt,
+                         int kmax, int B, int L, int Hq, int Hkv, float scale, void* out, float* lse,
+                         cudaStream_t st) {
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  constexpr int D = 128;
+  sa::PfParams p;
+  p.idx = idx;
+  p.cnt = cnt;
+  p.kmax = kmax;
+  p.L = L;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.groups = B * Hkv;
+  p.nq = cdiv(L, sa::kPfRows);
+  p.nb = cdiv(L, sa::kPfKeys);
+  p.npairs = cdiv(p.G, 2);
+  const long long units = static_cast<long long>(p.groups) * p.nq * p.npairs;
+  SA_ARG(units < (1LL << 31), "too many prefill work units");
+  p.units = static_cast<int>(units);
+  p.qscale = scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  CUtensorMap qm, km, vm;
+  SA_TRY(make_map_3d(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, D, Hq, static_cast<uint64_t>(B) * L, D * 2,
+                     static_cast<uint64_t>(Hq) * D * 2, 64, 1, sa::kPfRows, CU_TENSOR_MAP_SWIZZLE_128B));
+  const uint64_t rows = static_cast<uint64_t>(B) * Hkv * L;
+  SA_TRY(make_map_2d(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, D, rows, D * 2, 64, sa::kPfKeys,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  SA_TRY(make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, D, rows, D * 2, 64, sa::kPfKeys,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  SA_TRY(set_smem(sa::prefill_kernel, sa::PfSmem::kBytes));
+  const int grid = static_cast<int>(std::min<long long>(units, di.sms));
+  sa::prefill_kernel<<<grid, sa::kPfThreads, sa::PfSmem::kBytes, st>>>(qm, km, vm, p);
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
 }
 size_t mass_ws_bytes(int, int, int, int, int, int) { return 0; }
-sa_status_t mass_impl(const void*, const void*, int, int, int, int, float, float*, void*, cudaStream_t) {
-  return fail(SA_ERR_UNSUPPORTED, "sa_oracle_mass: not built yet");
+
+sa_status_t mass_impl(const void* q, const void* k, int B, int L, int Hq, int Hkv, float scale, float* mass,
+                      cudaStream_t st) {
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  constexpr int D = 128;
+  sa::MsParams p;
+  p.L = L;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.groups = B * Hkv;
+  p.nq = cdiv(L, sa::kPfRows);
+  p.nb = cdiv(L, sa::kPfKeys);
+  p.npairs = cdiv(p.G, 2);
+  SA_SUP(p.nb <= sa::kMsMaxBlocks, "oracle mass supports at most %d key blocks (L <= %d)", sa::kMsMaxBlocks,
+         sa::kMsMaxBlocks * sa::kPfKeys);
+  const long long units = static_cast<long long>(p.groups) * p.nq;
+  SA_ARG(units < (1LL << 31), "too many work units");
+  p.units = static_cast<int>(units);
+  p.qscale = scale * 1.4426950408889634f;
+  p.mass = mass;
+  CUtensorMap qm, km;
+  SA_TRY(make_map_3d(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, D, Hq, static_cast<uint64_t>(B) * L, D * 2,
+                     static_cast<uint64_t>(Hq) * D * 2, 64, 1, sa::kPfRows, CU_TENSOR_MAP_SWIZZLE_128B));
+  SA_TRY(make_map_2d(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, D, static_cast<uint64_t>(B) * Hkv * L, D * 2, 64,
+                     sa::kPfKeys, CU_TENSOR_MAP_SWIZZLE_128B));
+  const int smem = sa::MsSmem::bytes(p.nb);
+  SA_TRY(set_smem(sa::mass_kernel, smem));
+  const int grid = static_cast<int>(std::min<long long>(units, di.sms));
+  sa::mass_kernel<<<grid, sa::kMsThreads, smem, st>>>(qm, km, p);
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
 }
 
 }  // namespace
@@ -633,6 +718,10 @@ sa_status_t sa_prefill(const void* q, const void* k, const void* v, int dtype, c
   SA_ARG(L >= 1 && kmax >= 1, "L >= 1 and kmax >= 1 required");
   SA_SUP(dtype == SA_BF16 && d == 128 && qtile == 128 && block == 128,
          "prefill supports bf16, d == 128, qtile == block == 128");
+  SA_ARG(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out), "q, k, v, out must be 16-byte aligned");
+  SA_ARG(scale > 0.f && scale < 1e30f, "scale must be positive and finite");
+  SA_ARG(static_cast<long long>(B) * L * Hq < (1LL << 31) && static_cast<long long>(B) * Hkv * L < (1LL << 31),
+         "B*L*Hq and B*Hkv*L must be < 2^31");
   return prefill_impl(q, k, v, idx, cnt, kmax, B, L, Hq, Hkv, scale, out, lse_out, as_stream(stream));
 }
 
@@ -644,14 +733,18 @@ size_t sa_oracle_mass_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int 
 sa_status_t sa_oracle_mass(const void* q, const void* k, int dtype, int B, int L, int Hq, int Hkv, int d, int qtile,
                            int block, float scale, float* mass, void* workspace, size_t ws_bytes, void* stream) {
   t_err.clear();
+  (void)workspace;
+  (void)ws_bytes;
   SA_TRY(check_common(dtype, B, Hq, Hkv, d));
   SA_ARG(q && k && mass, "null pointer argument");
   SA_ARG(L >= 1, "L >= 1 required");
   SA_SUP(dtype == SA_BF16 && d == 128 && qtile == 128 && block == 128,
          "oracle mass supports bf16, d == 128, qtile == block == 128");
-  const size_t need = mass_ws_bytes(B, L, Hq, Hkv, qtile, block);
-  SA_ARG(need == 0 || (workspace && ws_bytes >= need), "workspace too small: %zu < %zu bytes", ws_bytes, need);
-  return mass_impl(q, k, B, L, Hq, Hkv, scale, mass, workspace, as_stream(stream));
+  SA_ARG(aligned16(q) && aligned16(k), "q and k must be 16-byte aligned");
+  SA_ARG(scale > 0.f && scale < 1e30f, "scale must be positive and finite");
+  SA_ARG(static_cast<long long>(B) * L * Hq < (1LL << 31) && static_cast<long long>(B) * Hkv * L < (1LL << 31),
+         "B*L*Hq and B*Hkv*L must be < 2^31");
+  return mass_impl(q, k, B, L, Hq, Hkv, scale, mass, as_stream(stream));
 }
 
 size_t sa_decode_step_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int dtype, int kmax) {
