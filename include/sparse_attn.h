@@ -173,6 +173,33 @@ sa_status_t sa_decode(const void* q, const void* k_cache, const void* v_cache, i
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * sa_decode without a workspace argument, for callers that cannot allocate
+ * device memory: code embedded in a host runtime that owns the whole device
+ * memory pool and gives its plugins no allocation hook, or a latency-critical
+ * path that must not pay for cudaMalloc (which can synchronize the device).
+ * The pages have no counterpart of this call; it is a deployment variant of
+ * sa_decode with the same arguments, layouts and results.
+ *
+ * Scratch: the library keeps one fixed array of 8 MiB (8388608 bytes) in
+ * device memory for this call, on every device that loads the library, until
+ * the process exits.  A problem whose sa_decode_workspace_bytes(...) exceeds
+ * 8 MiB is rejected with SA_ERR_INVALID_ARG before any device work.  No device
+ * memory is allocated by this call.
+ *
+ * The first call made with a given device current looks up the array's device
+ * address on that device (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  Each call clears the arrival counters at the head of
+ * the array on `stream`, then runs the same kernels as sa_decode.  All calls
+ * share the one array: calls that overlap on the device (on different streams,
+ * or from several host threads without ordering) race on it and give wrong
+ * results; order them on one stream or with events.
+ */
+sa_status_t sa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, int dtype,
+                              const int32_t* idx, const int32_t* cnt, int kmax, int B, int T, int Hq,
+                              int Hkv, int d, int L, int L_stride, int block, float scale, void* out,
+                              void* stream);
+
+/*
  * a4, prefill. Causal exact attention per query tile over the tile's
  * selected blocks ("How Much Dense Attention is Necessary?" Sec. 2.1,
  * support shared by the tile; "The Sparse Frontier" RQ2, block-sparse

@@ -52,6 +52,7 @@ SIGNATURES = {
     "sa_select_kmax": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "sa_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "sa_decode": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "sa_decode_noalloc": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "sa_prefill": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp], _i),
     "sa_oracle_mass_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "sa_oracle_mass": ([_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
@@ -150,6 +151,15 @@ def sa_decode(q, k_cache, v_cache, idx, cnt, L, block, scale, out, workspace, st
     _check(lib.sa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(q), _ptr(idx), _ptr(cnt), kmax, B, T, Hq, Hkv,
                          d, L, Ls, block, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
                          _stream(stream)))
+
+
+def sa_decode_noalloc(q, k_cache, v_cache, idx, cnt, L, block, scale, out, stream=None):
+    """sa_decode with the library's fixed scratch instead of a workspace (for callers that cannot allocate)."""
+    B, T, Hq, d = q.shape
+    Hkv, Ls = k_cache.shape[1], k_cache.shape[2]
+    kmax = idx.shape[-1]
+    _check(lib.sa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(q), _ptr(idx), _ptr(cnt), kmax, B, T,
+                                 Hq, Hkv, d, L, Ls, block, float(scale), _ptr(out), _stream(stream)))
 
 
 def sa_prefill(q, k, v, idx, cnt, qtile, block, scale, out, lse=None, stream=None):

@@ -801,3 +801,6 @@ sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, 
 }
 
 }  // extern "C"
+
+// The allocation-free decode entry point (needs the helpers above).
+#include "sa_noalloc.cu"
