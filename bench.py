@@ -13,8 +13,15 @@ Prints ONE JSON line.  `value` = bytes the step must move (selected K/V blocks
 blocks in L2.  `e2e` = the same bytes / wall time per step through the C-ABI
 decode-step call with pinned host q/k_new/v_new/out, copies included.
 
+The same line carries a `prefill` list with the two prefill workloads, each
+timed as whole steps on the full workload: sketch-selected prefill (batch 2,
+Hq 32, Hkv 8, context 131072: sketch build + tile scoring/top-k + tcgen05
+sparse prefill) and oracle-mass prefill (batch 1, Hq 16, Hkv 2, context 32768:
+tcgen05 mass + top-k + sparse prefill), with tensor-core rooflines.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload c2|c3]
+                    [--workload c2|c3] [--prefill-steps P] [--prefill-only]
+                    [--prefill-B B --prefill-L L]   (smaller prefill case for profiling)
 """
 from __future__ import annotations
 
@@ -386,6 +393,121 @@ def bench_decode(args, wl, rank, world):
     return res
 
 
+def _events_ms(fn, reps, stream):
+    """Median over reps of the CUDA-event time of fn() on `stream` (one launch sequence each)."""
+    import torch
+    ts = []
+    with torch.cuda.stream(stream):
+        fn()
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def bench_prefill(wl, steps, peaks, peak_src):
+    """One prefill step = (sketch build + sketch select | oracle mass + mass select) + sparse prefill,
+    on the full workload.  Returns a dict with per-kernel times and tensor-core rooflines."""
+    import numpy as np
+    import torch
+
+    import synth
+    import top_block_sparse_pooled_b300 as sa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = synth.make_inputs(wl)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = up(x.q), up(x.k), up(x.v)
+    del x
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, wl.Qt, True, wl.k, wl.frac_num, wl.frac_den)
+    idx = torch.empty((wl.B, wl.Hkv, wl.nq, kmax), dtype=torch.int32, device=dev)
+    cnt = torch.empty((wl.B, wl.Hkv, wl.nq), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream(device=dev)
+    if wl.mode == "mass":
+        mass = torch.empty((wl.B, wl.Hkv, wl.nq, wl.nb), dtype=torch.float32, device=dev)
+
+        def score():
+            sa.sa_oracle_mass(q, k, wl.Qt, wl.Bk, wl.scale, mass, None)
+
+        def select():
+            sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, mass, wl.Hkv, wl.L, wl.L, wl.Bk, wl.Qt, True, wl.k,
+                              wl.frac_num, wl.frac_den, wl.scale, idx, cnt, d=wl.d, dtype=sa.SA_BF16, B=wl.B,
+                              Tq=wl.L, Hq=wl.Hq)
+    else:
+        sk = torch.empty((wl.B, wl.Hkv, wl.nb, wl.d), dtype=torch.float32, device=dev)
+
+        def score():
+            sa.sa_build_sketch(k, wl.L, wl.Bk, sk)
+
+        def select():
+            sa.sa_select_topk(sa.SA_SELECT_SKETCH, q, sk, None, wl.Hkv, wl.L, wl.L, wl.Bk, wl.Qt, True, wl.k,
+                              wl.frac_num, wl.frac_den, wl.scale, idx, cnt)
+
+    def attend():
+        sa.sa_prefill(q, k, v, idx, cnt, wl.Qt, wl.Bk, wl.scale, out)
+
+    def step():
+        score()
+        select()
+        attend()
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    if sa.sa_device_status() != 0:
+        raise RuntimeError("device status word set during prefill warm-up")
+    t_step = _events_ms(lambda: [step() for _ in range(steps)], 1, stream) / steps
+    reps = max(3, steps)
+    t_score = _events_ms(score, reps, stream)
+    t_select = _events_ms(select, reps, stream)
+    t_attend = _events_ms(attend, reps, stream)
+    pairs = int(cnt.sum().item())  # (group, tile, block) triples executed
+    tile_flops = 4 * wl.d * wl.Qt * wl.Bk  # QK^T + PV of one 128 x 128 tile, one head
+    executed = pairs * wl.G * tile_flops
+    causal_tiles = wl.B * wl.Hkv * sum(min(i + 1, wl.nb) for i in range(wl.nq))
+    dense = causal_tiles * wl.G * tile_flops
+    achieved = executed / (t_attend * 1e-3) / 1e12
+    res = {
+        "workload": "%s %s prefill: B=%d Hq=%d Hkv=%d d=%d L=%d qtile=%d block=%d, %s top-%d%%+sink+diagonal" % (
+            wl.name, wl.mode, wl.B, wl.Hq, wl.Hkv, wl.d, wl.L, wl.Qt, wl.Bk,
+            "oracle-mass" if wl.mode == "mass" else "mean-key sketch", round(100 * wl.frac_num / wl.frac_den)),
+        "ms_per_step": round(t_step, 4),
+        "steps": steps,
+        "kernels_ms": {"score": round(t_score, 4), "select": round(t_select, 4), "prefill": round(t_attend, 4)},
+        "selected_tiles": pairs,
+        "causal_tiles": causal_tiles,
+        "executed_tflop": round(executed / 1e12, 4),
+        "dense_causal_tflop": round(dense / 1e12, 3),
+        "tflops_executed": round(achieved, 2),
+        "tflops_dense_equivalent": round(dense / (t_attend * 1e-3) / 1e12, 1),
+        "roofline": {"kernel": "sa_prefill (prefill_kernel, tcgen05)", "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_tflops"], "peak_source": peak_src + " bf16 burst", "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                     "avg_launch_ms": round(t_attend, 4), "algorithmic_flop_per_launch": executed},
+        "l2": "inputs %.2f GB resident, larger than L2" % ((q.numel() + k.numel() + v.numel()) * 2 / 1e9),
+    }
+    if wl.mode == "mass":
+        mass_flops = 2 * 2 * wl.d * wl.Qt * wl.Bk * wl.G * causal_tiles
+        res["mass_roofline"] = {"kernel": "sa_oracle_mass (mass_kernel, tcgen05)", "bound": "tensor",
+                                "achieved": round(mass_flops / (t_score * 1e-3) / 1e12, 2),
+                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": round(mass_flops / (t_score * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                                "algorithmic_flop_per_launch": mass_flops}
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def _kernel_hash():
     import hashlib
     h = hashlib.sha256()
@@ -452,6 +574,11 @@ def main():
     ap.add_argument("--rotate", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--prefill-steps", type=int, default=5,
+                    help="steps of each prefill leg (c5 sketch-selected, c4 oracle-mass); 0 skips them")
+    ap.add_argument("--prefill-only", action="store_true", help="run only the prefill legs (profiling)")
+    ap.add_argument("--prefill-B", type=int, default=0, help="override the prefill legs' batch (profiling)")
+    ap.add_argument("--prefill-L", type=int, default=0, help="override the prefill legs' context (profiling)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -467,7 +594,25 @@ def main():
     if args.impl == "reference":
         res = bench_reference(args, wl, rank, world)
     else:
-        res = bench_decode(args, wl, rank, world)
+        def pf_wl(name):
+            w = workload(name)
+            if args.prefill_B:
+                w = w.replace(B=args.prefill_B)
+            if args.prefill_L:
+                w = w.replace(L=args.prefill_L)
+            return w
+
+        if args.prefill_only:
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            peaks, src = load_peaks()
+            res = {"prefill": [bench_prefill(pf_wl(n), max(1, args.prefill_steps), peaks, src) for n in ("c5", "c4")]}
+        else:
+            res = bench_decode(args, wl, rank, world)
+            if args.prefill_steps > 0 and res is not None:
+                peaks, src = load_peaks()
+                res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src) for n in ("c5", "c4")]
+                res["gpu_launches"] += 3 * args.prefill_steps * 2
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:
