@@ -444,12 +444,13 @@ def bench_prefill(wl, steps, peaks, peak_src):
                               Tq=wl.L, Hq=wl.Hq)
     else:
         sk = torch.empty((wl.B, wl.Hkv, wl.nb, wl.d), dtype=torch.float32, device=dev)
+        tile_scores = torch.empty((wl.B, wl.Hkv, wl.nq, wl.nb), dtype=torch.float32, device=dev)
 
         def score():
             sa.sa_build_sketch(k, wl.L, wl.Bk, sk)
 
         def select():
-            sa.sa_select_topk(sa.SA_SELECT_SKETCH, q, sk, None, wl.Hkv, wl.L, wl.L, wl.Bk, wl.Qt, True, wl.k,
+            sa.sa_select_topk(sa.SA_SELECT_SKETCH, q, sk, tile_scores, wl.Hkv, wl.L, wl.L, wl.Bk, wl.Qt, True, wl.k,
                               wl.frac_num, wl.frac_den, wl.scale, idx, cnt)
 
     def attend():
@@ -612,7 +613,7 @@ def main():
             if args.prefill_steps > 0 and res is not None:
                 peaks, src = load_peaks()
                 res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src) for n in ("c5", "c4")]
-                res["gpu_launches"] += 3 * args.prefill_steps * 2
+                res["gpu_launches"] += 4 * args.prefill_steps * 2
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

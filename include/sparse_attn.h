@@ -134,14 +134,17 @@ sa_status_t sa_append_kv(const void* k_new, const void* v_new, int dtype, int B,
  *
  * mode SA_SELECT_SKETCH: score s = max over the group's query heads and the
  *   unit's query rows of scale * (q . sketch[g, b]), in float32.  `sketch`
- *   must be given.  If `scores` is not NULL the scores are written there
- *   ([B, Hkv, nq, nb]; non-causal entries of prefill tiles are -inf).
+ *   must be given.  Decode: if `scores` is not NULL the scores are written
+ *   there ([B, Hkv, 1, nb]).  Prefill: `scores` is required and written
+ *   ([B, Hkv, nq, nb]; non-causal entries are -inf); the tile scores are
+ *   computed on the tensor cores (q bf16 times the fp32 sketch split into
+ *   three bf16 parts, fp32 accumulation), then each tile's top-k is taken.
  * mode SA_SELECT_MASS: `scores` is an input (e.g. from sa_oracle_mass);
  *   q and sketch are not read.
  * idx: [B, Hkv, nq, kmax] int32 written (ascending, -1 padded), cnt:
  *   [B, Hkv, nq] int32 written.  kmax must be >= sa_select_kmax(...).
- * Requires d in {64, 128}; G * Tq <= 32 for decode; qtile == Bk == 128 and
- * d == 128 for prefill in SKETCH mode.
+ * Requires d in {64, 128}; G * Tq <= 32 for decode; qtile == Bk == 128,
+ * d == 128, bf16 q and scale > 0 for prefill in SKETCH mode.
  */
 sa_status_t sa_select_topk(int mode, const void* q, int dtype, const float* sketch, float* scores,
                            int B, int Tq, int Hq, int Hkv, int d, int L, int L_stride, int block,

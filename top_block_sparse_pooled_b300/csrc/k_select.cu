@@ -327,128 +327,4 @@ __global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* 
   block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, S);
 }
 
-// --------------------------------------------------------------------------
-// Prefill sketch selection (CUDA cores, float32).  grid (nq, groups).
-// For tile i: s[b] = max over the group's heads and the tile's rows of
-// scale * q . sketch[b] for b <= i (qtile == Bk), then top-k.
-// Rows are processed in chunks of kPfRowChunk; each thread owns rows and
-// accumulates 32 block scores at a time against a shared sketch slab.
-constexpr int kPfRowChunk = 256;
-constexpr int kPfBlk = 32;
-
-template <int D>
-struct SelPrefillSmem {
-  static constexpr int kQBytes = kPfRowChunk * D * 2;       // bf16 rows, swizzled 16-byte chunks
-  static constexpr int kSkOff = kQBytes;
-  static constexpr int kSkBytes = kPfBlk * D * 4;
-  static constexpr int kRedOff = kSkOff + kSkBytes;
-  static constexpr int kRedBytes = (kSelThreads / 32) * kPfBlk * 4;
-  static constexpr int kScOff = kRedOff + kRedBytes;
-  static constexpr int kMaxBlocks = 8192;
-  static constexpr int kTopkOff = kScOff + kMaxBlocks * 4;
-  static constexpr int kBytes = kTopkOff + ((sizeof(TopkShared) + 15) / 16) * 16;
-};
-
-template <int D>
-__global__ void __launch_bounds__(kSelThreads) select_prefill_sketch_kernel(
-    const __nv_bfloat16* __restrict__ q, const float* __restrict__ sketch, int L, int Hq, int Hkv, int nb_cap,
-    int qtile, int Bk, float scale, int k, int frac_num, int frac_den, float* __restrict__ scores_out, int nb,
-    int32_t* __restrict__ idx, int32_t* __restrict__ cnt, int kmax) {
-  using SM = SelPrefillSmem<D>;
-  extern __shared__ __align__(1024) uint8_t smem_sel_pf[];
-  uint8_t* smem_raw = smem_sel_pf;
-  uint8_t* q_s = smem_raw;
-  float* sk_s = reinterpret_cast<float*>(smem_raw + SM::kSkOff);
-  float* red = reinterpret_cast<float*>(smem_raw + SM::kRedOff);
-  float* sc = reinterpret_cast<float*>(smem_raw + SM::kScOff);
-  TopkShared& S = *reinterpret_cast<TopkShared*>(smem_raw + SM::kTopkOff);
-  constexpr int CPR = D / 8;  // 16-byte chunks per bf16 row
-
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int i = blockIdx.x, g = blockIdx.y, nq = gridDim.x;
-  const int G = Hq / Hkv, b = g / Hkv, kvh = g % Hkv;
-  const int t0 = i * qtile, t1 = min(t0 + qtile, L);
-  const int nvalid = (t1 - 1) / Bk + 1;
-  const int nrows = (t1 - t0) * G;
-  for (int bb = tid; bb < nvalid; bb += kSelThreads) sc[bb] = -INFINITY;
-  __syncthreads();
-  for (int rc = 0; rc < nrows; rc += kPfRowChunk) {
-    const int nr = min(kPfRowChunk, nrows - rc);
-    // stage rows (row r of the chunk = tile row (rc + r) / G, head (rc + r) % G)
-    for (int e = tid; e < nr * CPR; e += kSelThreads) {
-      const int r = e / CPR, c = e % CPR;
-      const int rr = rc + r;
-      const int t = t0 + rr / G, h = kvh * G + rr % G;
-      const uint4 v = *reinterpret_cast<const uint4*>(q + ((static_cast<size_t>(b) * L + t) * Hq + h) * D + c * 8);
-      *reinterpret_cast<uint4*>(q_s + r * (D * 2) + ((c ^ (r & (CPR - 1))) << 4)) = v;
-    }
-    __syncthreads();
-    for (int bs = 0; bs < nvalid; bs += kPfBlk) {
-      const int nbk = min(kPfBlk, nvalid - bs);
-      for (int e = tid; e < kPfBlk * D; e += kSelThreads) {
-        const int bb = e / D;
-        sk_s[e] = bb < nbk ? sketch[(static_cast<size_t>(g) * nb_cap + bs + bb) * D + e % D] * scale : 0.f;
-      }
-      __syncthreads();
-      float mx[kPfBlk];
-#pragma unroll
-      for (int j = 0; j < kPfBlk; ++j) mx[j] = -INFINITY;
-      for (int r = tid; r < nr; r += kSelThreads) {
-        float acc[kPfBlk];
-#pragma unroll
-        for (int j = 0; j < kPfBlk; ++j) acc[j] = 0.f;
-        for (int c = 0; c < CPR; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(q_s + r * (D * 2) + ((c ^ (r & (CPR - 1))) << 4));
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-          float qf[8];
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            qf[2 * e2] = __uint_as_float(wv[e2] << 16);
-            qf[2 * e2 + 1] = __uint_as_float(wv[e2] & 0xFFFF0000u);
-          }
-#pragma unroll
-          for (int j = 0; j < kPfBlk; ++j) {
-            const float4 s0 = *reinterpret_cast<const float4*>(sk_s + j * D + c * 8);
-            const float4 s1 = *reinterpret_cast<const float4*>(sk_s + j * D + c * 8 + 4);
-            float a = acc[j];
-            a = fmaf(qf[0], s0.x, a);
-            a = fmaf(qf[1], s0.y, a);
-            a = fmaf(qf[2], s0.z, a);
-            a = fmaf(qf[3], s0.w, a);
-            a = fmaf(qf[4], s1.x, a);
-            a = fmaf(qf[5], s1.y, a);
-            a = fmaf(qf[6], s1.z, a);
-            a = fmaf(qf[7], s1.w, a);
-            acc[j] = a;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kPfBlk; ++j) mx[j] = fmaxf(mx[j], acc[j]);
-      }
-      // max over the CTA's rows for each of the kPfBlk blocks
-#pragma unroll
-      for (int j = 0; j < kPfBlk; ++j) {
-        float v = mx[j];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-        if (lane == 0) red[w * kPfBlk + j] = v;
-      }
-      __syncthreads();
-      if (tid < nbk) {
-        float v = -INFINITY;
-        for (int ww = 0; ww < kSelThreads / 32; ++ww) v = fmaxf(v, red[ww * kPfBlk + tid]);
-        sc[bs + tid] = fmaxf(sc[bs + tid], v);
-      }
-      __syncthreads();
-    }
-  }
-  const size_t u = static_cast<size_t>(g) * nq + i;
-  if (scores_out)
-    for (int bb = tid; bb < nb; bb += kSelThreads) scores_out[u * nb + bb] = bb < nvalid ? sc[bb] : -INFINITY;
-  int budget = k;
-  if (frac_num > 0) budget = k + (frac_num * nvalid + frac_den - 1) / frac_den;
-  __syncthreads();
-  block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, S);
-}
-
 }  // namespace sa

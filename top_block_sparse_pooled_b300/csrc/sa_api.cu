@@ -18,6 +18,7 @@
 #include "k_prefill.cu"
 #include "k_mass.cu"
 #include "k_select.cu"
+#include "k_score.cu"
 #include "k_sketch.cu"
 
 namespace {
@@ -305,22 +306,34 @@ sa_status_t run_select(const SelectArgs& a, cudaStream_t st) {
     return a.d == 128 ? dispatch_select_decode_r<__nv_bfloat16, 128>(a, di, st)
                       : dispatch_select_decode_r<__nv_bfloat16, 64>(a, di, st);
   }
-  // prefill, sketch mode (bf16 queries)
+  // prefill, sketch mode: tensor-core tile scoring into `scores`, then the top-k of each tile
   const int nq = cdiv(a.L, a.qtile);
-  const int nb_cap = cdiv(a.Ls, a.block);
-  if (a.d == 128) {
-    using SM = sa::SelPrefillSmem<128>;
-    SA_TRY(set_smem(sa::select_prefill_sketch_kernel<128>, SM::kBytes));
-    sa::select_prefill_sketch_kernel<128><<<dim3(nq, groups), sa::kSelThreads, SM::kBytes, st>>>(
-        static_cast<const __nv_bfloat16*>(a.q), a.sketch, a.L, a.Hq, a.Hkv, nb_cap, a.qtile, a.block, a.scale, a.k,
-        a.frac_num, a.frac_den, a.scores, nb, a.idx, a.cnt, a.kmax);
-  } else {
-    using SM = sa::SelPrefillSmem<64>;
-    SA_TRY(set_smem(sa::select_prefill_sketch_kernel<64>, SM::kBytes));
-    sa::select_prefill_sketch_kernel<64><<<dim3(nq, groups), sa::kSelThreads, SM::kBytes, st>>>(
-        static_cast<const __nv_bfloat16*>(a.q), a.sketch, a.L, a.Hq, a.Hkv, nb_cap, a.qtile, a.block, a.scale, a.k,
-        a.frac_num, a.frac_den, a.scores, nb, a.idx, a.cnt, a.kmax);
-  }
+  sa::ScParams p;
+  p.sketch = a.sketch;
+  p.scores = a.scores;
+  p.L = a.L;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.groups = groups;
+  p.nq = nq;
+  p.nb = nb;
+  p.nb_cap = cdiv(a.Ls, a.block);
+  const long long units = static_cast<long long>(groups) * nq;
+  SA_ARG(units < (1LL << 31), "too many tiles");
+  p.units = static_cast<int>(units);
+  p.scale = a.scale;
+  CUtensorMap qm;
+  SA_TRY(make_map_3d(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, 128, a.Hq, static_cast<uint64_t>(a.B) * a.L, 256,
+                     static_cast<uint64_t>(a.Hq) * 256, 64, 1, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+  SA_TRY(set_smem(sa::score_prefill_kernel, sa::ScSmem::kBytes));
+  const int grid = static_cast<int>(std::min<long long>(units, di.sms));
+  sa::score_prefill_kernel<<<grid, sa::kScThreads, sa::ScSmem::kBytes, st>>>(qm, p);
+  SA_CUDA(cudaGetLastError());
+  const int smem = static_cast<int>(((sizeof(sa::TopkShared) + 15) / 16) * 16) + nb * 4;
+  SA_TRY(set_smem(sa::select_given_kernel, smem));
+  sa::select_given_kernel<<<dim3(nq, groups), sa::kSelThreads, smem, st>>>(
+      a.scores, nb, 1, a.L, a.qtile, a.block, a.k, a.frac_num, a.frac_den, a.idx, a.cnt, a.kmax);
   SA_CUDA(cudaGetLastError());
   return SA_OK;
 }
@@ -530,10 +543,12 @@ sa_status_t validate_select(const SelectArgs& a) {
     SA_ARG(a.Tq >= 1, "Tq must be >= 1");
     SA_SUP((a.Hq / a.Hkv) * a.Tq <= 32, "G*Tq (%d) must be <= 32 for decode selection", (a.Hq / a.Hkv) * a.Tq);
   } else {
-    SA_SUP(a.dtype == SA_BF16, "prefill sketch selection needs bf16 queries");
-    SA_SUP(nb <= sa::SelPrefillSmem<128>::kMaxBlocks, "prefill sketch selection supports <= %d blocks",
-           sa::SelPrefillSmem<128>::kMaxBlocks);
+    SA_SUP(a.dtype == SA_BF16 && a.d == 128 && a.qtile == 128 && a.block == 128,
+           "prefill sketch selection supports bf16 queries, d == 128, qtile == block == 128");
+    SA_ARG(a.scores != nullptr, "prefill sketch selection needs the scores array (it is written)");
     SA_ARG(aligned16(a.q), "q must be 16-byte aligned");
+    SA_ARG(a.scale > 0.f && a.scale < 1e30f, "scale must be positive and finite");
+    SA_ARG(static_cast<long long>(a.B) * a.L * a.Hq < (1LL << 31), "B*L*Hq must be < 2^31");
   }
   return SA_OK;
 }
