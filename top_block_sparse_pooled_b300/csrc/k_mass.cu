@@ -192,36 +192,45 @@ __global__ void __launch_bounds__(kMsThreads, 1) mass_kernel(const __grid_consta
             tc::fence_after_sync();
             const uint32_t s_addr = lane_base + (2 * t + buf) * 128;
             const int lim = live ? qpos - j * kPfKeys : -1;  // last visible key column
+            const bool full = lim >= kPfKeys - 1;            // every key of the block visible
+            // the whole row of S in registers (two loads per wait), then S_t[buf] is free
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; c += 2) {
+              tc::tmem_ld32(s_addr + 32 * c, s + 32 * c);
+              tc::tmem_ld32(s_addr + 32 * c + 32, s + 32 * c + 32);
+            }
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            mbar_arrive(bar(MsSmem::S_FREE + 2 * t + buf));
+            if (!full) {
+#pragma unroll
+              for (int e = 0; e < 128; ++e) s[e] = (e <= lim) ? s[e] : -INFINITY;
+            }
             float rs = 0.f;
+            if (pass == 0) {
+              // online log-sum-exp (base 2): block max first, then one exp per key
+              float m8[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float s[32];
-              tc::tmem_ld32(s_addr + 32 * c, s);
-              tc::tmem_wait_ld();
-              if (c == 3) {
-                tc::fence_before_sync();
-                mbar_arrive(bar(MsSmem::S_FREE + 2 * t + buf));
+              for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+#pragma unroll
+              for (int e = 0; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[e]);
+              float bm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+              bm = (bm == -INFINITY) ? -INFINITY : bm * p.qscale;
+              const float mn = fmaxf(m, bm);
+              if (mn != -INFINITY) {
+                float c4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 128; ++e) c4[e & 3] += ex2_approx(fmaf(s[e], p.qscale, -mn));
+                l = l * ex2_approx(m - mn) + ((c4[0] + c4[1]) + (c4[2] + c4[3]));
+                m = mn;
               }
-              if (pass == 0) {
-                float cm = -INFINITY;
+            } else {
+              float c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  s[e] = (32 * c + e <= lim) ? s[e] * p.qscale : -INFINITY;
-                  cm = fmaxf(cm, s[e]);
-                }
-                const float mn = fmaxf(m, cm);
-                if (mn != -INFINITY) {
-                  float cs = 0.f;
-#pragma unroll
-                  for (int e = 0; e < 32; ++e) cs += exp2f(s[e] - mn);
-                  l = l * exp2f(m - mn) + cs;
-                  m = mn;
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  rs += (32 * c + e <= lim) ? exp2f(fmaf(s[e], p.qscale, -lse2)) : 0.f;
-              }
+              for (int e = 0; e < 128; ++e) c4[e & 3] += ex2_approx(fmaf(s[e], p.qscale, -lse2));
+              rs = (c4[0] + c4[1]) + (c4[2] + c4[3]);
             }
             if (pass == 1) {
 #pragma unroll

@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         const PfUnit w = pf_unit(p, u);
         if (ok) ok = mbar_wait(bar(PfSmem::Q_FULL), nu & 1);
         tc::fence_after_sync();
+        int last_valid = w.n - 1;  // Q is released right after the S MMAs of the unit's last block
+        while (last_valid >= 0 && !pf_valid(w.ids[last_valid], p.nb)) --last_valid;
+        if (last_valid < 0) tc::mma_commit(bar(PfSmem::Q_EMPTY));
         int jj = 0;
         for (int j = 0; j < w.n; ++j) {
           const int blk = w.ids[j];
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             tc::mma_commit(bar(PfSmem::S_FULL + t));
           }
           tc::mma_commit(bar(PfSmem::K_EMPTY + s));
+          if (j == last_valid) tc::mma_commit(bar(PfSmem::Q_EMPTY));
           if (ok) ok = mbar_wait(bar(PfSmem::V_FULL + s), ph);
           tc::fence_after_sync();
           const uint32_t vst = sbase + PfSmem::kV + s * kPfTile;
@@ -235,7 +239,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           ++it;
           ++jj;
         }
-        tc::mma_commit(bar(PfSmem::Q_EMPTY));
         for (int t = 0; t < w.nt; ++t) ++units_t[t];
       }
       // drain: every MMA issued has completed before TMEM is freed
@@ -264,18 +267,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         ok = __all_sync(0xFFFFFFFFu, ok);  // keep the warp converged for its TMEM accesses
         ++s_waits;
         tc::fence_after_sync();
-        // pass 1: row max over the visible keys (raw dot products; qscale > 0)
+        // pass 1: row max over the visible keys (raw dot products; qscale > 0).
+        // Two 32-column loads in flight, eight independent max chains.
         const int kbase = blk * kPfKeys;
         const bool full = kbase + kPfKeys - 1 <= qpos && kbase + kPfKeys <= p.L;
         const int lim = full ? kPfKeys - 1 : min(qpos, p.L - 1) - kbase;  // last visible key column
-        float mx = -INFINITY;
+        float mx;
+        {
+          float m8[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float s[32];
-          tc::tmem_ld32(s_addr + 32 * c, s);
-          tc::tmem_wait_ld();
+          for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, (32 * c + e <= lim) ? s[e] : -INFINITY);
+          for (int c = 0; c < 4; c += 2) {
+            float s0[32], s1[32];
+            tc::tmem_ld32(s_addr + 32 * c, s0);
+            tc::tmem_ld32(s_addr + 32 * c + 32, s1);
+            tc::tmem_wait_ld();
+            if (full) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], fmaxf(s0[e], s1[e]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float a0 = (32 * c + e <= lim) ? s0[e] : -INFINITY;
+                const float a1 = (32 * c + 32 + e <= lim) ? s1[e] : -INFINITY;
+                m8[e & 7] = fmaxf(m8[e & 7], fmaxf(a0, a1));
+              }
+            }
+          }
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
         mx = (mx == -INFINITY) ? -INFINITY : mx * p.qscale;
         if (jj > 0) {  // PV_t of the previous block has completed: O_t is stable
@@ -304,24 +324,42 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // pass 2: P = exp2(S * qscale - m) as bf16 pairs into columns 0-63 of S_t
         // (chunk c's pairs land on columns 16c..16c+15, already read)
         const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-        float ls = 0.f;
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float s[32];
-          tc::tmem_ld32(s_addr + 32 * c, s);
+        for (int c = 0; c < 4; c += 2) {
+          float s0[32], s1[32];
+          tc::tmem_ld32(s_addr + 32 * c, s0);
+          tc::tmem_ld32(s_addr + 32 * c + 32, s1);
           tc::tmem_wait_ld();
-          uint32_t pk[16];
+          uint32_t pk0[16], pk1[16];
+          if (full) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = 32 * c + 2 * e;
-            const float a0 = (c0 <= lim) ? exp2f(fmaf(s[2 * e], p.qscale, -mu)) : 0.f;
-            const float a1 = (c0 + 1 <= lim) ? exp2f(fmaf(s[2 * e + 1], p.qscale, -mu)) : 0.f;
-            ls += a0 + a1;
-            __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-            pk[e] = *reinterpret_cast<uint32_t*>(&h);
+            for (int e = 0; e < 16; ++e) {
+              const float a0 = ex2_approx(fmaf(s0[2 * e], p.qscale, -mu));
+              const float a1 = ex2_approx(fmaf(s0[2 * e + 1], p.qscale, -mu));
+              const float b0 = ex2_approx(fmaf(s1[2 * e], p.qscale, -mu));
+              const float b1 = ex2_approx(fmaf(s1[2 * e + 1], p.qscale, -mu));
+              ls4[e & 3] += (a0 + a1) + (b0 + b1);
+              pk0[e] = pack_bf16x2(a0, a1);
+              pk1[e] = pack_bf16x2(b0, b1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c0 = 32 * c + 2 * e;
+              const float a0 = (c0 <= lim) ? ex2_approx(fmaf(s0[2 * e], p.qscale, -mu)) : 0.f;
+              const float a1 = (c0 + 1 <= lim) ? ex2_approx(fmaf(s0[2 * e + 1], p.qscale, -mu)) : 0.f;
+              const float b0 = (c0 + 32 <= lim) ? ex2_approx(fmaf(s1[2 * e], p.qscale, -mu)) : 0.f;
+              const float b1 = (c0 + 33 <= lim) ? ex2_approx(fmaf(s1[2 * e + 1], p.qscale, -mu)) : 0.f;
+              ls4[e & 3] += (a0 + a1) + (b0 + b1);
+              pk0[e] = pack_bf16x2(a0, a1);
+              pk1[e] = pack_bf16x2(b0, b1);
+            }
           }
-          tc::tmem_st16(s_addr + 16 * c, pk);
+          tc::tmem_st16(s_addr + 16 * c, pk0);
+          tc::tmem_st16(s_addr + 16 * c + 16, pk1);
         }
+        const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         l_run += ls;
         tc::tmem_wait_st();
         tc::fence_before_sync();

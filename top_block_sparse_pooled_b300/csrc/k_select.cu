@@ -233,10 +233,17 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
   const int b0 = static_cast<int>(rank) * per;
   const int b1 = min(nb, b0 + per);
 
+  auto issue_tile = [&](int t0) {  // thread 0: the sketch rows t0 .. t0 + tile_rows - 1 of this group
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(lay.tile_bytes));
+#pragma unroll
+    for (int bx = 0; bx < kBoxes; ++bx)
+      tma_g2s_2d(smem_u32(smem + bx * tile_rows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
+  };
   if (tid == 0) {
     prefetch_tmap(&sk_map);
     mbar_init(bar, 1);
     fence_mbar_init();
+    if (b0 < b1) issue_tile(b0);  // the first tile's copy overlaps the q staging below
   }
   for (int i = tid; i < RMAX * D; i += kSelThreads) {
     const int r = i / D, c = i % D;
@@ -254,12 +261,7 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
   bool ok = true;
   uint32_t phase = 0;
   for (int t0 = b0; t0 < b1; t0 += tile_rows) {
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(lay.tile_bytes));
-#pragma unroll
-      for (int bx = 0; bx < kBoxes; ++bx)
-        tma_g2s_2d(smem_u32(smem + bx * tile_rows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
-    }
+    if (tid == 0 && t0 != b0) issue_tile(t0);
     ok = mbar_wait(bar, phase);
     phase ^= 1;
     if (__syncthreads_or(!ok)) break;

@@ -165,4 +165,20 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: one MUFU op,
+// relative error of a few ulp, subnormal results flushed to zero); used for
+// softmax weights, whose error budget is far larger.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Packs two floats into a bf16x2 word (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 }  // namespace sa
