@@ -106,7 +106,7 @@ struct DmParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kDmThreads, 2) decode_mma_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap vmap,
                                                                    const DmParams p) {
   using C = DmCfg<D>;
@@ -128,18 +128,7 @@ __global__ void __launch_bounds__(kDmThreads, 2) decode_mma_kernel(const __grid_
   const int nu = min(p.per, p.U - u0);
   const int G = p.Hq / p.Hkv;
 
-  // unit list: (group, block id or -1 when the unit is past the group's count)
-  for (int i = tid; i < nu; i += kDmThreads) {
-    const int u = u0 + i;
-    const int g = u / p.kmax, s = u % p.kmax;
-    const int n = min(p.cnt[g], p.kmax);
-    int blk = -1;
-    if (s < n) {
-      blk = p.idx[static_cast<size_t>(g) * p.kmax + s];
-      if (blk < 0 || blk * kDmBk >= p.L) blk = -1;
-    }
-    list[i] = make_int2(g, blk);
-  }
+  pdl_launch_dependents();
   if (tid == 0) {
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
@@ -148,6 +137,17 @@ __global__ void __launch_bounds__(kDmThreads, 2) decode_mma_kernel(const __grid_
       mbar_init(empty0 + 8 * s, kDmConsumers);
     }
     fence_mbar_init();
+  }
+  pdl_wait();  // idx / cnt come from the selection kernel
+  // unit list: (group, block id or -1 when the unit is past the group's count);
+  // the count and the id are loaded together (the id slot is always in bounds)
+  for (int i = tid; i < nu; i += kDmThreads) {
+    const int u = u0 + i;
+    const int g = u / p.kmax, s = u % p.kmax;
+    const int n = p.cnt[g];
+    int blk = p.idx[static_cast<size_t>(g) * p.kmax + s];
+    if (s >= min(n, p.kmax) || blk < 0 || blk * kDmBk >= p.L) blk = -1;
+    list[i] = make_int2(g, blk);
   }
   __syncthreads();
 

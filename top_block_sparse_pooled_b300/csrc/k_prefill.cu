@@ -41,18 +41,24 @@ constexpr int kPfRows = 128;            // query rows per M tile (= qtile)
 constexpr int kPfKeys = 128;            // keys per KV block
 constexpr int kPfTile = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 operand (two 64-column boxes)
 constexpr int kPfBox = 128 * 128;       // bytes of one 64-column box of 128 rows
-constexpr int kPfStages = 2;
-constexpr int kPfThreads = 384;
+#ifndef SA_PF_KSTAGES
+#define SA_PF_KSTAGES 2
+#endif
+constexpr int kPfKStages = SA_PF_KSTAGES;  // K ring (K is consumed first, so it runs ahead)
+constexpr int kPfVStages = 2;              // V ring
+constexpr int kPfThreads = 320;  // warp 0 producer, warp 1 MMA, warps 2-9 two softmax warpgroups
 constexpr float kPfRescale = 8.0f;  // log2 growth of the running max that forces an O rescale
 
 struct PfSmem {
   static constexpr int kQ = 0;                         // [2] M tiles
-  static constexpr int kK = kQ + 2 * kPfTile;          // [kPfStages]
-  static constexpr int kV = kK + kPfStages * kPfTile;  // [kPfStages]
-  static constexpr int kBar = kV + kPfStages * kPfTile;
+  static constexpr int kK = kQ + 2 * kPfTile;           // [kPfKStages]
+  static constexpr int kV = kK + kPfKStages * kPfTile;  // [kPfVStages]
+  static constexpr int kBar = kV + kPfVStages * kPfTile;
   // mbarrier slots (8 bytes each)
-  static constexpr int Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = 4, V_FULL = 6, V_EMPTY = 8, S_FULL = 10,
-                       P_FULL = 12, O_BAR = 14, O_FREE = 16, DONE = 18, NBARS = 19;
+  static constexpr int Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = K_FULL + kPfKStages,
+                       V_FULL = K_EMPTY + kPfKStages, V_EMPTY = V_FULL + kPfVStages, S_FULL = V_EMPTY + kPfVStages,
+                       P_FULL = S_FULL + 2, O_BAR = P_FULL + 2, O_FREE = O_BAR + 2, DONE = O_FREE + 2,
+                       NBARS = DONE + 1;
   static constexpr int kSlot = kBar + NBARS * 8;
   static constexpr int kBytes = kSlot + 16 + 1024;  // + slack for 1024-byte alignment
 };
@@ -111,9 +117,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     prefetch_tmap(&vmap);
     mbar_init(bar(PfSmem::Q_FULL), 1);
     mbar_init(bar(PfSmem::Q_EMPTY), 1);
-    for (int s = 0; s < kPfStages; ++s) {
+    for (int s = 0; s < kPfKStages; ++s) {
       mbar_init(bar(PfSmem::K_FULL + s), 1);
       mbar_init(bar(PfSmem::K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < kPfVStages; ++s) {
       mbar_init(bar(PfSmem::V_FULL + s), 1);
       mbar_init(bar(PfSmem::V_EMPTY + s), 1);
     }
@@ -152,25 +160,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         for (int j = 0; j < w.n; ++j) {
           const int blk = w.ids[j];
           if (!pf_valid(blk, p.nb)) continue;
-          const int s = it % kPfStages;
-          const uint32_t ph = (it / kPfStages) & 1;
+          const int sk = it % kPfKStages, sv = it % kPfVStages;
           const int row = w.g * p.L + blk * kPfKeys;
-          if (it >= kPfStages && ok) ok = mbar_wait(bar(PfSmem::K_EMPTY + s), ph ^ 1);
-          mbar_arrive_expect_tx(bar(PfSmem::K_FULL + s), kPfTile);
+          if (it >= kPfKStages && ok) ok = mbar_wait(bar(PfSmem::K_EMPTY + sk), ((it / kPfKStages) - 1) & 1);
+          mbar_arrive_expect_tx(bar(PfSmem::K_FULL + sk), kPfTile);
           for (int bx = 0; bx < 2; ++bx)
-            tma_g2s_2d(sbase + PfSmem::kK + s * kPfTile + bx * kPfBox, &kmap, bx * 64, row, bar(PfSmem::K_FULL + s));
-          if (it >= kPfStages && ok) ok = mbar_wait(bar(PfSmem::V_EMPTY + s), ph ^ 1);
-          mbar_arrive_expect_tx(bar(PfSmem::V_FULL + s), kPfTile);
+            tma_g2s_2d(sbase + PfSmem::kK + sk * kPfTile + bx * kPfBox, &kmap, bx * 64, row,
+                       bar(PfSmem::K_FULL + sk));
+          if (it >= kPfVStages && ok) ok = mbar_wait(bar(PfSmem::V_EMPTY + sv), ((it / kPfVStages) - 1) & 1);
+          mbar_arrive_expect_tx(bar(PfSmem::V_FULL + sv), kPfTile);
           for (int bx = 0; bx < 2; ++bx)
-            tma_g2s_2d(sbase + PfSmem::kV + s * kPfTile + bx * kPfBox, &vmap, bx * 64, row, bar(PfSmem::V_FULL + s));
+            tma_g2s_2d(sbase + PfSmem::kV + sv * kPfTile + bx * kPfBox, &vmap, bx * 64, row,
+                       bar(PfSmem::V_FULL + sv));
           ++it;
         }
       }
       // never exit with copies in flight: wait for the last fill of each stage and of Q
-      for (uint32_t k = it > kPfStages ? it - kPfStages : 0; k < it; ++k) {
-        mbar_wait_drain(bar(PfSmem::K_FULL + k % kPfStages), (k / kPfStages) & 1);
-        mbar_wait_drain(bar(PfSmem::V_FULL + k % kPfStages), (k / kPfStages) & 1);
-      }
+      for (uint32_t k = it > kPfKStages ? it - kPfKStages : 0; k < it; ++k)
+        mbar_wait_drain(bar(PfSmem::K_FULL + k % kPfKStages), (k / kPfKStages) & 1);
+      for (uint32_t k = it > kPfVStages ? it - kPfVStages : 0; k < it; ++k)
+        mbar_wait_drain(bar(PfSmem::V_FULL + k % kPfVStages), (k / kPfVStages) & 1);
       if (nu > 0) mbar_wait_drain(bar(PfSmem::Q_FULL), (nu - 1) & 1);
     }
   } else if (warp == 1) {
@@ -196,11 +205,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         for (int j = 0; j < w.n; ++j) {
           const int blk = w.ids[j];
           if (!pf_valid(blk, p.nb)) continue;
-          const int s = it % kPfStages;
-          const uint32_t ph = (it / kPfStages) & 1;
-          if (ok) ok = mbar_wait(bar(PfSmem::K_FULL + s), ph);
+          const int sk = it % kPfKStages, sv = it % kPfVStages;
+          if (ok) ok = mbar_wait(bar(PfSmem::K_FULL + sk), (it / kPfKStages) & 1);
           tc::fence_after_sync();
-          const uint32_t kst = sbase + PfSmem::kK + s * kPfTile;
+          const uint32_t kst = sbase + PfSmem::kK + sk * kPfTile;
           for (int t = 0; t < w.nt; ++t) {
             if (pv_pending[t]) {  // P_t (aliasing S_t) must be consumed before S_t is rewritten
               if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), (o_commits[t] - 1) & 1);
@@ -215,11 +223,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             }
             tc::mma_commit(bar(PfSmem::S_FULL + t));
           }
-          tc::mma_commit(bar(PfSmem::K_EMPTY + s));
+          tc::mma_commit(bar(PfSmem::K_EMPTY + sk));
           if (j == last_valid) tc::mma_commit(bar(PfSmem::Q_EMPTY));
-          if (ok) ok = mbar_wait(bar(PfSmem::V_FULL + s), ph);
+          if (ok) ok = mbar_wait(bar(PfSmem::V_FULL + sv), (it / kPfVStages) & 1);
           tc::fence_after_sync();
-          const uint32_t vst = sbase + PfSmem::kV + s * kPfTile;
+          const uint32_t vst = sbase + PfSmem::kV + sv * kPfTile;
           for (int t = 0; t < w.nt; ++t) {
             if (ok) ok = mbar_wait(bar(PfSmem::P_FULL + t), p_waits[t] & 1);
             ++p_waits[t];
@@ -235,7 +243,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             ++o_commits[t];
             pv_pending[t] = true;
           }
-          tc::mma_commit(bar(PfSmem::V_EMPTY + s));
+          tc::mma_commit(bar(PfSmem::V_EMPTY + sv));
           ++it;
           ++jj;
         }
@@ -245,9 +253,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       tc::mma_commit(bar(PfSmem::DONE));
       mbar_wait_drain(bar(PfSmem::DONE), 0);
     }
-  } else if (warp >= 4) {
+  } else {
     // -------------------------------------------------------------- softmax
-    const int t = (warp - 4) >> 2;           // M tile of this warpgroup
+    const int t = (warp - 2) >> 2;           // M tile of this warpgroup
     const int r = ((warp & 3) << 5) | lane;  // row within the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_addr = lane_base + t * 128;
@@ -267,100 +275,70 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         ok = __all_sync(0xFFFFFFFFu, ok);  // keep the warp converged for its TMEM accesses
         ++s_waits;
         tc::fence_after_sync();
-        // pass 1: row max over the visible keys (raw dot products; qscale > 0).
-        // Two 32-column loads in flight, eight independent max chains.
+        // the whole S row in registers (one TMEM round trip), then the row max
+        // over the visible keys (raw dot products; qscale > 0), eight chains
         const int kbase = blk * kPfKeys;
         const bool full = kbase + kPfKeys - 1 <= qpos && kbase + kPfKeys <= p.L;
         const int lim = full ? kPfKeys - 1 : min(qpos, p.L - 1) - kbase;  // last visible key column
+        float sr[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_addr + 32 * c, sr + 32 * c);
+        tc::tmem_wait_ld();
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e) sr[e] = (e <= lim) ? sr[e] : -INFINITY;
+        }
         float mx;
         {
           float m8[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+          for (int e = 0; e < 8; ++e) m8[e] = sr[e];
 #pragma unroll
-          for (int c = 0; c < 4; c += 2) {
-            float s0[32], s1[32];
-            tc::tmem_ld32(s_addr + 32 * c, s0);
-            tc::tmem_ld32(s_addr + 32 * c + 32, s1);
-            tc::tmem_wait_ld();
-            if (full) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], fmaxf(s0[e], s1[e]));
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float a0 = (32 * c + e <= lim) ? s0[e] : -INFINITY;
-                const float a1 = (32 * c + 32 + e <= lim) ? s1[e] : -INFINITY;
-                m8[e & 7] = fmaxf(m8[e & 7], fmaxf(a0, a1));
-              }
-            }
-          }
+          for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], sr[e]);
           mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
         mx = (mx == -INFINITY) ? -INFINITY : mx * p.qscale;
+        // lazy rescale: the running max moves only when it grows by more than
+        // 2^kPfRescale; P is then taken against the new max and O, l are scaled
+        const bool need = mx > m_run + kPfRescale;
+        const float m_new = need ? mx : m_run;
+        const float corr = (need && m_run != -INFINITY) ? ex2_approx(m_run - m_new) : 1.f;
+        // P = exp2(S * qscale - m) as bf16 pairs into columns 0-63 of S_t (the S
+        // values are all in registers already; masked keys are -inf, giving 0)
+        const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a0 = ex2_approx(fmaf(sr[32 * c + 2 * e], p.qscale, -mu));
+            const float a1 = ex2_approx(fmaf(sr[32 * c + 2 * e + 1], p.qscale, -mu));
+            ls4[e & 3] += a0 + a1;
+            pk[e] = pack_bf16x2(a0, a1);
+          }
+          tc::tmem_st16(s_addr + 16 * c, pk);
+        }
         if (jj > 0) {  // PV_t of the previous block has completed: O_t is stable
           if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), o_waits & 1);
           ok = __all_sync(0xFFFFFFFFu, ok);
           ++o_waits;
           tc::fence_after_sync();
-        }
-        // lazy rescale; TMEM accesses are warp-wide, so a warp rescales when any
-        // of its rows needs it (the others use a factor of 1)
-        const bool need = mx > m_run + kPfRescale;
-        if (jj > 0 && __any_sync(0xFFFFFFFFu, need)) {
-          const float corr = (need && m_run != -INFINITY) ? exp2f(m_run - mx) : 1.f;
-          l_run *= corr;
+          // TMEM accesses are warp-wide: a warp rescales when any of its rows needs it
+          if (__any_sync(0xFFFFFFFFu, need)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tc::tmem_ld32(o_addr + 32 * c, o);
-            tc::tmem_wait_ld();
+            for (int c = 0; c < 4; ++c) {
+              float o[32];
+              tc::tmem_ld32(o_addr + 32 * c, o);
+              tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= corr;
-            tc::tmem_st32(o_addr + 32 * c, o);
-          }
-        }
-        if (need) m_run = mx;
-        // pass 2: P = exp2(S * qscale - m) as bf16 pairs into columns 0-63 of S_t
-        // (chunk c's pairs land on columns 16c..16c+15, already read)
-        const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < 4; c += 2) {
-          float s0[32], s1[32];
-          tc::tmem_ld32(s_addr + 32 * c, s0);
-          tc::tmem_ld32(s_addr + 32 * c + 32, s1);
-          tc::tmem_wait_ld();
-          uint32_t pk0[16], pk1[16];
-          if (full) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float a0 = ex2_approx(fmaf(s0[2 * e], p.qscale, -mu));
-              const float a1 = ex2_approx(fmaf(s0[2 * e + 1], p.qscale, -mu));
-              const float b0 = ex2_approx(fmaf(s1[2 * e], p.qscale, -mu));
-              const float b1 = ex2_approx(fmaf(s1[2 * e + 1], p.qscale, -mu));
-              ls4[e & 3] += (a0 + a1) + (b0 + b1);
-              pk0[e] = pack_bf16x2(a0, a1);
-              pk1[e] = pack_bf16x2(b0, b1);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c0 = 32 * c + 2 * e;
-              const float a0 = (c0 <= lim) ? ex2_approx(fmaf(s0[2 * e], p.qscale, -mu)) : 0.f;
-              const float a1 = (c0 + 1 <= lim) ? ex2_approx(fmaf(s0[2 * e + 1], p.qscale, -mu)) : 0.f;
-              const float b0 = (c0 + 32 <= lim) ? ex2_approx(fmaf(s1[2 * e], p.qscale, -mu)) : 0.f;
-              const float b1 = (c0 + 33 <= lim) ? ex2_approx(fmaf(s1[2 * e + 1], p.qscale, -mu)) : 0.f;
-              ls4[e & 3] += (a0 + a1) + (b0 + b1);
-              pk0[e] = pack_bf16x2(a0, a1);
-              pk1[e] = pack_bf16x2(b0, b1);
+              for (int e = 0; e < 32; ++e) o[e] *= corr;
+              tc::tmem_st32(o_addr + 32 * c, o);
             }
           }
-          tc::tmem_st16(s_addr + 16 * c, pk0);
-          tc::tmem_st16(s_addr + 16 * c + 16, pk1);
         }
-        const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-        l_run += ls;
+        m_run = m_new;
+        l_run = l_run * corr + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
         tc::tmem_wait_st();
         tc::fence_before_sync();
         mbar_arrive(bar(PfSmem::P_FULL + t));

@@ -239,12 +239,14 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
     for (int bx = 0; bx < kBoxes; ++bx)
       tma_g2s_2d(smem_u32(smem + bx * tile_rows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
   };
+  pdl_launch_dependents();
   if (tid == 0) {
     prefetch_tmap(&sk_map);
     mbar_init(bar, 1);
     fence_mbar_init();
-    if (b0 < b1) issue_tile(b0);  // the first tile's copy overlaps the q staging below
   }
+  pdl_wait();  // the sketch and q may come from the previous kernel
+  if (tid == 0 && b0 < b1) issue_tile(b0);  // the first tile's copy overlaps the q staging below
   for (int i = tid; i < RMAX * D; i += kSelThreads) {
     const int r = i / D, c = i % D;
     float v = 0.f;

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kSketchThreads) append_kv_kernel(const TE* __r
   __shared__ __align__(16) float red[kSketchThreads * 8];
   using V = Vec16<TE>;
   constexpr int CPR = D / V::N;
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel may still read the cache rows written below
   const int g = blockIdx.x;
   const int b = g / Hkv, kvh = g % Hkv;
   // copy rows: element (t, chunk) per thread

@@ -13,6 +13,17 @@
 
 #include "sparse_attn.h"
 
+// Resident CTAs per SM of the bf16 decode kernel (each gets an equal share of
+// the SM's shared memory for its K/V ring).
+#ifndef SA_DM_CTAS_PER_SM
+#define SA_DM_CTAS_PER_SM 2
+#endif
+// Work ranges per resident CTA slot (more, shorter ranges let the block
+// scheduler balance SMs that are served later by the memory system).
+#ifndef SA_DM_WAVES
+#define SA_DM_WAVES 1
+#endif
+
 #include "k_decode.cu"
 #include "k_decode_mma.cu"
 #include "k_prefill.cu"
@@ -92,6 +103,25 @@ template <typename K>
 sa_status_t set_smem(K kernel, int bytes) {
   SA_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                bytes));
+  return SA_OK;
+}
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel of the stream finishes (it calls pdl_wait() before
+// touching memory that kernel uses).
+template <typename... KArgs, typename... Args>
+sa_status_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  SA_CUDA(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
   return SA_OK;
 }
 
@@ -184,15 +214,12 @@ sa_status_t launch_append(const void* kn, const void* vn, int B, int Hkv, int T,
                           int pos, int block, float* sketch, cudaStream_t st) {
   const int nb_cap = cdiv(Ls, block);
   if (d == 128)
-    sa::append_kv_kernel<TE, 128><<<B * Hkv, sa::kSketchThreads, 0, st>>>(
-        static_cast<const TE*>(kn), static_cast<const TE*>(vn), T, Hkv, static_cast<TE*>(kc), static_cast<TE*>(vc),
-        Ls, pos, block, nb_cap, sketch);
-  else
-    sa::append_kv_kernel<TE, 64><<<B * Hkv, sa::kSketchThreads, 0, st>>>(
-        static_cast<const TE*>(kn), static_cast<const TE*>(vn), T, Hkv, static_cast<TE*>(kc), static_cast<TE*>(vc),
-        Ls, pos, block, nb_cap, sketch);
-  SA_CUDA(cudaGetLastError());
-  return SA_OK;
+    return launch_pdl(sa::append_kv_kernel<TE, 128>, dim3(B * Hkv), dim3(sa::kSketchThreads), 0, st,
+                      static_cast<const TE*>(kn), static_cast<const TE*>(vn), T, Hkv, static_cast<TE*>(kc),
+                      static_cast<TE*>(vc), Ls, pos, block, nb_cap, sketch);
+  return launch_pdl(sa::append_kv_kernel<TE, 64>, dim3(B * Hkv), dim3(sa::kSketchThreads), 0, st,
+                    static_cast<const TE*>(kn), static_cast<const TE*>(vn), T, Hkv, static_cast<TE*>(kc),
+                    static_cast<TE*>(vc), Ls, pos, block, nb_cap, sketch);
 }
 
 // ================================================================== a2 + a3
@@ -263,13 +290,15 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
   cfg.blockDim = dim3(sa::kSelThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = cs;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   SA_CUDA(cudaLaunchKernelEx(&cfg, kern, map, static_cast<const TE*>(a.q), a.Tq, a.Hq, a.Hkv, nb, nb_cap, a.scale,
                              per, tile_rows, a.k, a.scores, a.idx, a.cnt, a.kmax));
   return SA_OK;
@@ -373,13 +402,13 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
   const long long U = static_cast<long long>(groups) * a.kmax;
   SA_ARG(U < (1LL << 31), "too many (group, block) units");
   // two CTAs per SM; equal contiguous ranges of units
-  const long long target = 2LL * di.sms;
+  const long long target = static_cast<long long>(SA_DM_WAVES) * SA_DM_CTAS_PER_SM * di.sms;
   long long per = (U + target - 1) / target;
   per = std::max<long long>(per, (a.kmax + sa::kDmMaxParts - 2) / (sa::kDmMaxParts - 1));  // <= 64 partials per group
   per = std::min<long long>(std::max<long long>(per, 1), sa::kDmMaxList);
   const int nctas = static_cast<int>((U + per - 1) / per);
   sa::DmLayout lay{2, R, D, static_cast<int>(per)};
-  const int budget = 113 * 1024;  // two CTAs in the 228 KB of shared memory per SM
+  const int budget = (227 * 1024) / SA_DM_CTAS_PER_SM - 1024;  // the CTAs of one SM share its shared memory
   const int fixed = lay.bytes() - 2 * Cfg::STAGEB;
   lay.nstages = std::max(2, std::min(6, (budget - fixed) / Cfg::STAGEB));
   const int smem = lay.bytes();
@@ -414,9 +443,7 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
                      CU_TENSOR_MAP_SWIZZLE_128B));
   SA_TRY(make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.vc, D, rows, D * 2, 64, sa::kDmBk,
                      CU_TENSOR_MAP_SWIZZLE_128B));
-  kern<<<nctas, sa::kDmThreads, smem, st>>>(km, vm, p);
-  SA_CUDA(cudaGetLastError());
-  return SA_OK;
+  return launch_pdl(kern, dim3(nctas), dim3(sa::kDmThreads), smem, st, km, vm, p);
 }
 
 template <typename TE, int D, int RMAX>

@@ -29,6 +29,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel in the stream is still running: it must call pdl_wait()
+// before it reads what that kernel wrote or writes what that kernel reads
+// (pdl_wait returns once the previous grid has completed and its memory is
+// visible; without the launch attribute it returns at once).
+// pdl_launch_dependents() lets the next kernel of the stream be scheduled now.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
