@@ -169,20 +169,35 @@ __global__ void __launch_bounds__(kScThreads, 1) score_prefill_kernel(const __gr
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     uint32_t mt = 0, dc = 0;
     bool ok = true;
+    // this thread's 16 four-float pieces of an M tile's sketch rows (blocks past i read as zero);
+    // the next M tile's pieces are loaded while the tensor core works on the current one
+    float4 cur[16];
+    auto load_tile = [&](int uu, int mm) {
+      const int ii = p.nq - 1 - uu / p.groups, gg = uu % p.groups;
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int item = ct + it * 256;
+        const int r = item >> 5, c4 = item & 31;
+        const int blk = mm * 128 + r;
+        cur[it] = (blk <= ii && blk < p.nb)
+                      ? __ldg(reinterpret_cast<const float4*>(p.sketch + (static_cast<size_t>(gg) * p.nb_cap + blk) * 128) + c4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    };
+    if (blockIdx.x < p.units) load_tile(blockIdx.x, 0);
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       const int i = p.nq - 1 - u / p.groups, g = u % p.groups;
       const int mtiles = i / 128 + 1;
       const int rows_valid = min(128, p.L - i * 128);  // query rows of the tile (last tile may be short)
       float* srow = p.scores + (static_cast<size_t>(g) * p.nq + i) * p.nb;
       for (int m = 0; m < mtiles; ++m, ++mt) {
-        // ---- convert sketch rows 128m .. 128m+127 (blocks past i become zero rows)
+        // ---- convert sketch rows 128m .. 128m+127 into the three bf16 parts
         if (mt > 0 && ok) ok = mbar_wait(bar(ScSmem::A_EMPTY), (mt - 1) & 1);
-        for (int item = ct; item < 128 * 32; item += 256) {
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+          const int item = ct + it * 256;
           const int r = item >> 5, c4 = item & 31;  // row, 4-float chunk
-          const int blk = m * 128 + r;
-          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (blk <= i && blk < p.nb)
-            x = *reinterpret_cast<const float4*>(p.sketch + (static_cast<size_t>(g) * p.nb_cap + blk) * 128 + c4 * 4);
+          const float4 x = cur[it];
           const float xs[4] = {x.x, x.y, x.z, x.w};
           uint32_t part[3][2];
 #pragma unroll
@@ -213,6 +228,8 @@ __global__ void __launch_bounds__(kScThreads, 1) score_prefill_kernel(const __gr
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(ScSmem::A_FULL));
+        if (m + 1 < mtiles) load_tile(u, m + 1);
+        else if (u + static_cast<int>(gridDim.x) < p.units) load_tile(u + gridDim.x, 0);
         if (!epi) continue;
         // ---- epilogue: max over the chunk columns of this block lane
         float mx = -INFINITY;

@@ -520,7 +520,7 @@ sa_status_t validate_decode(const DecodeArgs& a) {
   SA_ARG(a.T <= a.block && a.T <= a.L, "T (%d) must be <= block and <= L", a.T);
   SA_SUP((a.Hq / a.Hkv) * a.T <= 32, "G*T (%d) must be <= 32", (a.Hq / a.Hkv) * a.T);
   SA_ARG(a.kmax >= 1, "kmax must be >= 1");
-  SA_ARG(aligned16(a.kc) && aligned16(a.vc), "k/v caches must be 16-byte aligned");
+  SA_ARG(aligned16(a.kc) && aligned16(a.vc) && aligned16(a.q), "q and the k/v caches must be 16-byte aligned");
   SA_ARG(static_cast<long long>(a.B) * a.Hkv * a.Ls < (1LL << 31), "B*Hkv*L_stride too large");
   SA_ARG(a.ws && aligned16(a.ws), "workspace must be a 16-byte-aligned device pointer");
   const size_t need = decode_ws_bytes(a.B * a.Hkv, (a.Hq / a.Hkv) * a.T, a.d, a.kmax);
