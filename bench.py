@@ -381,13 +381,16 @@ def bench_decode(args, wl, rank, world):
         gbs, cores, sample = cpu_oracle_decode(wl, x, args.cpu_seconds)
         res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                "sample": sample}
-    traffic = os.path.join(ROOT, "profiles", "decode_c2_traffic.json")
-    if os.path.exists(traffic) and wl.name == "c2":
+    traffic = os.path.join(ROOT, "profiles", "decode_c2_traffic.txt")
+    if os.path.exists(traffic) and wl.name == "c2" and bf and wl.G * wl.T <= 16:
         try:
-            with open(traffic) as f:
-                t = json.load(f)
+            t = {}
+            for line in open(traffic):
+                if ":" in line and not line.startswith("#"):
+                    key, val = line.split(":", 1)
+                    t[key.strip()] = val.strip()
             if t.get("kernel_source_hash") == _kernel_hash():
-                res["roofline"]["traffic"] = t["dram_bytes_per_launch"]
+                res["roofline"]["traffic"] = int(t["dram_bytes_per_launch"])
         except Exception:
             pass
     return res
@@ -512,7 +515,7 @@ def bench_prefill(wl, steps, peaks, peak_src):
 def _kernel_hash():
     import hashlib
     h = hashlib.sha256()
-    for fn in ("k_decode.cu", "sa_ptx.cuh"):
+    for fn in ("k_decode_mma.cu", "sa_ptx.cuh"):
         with open(os.path.join(ROOT, "top_block_sparse_pooled_b300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
