@@ -7,9 +7,11 @@
 // partial softmaxes over disjoint key sets merge exactly (online softmax).
 //
 // Work split: the (group, selected-block) units of all groups are laid end to
-// end and cut into equal contiguous ranges, one per CTA (about two CTAs per
-// SM), so every SM streams the same number of blocks whatever the group
-// count.  A CTA whose range spans several groups emits one partial per group;
+// end and cut into equal contiguous ranges, one per CTA (one CTA per SM, a
+// four-stage K/V ring), so every SM streams the same number of blocks whatever
+// the group count.  (Measured on the B300: one SM sustains only ~45 GB/s of
+// these copies, so all SMs must stream; a smaller first burst of requests
+// evens out how soon the CTAs are served.)  A CTA whose range spans several groups emits one partial per group;
 // the partial of (CTA c, group g) is stored at slot c + g (the pieces of two
 // interleaved partitions of a line, counted in order).  The CTA that brings a
 // group's arrival counter to its CTA count merges that group's partials and
@@ -26,6 +28,10 @@
 #pragma once
 
 #include "sa_ptx.cuh"
+
+#ifndef SA_DM_RAMP
+#define SA_DM_RAMP 0
+#endif
 
 namespace sa {
 
@@ -172,6 +178,11 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
           tma_g2s_2d(kt + C::TILEB + bx * kDmBk * 128, &vmap, bx * 64, row, full);
         }
         ++vi;
+#if SA_DM_RAMP
+        // ramp: request the rest of the ring once the first tile has landed, so the
+        // grid's first burst of requests is one tile per CTA
+        if (vi == 1 && ok) ok = mbar_wait(full0, 0);
+#endif
       }
       // never leave with copies in flight: wait for the last fill of every used stage
       for (int k = max(0, vi - NS); k < vi; ++k) mbar_wait_drain(full0 + 8 * (k % NS), (k / NS) & 1);

@@ -16,12 +16,16 @@
 // Resident CTAs per SM of the bf16 decode kernel (each gets an equal share of
 // the SM's shared memory for its K/V ring).
 #ifndef SA_DM_CTAS_PER_SM
-#define SA_DM_CTAS_PER_SM 2
+#define SA_DM_CTAS_PER_SM 1
 #endif
 // Work ranges per resident CTA slot (more, shorter ranges let the block
 // scheduler balance SMs that are served later by the memory system).
 #ifndef SA_DM_WAVES
 #define SA_DM_WAVES 1
+#endif
+// Upper bound on the K/V ring depth of each decode CTA.
+#ifndef SA_DM_MAXSTAGES
+#define SA_DM_MAXSTAGES 4
 #endif
 
 #include "k_decode.cu"
@@ -410,7 +414,7 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
   sa::DmLayout lay{2, R, D, static_cast<int>(per)};
   const int budget = (227 * 1024) / SA_DM_CTAS_PER_SM - 1024;  // the CTAs of one SM share its shared memory
   const int fixed = lay.bytes() - 2 * Cfg::STAGEB;
-  lay.nstages = std::max(2, std::min(6, (budget - fixed) / Cfg::STAGEB));
+  lay.nstages = std::max(2, std::min(SA_DM_MAXSTAGES, (budget - fixed) / Cfg::STAGEB));
   const int smem = lay.bytes();
   auto kern = sa::decode_mma_kernel<D>;
   SA_TRY(set_smem(kern, smem));
