@@ -45,6 +45,8 @@ def load(path: str = None):
     lib.orc_prefill_scores.argtypes = [vp, i, vp, l, l, l, l, l, l, l, l, d, vp, l, vp]
     lib.orc_select.argtypes = [vp, l, l, vp, vp, vp, l, vp, vp]
     lib.orc_select.restype = i
+    lib.orc_select_delta.argtypes = [vp, l, l, vp, vp, d, vp, l, vp, vp]
+    lib.orc_select_delta.restype = i
     lib.orc_attend.argtypes = [vp, vp, vp, i, l, l, l, l, l, l, l, l, l, d, vp, vp, l, l, l, vp, l, vp, vp]
     lib.orc_mass.argtypes = [vp, vp, i, l, l, l, l, l, l, l, l, l, l, d, vp, l, vp]
     lib.orc_causal_blocks.argtypes = [l, l, l, l, l]
@@ -152,6 +154,23 @@ def select(scores, nvalid, forced_hi, budget, kmax):
     return idx, cnt
 
 
+def select_delta(scores, nvalid, forced_hi, delta, cap, kmax):
+    """Top-delta: non-forced blocks scoring >= max(forced scores) - delta, at most cap of them
+    (highest first, ties -> lower index), plus the forced ones, ascending."""
+    scores = _c(scores, np.float64)
+    n, nb = scores.shape
+    nvalid = _c(np.broadcast_to(np.asarray(nvalid, dtype=np.int64), (n,)))
+    forced_hi = _c(np.broadcast_to(np.asarray(forced_hi, dtype=np.int64), (n,)))
+    cap = _c(np.broadcast_to(np.asarray(cap, dtype=np.int64), (n,)))
+    idx = np.empty((n, kmax), dtype=np.int32)
+    cnt = np.empty((n,), dtype=np.int32)
+    rc = _L().orc_select_delta(_p(scores), n, nb, _p(nvalid), _p(forced_hi), float(delta), _p(cap), kmax, _p(idx),
+                               _p(cnt))
+    if rc != 0:
+        raise ValueError("kmax too small for the selection")
+    return idx, cnt
+
+
 def attend(q, k, v, Hkv, L, pos0, Bk, scale, rows, idx=None, cnt=None, nsel=1, rows_per_sel=1 << 40):
     """Exact softmax attention of the given (b, t, h) rows over the selected blocks (all if idx is None)."""
     q, k, v = _c(q), _c(k), _c(v)
@@ -202,6 +221,17 @@ def decode_select(q, k, wl, kmax=None, sketch=None):
     nb = wl.nb
     kmax = kmax or (wl.k + 2)
     idx, cnt = select(s, nb, nb - 1, wl.k, kmax)
+    return idx, cnt, s, sketch
+
+
+def decode_select_delta(q, k, wl, delta, cap, kmax=None, sketch=None):
+    """Decode top-delta selection on sketch scores: pseudo-max from the sink and local blocks."""
+    if sketch is None:
+        sketch = block_means(k, wl.L, wl.Bk)
+    s = decode_scores(q, sketch, wl.Hkv, wl.scale)
+    nb = wl.nb
+    kmax = kmax or (cap + 2)
+    idx, cnt = select_delta(s, nb, nb - 1, delta, cap, kmax)
     return idx, cnt, s, sketch
 
 

@@ -222,6 +222,52 @@ int orc_select(const double* scores, long nunits, long nb, const long* nvalid,
 }
 
 /*
+ * Top-delta selection ("Faster Than Flash" Sec. 2: a key is kept when its score
+ * is at least the pseudo-maximum minus delta, the pseudo-maximum being taken
+ * over the sink and local-context keys only).  At block granularity: for unit
+ * u with valid blocks [0, nvalid[u]) and forced blocks {0, forced_hi[u]}, the
+ * pseudo-maximum is the larger score of the forced blocks; every other valid
+ * block with score >= pseudo-max - delta is kept; if more than cap[u] qualify,
+ * the cap[u] highest are kept (ties to the lower index).  Output as in
+ * orc_select.  Returns 0, or -1 if kmax is too small.
+ */
+int orc_select_delta(const double* scores, long nunits, long nb, const long* nvalid, const long* forced_hi,
+                     double delta, const long* cap, long kmax, int* idx, int* cnt) {
+  int bad = 0;
+  for (long u = 0; u < nunits; ++u) {
+    long nv = nvalid[u];
+    long f1 = forced_hi[u];
+    double pmax = -INFINITY;
+    if (nv > 0) pmax = scores[u * nb];
+    if (f1 > 0 && f1 < nv && scores[u * nb + f1] > pmax) pmax = scores[u * nb + f1];
+    const double thr = pmax - delta;
+    cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (size_t)(nv > 0 ? nv : 1));
+    long* sel = (long*)malloc(sizeof(long) * (size_t)(nv + 2));
+    long nc = 0, ns = 0;
+    for (long b = 0; b < nv; ++b) {
+      if (b == 0 || b == f1) continue;
+      if (scores[u * nb + b] >= thr) {
+        c[nc].s = scores[u * nb + b];
+        c[nc].b = b;
+        ++nc;
+      }
+    }
+    qsort(c, (size_t)nc, sizeof(cand_t), cand_cmp);
+    long take = cap[u] < nc ? cap[u] : nc;
+    if (nv > 0) sel[ns++] = 0;
+    if (f1 > 0 && f1 < nv) sel[ns++] = f1;
+    for (long r = 0; r < take; ++r) sel[ns++] = c[r].b;
+    qsort(sel, (size_t)ns, sizeof(long), long_cmp);
+    if (ns > kmax) bad = 1;
+    cnt[u] = (int)ns;
+    for (long r = 0; r < kmax; ++r) idx[u * kmax + r] = r < ns ? (int)sel[r] : -1;
+    free(c);
+    free(sel);
+  }
+  return bad ? -1 : 0;
+}
+
+/*
  * Exact softmax attention restricted to the selected blocks ("How Much Dense
  * Attention is Necessary?" Sec. 2.1: recompute with the original q, k, v on
  * the selected support only).

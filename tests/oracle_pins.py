@@ -347,3 +347,51 @@ ALL_PINS = [
     pin_decode_needles_selected,
     pin_mass_topk_captures_plant,
 ]
+
+
+def _brute_select_delta(scores, nvalid, forced_hi, delta, cap):
+    forced = {0, forced_hi} & set(range(nvalid))
+    pmax = max(scores[b] for b in forced) if forced else -math.inf
+    cands = [b for b in range(nvalid) if b not in forced and scores[b] >= pmax - delta]
+    ranked = sorted(cands, key=lambda b: (-scores[b], b))
+    return sorted(forced | set(ranked[: max(0, min(cap, len(cands)))]))
+
+
+def pin_select_delta_brute_force():
+    """Top-delta selection against a direct filter-then-sort on random small cases with ties."""
+    r = _rng(9)
+    for trial in range(300):
+        nb = int(r.integers(1, 40))
+        nvalid = int(r.integers(1, nb + 1))
+        scores = r.integers(-4, 5, size=nb).astype(np.float64) * 0.5
+        delta = float(r.choice([0.0, 0.5, 1.0, 2.5, 100.0]))
+        cap = int(r.integers(0, nb + 2))
+        idx, cnt = oracle.select_delta(scores[None, :], nvalid, nvalid - 1, delta, cap, nb + 2)
+        ref = _brute_select_delta(scores, nvalid, nvalid - 1, delta, cap)
+        assert idx[0, : cnt[0]].tolist() == ref, (trial, idx[0, : cnt[0]].tolist(), ref)
+        assert np.all(idx[0, cnt[0]:] == -1)
+
+
+def pin_select_delta_special_cases():
+    s = np.array([2.0, 5.0, 1.9, 1.0, 3.0, 0.0])  # forced 0 and 5: pseudo-max 2.0
+    # delta 0: only candidates at or above the pseudo-max
+    idx, cnt = oracle.select_delta(s[None], 6, 5, 0.0, 10, 8)
+    assert idx[0, : cnt[0]].tolist() == [0, 1, 4, 5]
+    # delta 0.1 admits the 1.9 block; a cap of 2 keeps the two highest of the three
+    idx, cnt = oracle.select_delta(s[None], 6, 5, 0.1, 10, 8)
+    assert idx[0, : cnt[0]].tolist() == [0, 1, 2, 4, 5]
+    idx, cnt = oracle.select_delta(s[None], 6, 5, 0.1, 2, 8)
+    assert idx[0, : cnt[0]].tolist() == [0, 1, 4, 5]
+    # a huge delta with cap k is the top-k selection
+    r = _rng(10)
+    sc = r.standard_normal((5, 30))
+    for k in (0, 3, 10, 28, 40):
+        a, ca = oracle.select_delta(sc, 30, 29, 1e9, k, 32)
+        b, cb = oracle.select(sc, 30, 29, k, 32)
+        assert np.array_equal(a, b) and np.array_equal(ca, cb)
+    # the pseudo-max is the larger of the two forced scores (here the local block)
+    s2 = np.array([0.0, 0.5, 0.9, 1.0])
+    idx, cnt = oracle.select_delta(s2[None], 4, 3, 0.2, 10, 6)
+    assert idx[0, : cnt[0]].tolist() == [0, 2, 3]
+
+ALL_PINS += [pin_select_delta_brute_force, pin_select_delta_special_cases]

@@ -37,6 +37,9 @@ MUTANTS = {
     "mass_not_normalised": ("ar[j / Bk] += exp(logit[j] - m) / den;", "ar[j / Bk] += exp(logit[j] - m);"),
     "mass_not_causal": ("long nk = qpos + 1 < L ? qpos + 1 : L;", "long nk = L;"),
     "mass_drops_scale": ("logit[j] = scale * a;", "logit[j] = a;"),
+    "delta_strict_threshold": ("if (scores[u * nb + b] >= thr) {", "if (scores[u * nb + b] > thr) {"),
+    "delta_pseudo_max_sink_only": ("if (f1 > 0 && f1 < nv && scores[u * nb + f1] > pmax) pmax = scores[u * nb + f1];", ""),
+    "delta_cap_ignored": ("long take = cap[u] < nc ? cap[u] : nc;", "long take = nc;"),
 }
 
 
