@@ -304,11 +304,21 @@ def bench_decode(args, wl, rank, world):
     def app(s):
         sa.sa_append_kv(s["k_new"], s["v_new"], s["kc"], s["vc"], pos, wl.Bk, s["sk"])
 
+    def seld(s):  # top-delta selection (threshold from the sink and local blocks), same budget as a cap
+        sa.sa_select_topdelta(s["q"], s["sk"], None, wl.Hkv, wl.L, wl.L, wl.Bk, 0.3, wl.k, wl.scale, s["idx"],
+                              s["cnt"])
+
     reps = max(10, min(500, K // (4 * R)))
     kern_us = {}
-    for name, fn in (("append", app), ("select", sel), ("decode", dec)):
+    for name, fn in (("append", app), ("select", sel), ("decode", dec), ("select_topdelta", seld)):
         g = capture([lambda s=s, fn=fn: fn(s) for s in sets * 4])
         kern_us[name] = round(graph_us(g, 4 * R, reps), 3)
+    torch.cuda.synchronize()
+    topdelta_blocks = float(sets[-1]["cnt"].float().mean().item())  # blocks kept per group at delta 0.3
+    with torch.cuda.stream(stream):
+        for s_ in sets:  # back to the top-k selection for the end-to-end leg below
+            sel(s_)
+    torch.cuda.synchronize()
     dec_ms = kern_us["decode"] * 1e-3
     dec_gbs = kv_b / (dec_ms * 1e-3) / 1e9
 
@@ -374,6 +384,8 @@ def bench_decode(args, wl, rank, world):
         "e2e": {"value": round(step_bytes / t_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 4)},
         "kernels_us": kern_us,
+        "topdelta": {"delta": 0.3, "cap": wl.k, "mean_blocks_kept_per_group": round(topdelta_blocks, 2),
+                     "select_us": kern_us["select_topdelta"]},
         "gpu_launches": K * (3 if bf and wl.G * wl.T <= 16 else 4),
         "clocks": clocks,
     }

@@ -151,6 +151,22 @@ sa_status_t sa_select_topk(int mode, const void* q, int dtype, const float* sket
                            int qtile, int prefill, int k, int frac_num, int frac_den, float scale,
                            int32_t* idx, int32_t* cnt, int kmax, void* stream);
 
+/*
+ * Decode top-delta selection ("Faster Than Flash" Sec. 2: a key is kept when
+ * its score is at least a pseudo-maximum minus delta; the pseudo-maximum comes
+ * from the sink and local-context keys only, so no global reduction is
+ * needed).  At block granularity: with the sketch scores s of sa_select_topk
+ * (mode SA_SELECT_SKETCH, decode), pm = max(s[0], s[nb-1]); the kept blocks
+ * are {0, nb-1} plus every other block with s >= pm - delta, at most `cap` of
+ * them (the highest, ties to the lower index).  The count per group varies:
+ * cnt[g] in [1, cap + 2]; kmax >= sa_select_kmax(L, block, 0, 0, cap, 0, 1).
+ * delta >= 0 in the units of the scores (scaled logits).  Other arguments and
+ * requirements as for sa_select_topk in decode mode.
+ */
+sa_status_t sa_select_topdelta(const void* q, int dtype, const float* sketch, float* scores, int B, int Tq,
+                               int Hq, int Hkv, int d, int L, int L_stride, int block, float delta,
+                               int cap, float scale, int32_t* idx, int32_t* cnt, int kmax, void* stream);
+
 /* Smallest kmax that holds every selection of the given problem (or -1 if invalid). */
 int sa_select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num, int frac_den);
 

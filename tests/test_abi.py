@@ -113,6 +113,13 @@ def test_invalid_arguments_rejected_on_host(sa):
     # append past the cache
     st = L.sa_append_kv(16, 16, sa.SA_BF16, 1, 1, 4, 128, 16, 16, 64, 62, 64, 16, None)
     assert st == sa.SA_ERR_INVALID_ARG
+    # top-delta: negative delta or cap rejected on the host
+    st = L.sa_select_topdelta(16, sa.SA_BF16, 16, None, 8, 1, 32, 8, 128, 32768, 32768, 64, -1.0, 32, 0.088, 16, 16,
+                              34, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"delta" in L.sa_last_error()
+    st = L.sa_select_topdelta(16, sa.SA_BF16, 16, None, 8, 1, 32, 8, 128, 32768, 32768, 64, 0.5, -2, 0.088, 16, 16,
+                              34, None)
+    assert st == sa.SA_ERR_INVALID_ARG
     # device status needs an output pointer
     assert L.sa_device_status(None, 0) == sa.SA_ERR_INVALID_ARG
 

@@ -62,3 +62,53 @@ def test_decode_select_small_block_counts(sa, nb):
     assert sa.sa_device_status(clear=True) == 0
     o_idx, o_cnt, o_s, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax)
     assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s, what="nb=%d" % nb)
+
+
+def _check_topdelta(g_idx, g_cnt, o_idx, o_cnt, s, delta, cap, rel=1e-5, what=""):
+    """Exact match, except blocks whose oracle score sits within rel of the threshold
+    (fp32 vs fp64 comparison) or of the cap's cut-off score (near-ties)."""
+    g_idx = np.asarray(g_idx).reshape(len(o_cnt), -1)
+    g_cnt = np.asarray(g_cnt).reshape(-1)
+    for u in range(len(o_cnt)):
+        su = np.asarray(s[u], dtype=np.float64)
+        nb = len(su)
+        row = g_idx[u, : g_cnt[u]].tolist()
+        assert row == sorted(set(row)) and np.all(g_idx[u, g_cnt[u]:] == -1), (what, u, row)
+        assert row[0] == 0 and row[-1] == nb - 1 and len(row) <= cap + 2, (what, u, row)
+        gs, os_ = set(row), set(o_idx[u, : o_cnt[u]].tolist())
+        if gs == os_:
+            continue
+        scale = np.abs(su).max()
+        thr = max(su[0], su[nb - 1]) - delta
+        cands = sorted([b for b in range(1, nb - 1) if su[b] >= thr], key=lambda b: (-su[b], b))
+        cut = su[cands[cap - 1]] if 0 < cap <= len(cands) else None
+        for b in gs ^ os_:
+            near_thr = abs(su[b] - thr) <= rel * scale
+            near_cut = cut is not None and abs(su[b] - cut) <= rel * scale
+            assert near_thr or near_cut, "%s unit %d: block %d (score %.9g, thr %.9g, cut %s) differs" % (
+                what, u, b, su[b], thr, cut)
+
+
+@pytest.mark.parametrize("name", ["c2", "c3"])
+def test_decode_topdelta_matches_oracle(sa, name):
+    wl = synth.WORKLOADS[name]
+    if name == "c3":
+        wl = wl.replace(L=65536, needles=10)
+    x = synth.make_inputs(wl)
+    q, k = dev(x.q), dev(x.k)
+    sk = torch.empty((wl.B, wl.Hkv, wl.nb, wl.d), dtype=torch.float32, device="cuda")
+    sa.sa_build_sketch(k, wl.L, wl.Bk, sk)
+    sketch = oracle.block_means(x.k, wl.L, wl.Bk)
+    for delta, cap in ((0.0, wl.k), (0.1, wl.k), (0.3, 2 * wl.k), (1.0, wl.k), (1e6, wl.k), (0.2, 0)):
+        kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, cap)
+        idx = torch.full((wl.B, wl.Hkv, 1, kmax), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.zeros((wl.B, wl.Hkv, 1), dtype=torch.int32, device="cuda")
+        sa.sa_select_topdelta(q, sk, None, wl.Hkv, wl.L, wl.L, wl.Bk, delta, cap, wl.scale, idx, cnt)
+        torch.cuda.synchronize()
+        assert sa.sa_device_status(clear=True) == 0
+        o_idx, o_cnt, o_s, _ = oracle.decode_select_delta(x.q, x.k, wl, delta, cap, kmax=kmax, sketch=sketch)
+        _check_topdelta(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s, delta, cap,
+                        what="%s delta=%g cap=%d" % (name, delta, cap))
+        if delta >= 1e6:  # no threshold: the top-k selection
+            t_idx, t_cnt, _, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax, sketch=sketch)
+            assert np.array_equal(o_idx, t_idx) and np.array_equal(o_cnt, t_cnt)

@@ -49,6 +49,7 @@ SIGNATURES = {
     "sa_append_kv": ([_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _i, _i, _i, _vp, _vp], _i),
     "sa_select_topk": ([_i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                         _vp, _vp, _i, _vp], _i),
+    "sa_select_topdelta": ([_vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _f, _vp, _vp, _i, _vp], _i),
     "sa_select_kmax": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "sa_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "sa_decode": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
@@ -137,6 +138,15 @@ def sa_select_topk(mode, q, sketch, scores, Hkv, L, L_stride, block, qtile, pref
     _check(lib.sa_select_topk(mode, _ptr(q), SA_BF16 if dtype is None else dtype, _ptr(sketch), _ptr(scores), B, Tq,
                               Hq, Hkv, d, L, L_stride, block, qtile, 1 if prefill else 0, k, frac_num, frac_den,
                               float(scale), _ptr(idx), _ptr(cnt), kmax, _stream(stream)))
+
+
+def sa_select_topdelta(q, sketch, scores, Hkv, L, L_stride, block, delta, cap, scale, idx, cnt, stream=None):
+    """Decode top-delta selection: q [B, T, Hq, d]; idx [B, Hkv, 1, kmax], cnt [B, Hkv, 1] (written)."""
+    B, Tq, Hq, d = q.shape
+    kmax = idx.shape[-1]
+    _check(lib.sa_select_topdelta(_ptr(q), _dtype(q), _ptr(sketch), _ptr(scores), B, Tq, Hq, Hkv, d, L, L_stride,
+                                  block, float(delta), cap, float(scale), _ptr(idx), _ptr(cnt), kmax,
+                                  _stream(stream)))
 
 
 def sa_decode_workspace_bytes(B, T, Hq, Hkv, d, kmax) -> int:

@@ -6,6 +6,10 @@
 // Attention" Phase 1, "Faster Than Flash" Sec. 2) and do not count against
 // the budget.  Ties go to the lower block index; the output is ascending.
 //
+// Top-delta (decode): the budget becomes the number of candidates that score at
+// least max(sink score, local score) - delta, capped at k; the same exact
+// top-k then picks exactly those candidates (they are the highest ones).
+//
 // Top-k is an exact MSB-first radix select on order-preserving 32-bit keys of
 // the float32 scores (four 8-bit digit passes over a 256-bin shared-memory
 // histogram), followed by an index-ordered scan that resolves ties at the
@@ -214,7 +218,7 @@ template <typename TE, int D, int RMAX>
 __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
     const __grid_constant__ CUtensorMap sk_map, const TE* __restrict__ q, int T, int Hq, int Hkv, int nb,
     int nb_cap, float scale, int per, int tile_rows, int k, float* __restrict__ scores_out,
-    int32_t* __restrict__ idx, int32_t* __restrict__ cnt, int kmax) {
+    int32_t* __restrict__ idx, int32_t* __restrict__ cnt, int kmax, int topdelta, float delta) {
   constexpr int kBoxes = D * 4 / 128;
   extern __shared__ __align__(1024) uint8_t smem_sel_dec[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_sel_dec) + 1023) & ~uintptr_t(1023));
@@ -302,7 +306,19 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
   if (!waited) cluster_wait();
   cluster_sync();  // all scores have landed in rank 0
   if (rank != 0) return;
-  block_topk(all, nb, k, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, S);
+  int budget = k;
+  if (topdelta) {
+    // top-delta ("Faster Than Flash" Sec. 2): the candidates scoring at least the
+    // pseudo-maximum (over the sink and local blocks) minus delta, at most k of them
+    const float thr = fmaxf(all[0], all[nb - 1]) - delta;
+    int c = 0;
+    for (int base = 0; base < nb; base += kSelThreads) {
+      const int b = base + tid;
+      c += __syncthreads_count(b >= 1 && b < nb - 1 && all[b] >= thr);
+    }
+    budget = min(c, k);
+  }
+  block_topk(all, nb, budget, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, S);
 }
 
 // --------------------------------------------------------------------------

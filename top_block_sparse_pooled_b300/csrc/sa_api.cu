@@ -238,6 +238,8 @@ struct SelectArgs {
   int32_t* idx;
   int32_t* cnt;
   int kmax;
+  int topdelta;  // decode sketch mode: keep candidates >= pseudo-max - delta, at most k
+  float delta;
 };
 
 int max_cluster_size(const void* fn, int smem, int groups, cudaStream_t st) {
@@ -304,7 +306,7 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   SA_CUDA(cudaLaunchKernelEx(&cfg, kern, map, static_cast<const TE*>(a.q), a.Tq, a.Hq, a.Hkv, nb, nb_cap, a.scale,
-                             per, tile_rows, a.k, a.scores, a.idx, a.cnt, a.kmax));
+                             per, tile_rows, a.k, a.scores, a.idx, a.cnt, a.kmax, a.topdelta, a.delta));
   return SA_OK;
 }
 
@@ -736,6 +738,18 @@ sa_status_t sa_select_topk(int mode, const void* q, int dtype, const float* sket
   t_err.clear();
   SelectArgs a{mode, q, dtype, sketch, scores, B, Tq, Hq, Hkv, d, L, L_stride, block, qtile, prefill ? 1 : 0, k,
                frac_num, frac_den, scale, idx, cnt, kmax};
+  SA_TRY(validate_select(a));
+  return run_select(a, as_stream(stream));
+}
+
+sa_status_t sa_select_topdelta(const void* q, int dtype, const float* sketch, float* scores, int B, int Tq, int Hq,
+                               int Hkv, int d, int L, int L_stride, int block, float delta, int cap, float scale,
+                               int32_t* idx, int32_t* cnt, int kmax, void* stream) {
+  t_err.clear();
+  SA_ARG(delta >= 0.f && delta < 1e30f, "delta must be >= 0 and finite");
+  SA_ARG(cap >= 0, "cap must be >= 0");
+  SelectArgs a{SA_SELECT_SKETCH, q, dtype, sketch, scores, B, Tq, Hq, Hkv, d, L, L_stride, block, 0, 0, cap,
+               0, 1, scale, idx, cnt, kmax, 1, delta};
   SA_TRY(validate_select(a));
   return run_select(a, as_stream(stream));
 }
