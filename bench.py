@@ -524,6 +524,63 @@ def bench_prefill(wl, steps, peaks, peak_src):
     return res
 
 
+def bench_length_sweep(lengths, k_ref, L_ref, exponent, reps=20):
+    """Decode (B=1, T=4, Hq=32, Hkv=8, d=128, block 64) across context lengths with the
+    length-aware budget k(L) = ceil(k_ref * (L / L_ref)^exponent).  Each rep: L2 flushed
+    (256 MB write, untimed), then sketch select + sparse decode timed with CUDA events."""
+    import numpy as np
+    import torch
+
+    import synth
+    import top_block_sparse_pooled_b300 as sa
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rows = []
+    for L in lengths:
+        k = sa.sa_budget_sublinear(L, 64, k_ref, L_ref, exponent)
+        nb = (L + 63) // 64
+        wl = synth.WORKLOADS["c3"].replace(L=L, k=k, needles=max(1, round(0.005 * nb)))
+        x = synth.make_inputs(wl)
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        q, kc, vc = up(x.q), up(x.k), up(x.v)
+        del x
+        sk = torch.empty((1, wl.Hkv, nb, wl.d), dtype=torch.float32, device=dev)
+        sa.sa_build_sketch(kc, L, 64, sk)
+        kmax = sa.sa_select_kmax(L, 64, 0, False, k)
+        idx = torch.empty((1, wl.Hkv, 1, kmax), dtype=torch.int32, device=dev)
+        cnt = torch.empty((1, wl.Hkv, 1), dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        ws = torch.zeros(sa.sa_decode_workspace_bytes(1, wl.T, wl.Hq, wl.Hkv, wl.d, kmax), dtype=torch.uint8,
+                         device=dev)
+        ts = []
+        for r in range(reps + 3):
+            flush.fill_(r & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            sa.sa_select_topk(sa.SA_SELECT_SKETCH, q, sk, None, wl.Hkv, L, L, 64, 0, False, k, 0, 1, wl.scale, idx,
+                              cnt)
+            sa.sa_decode(q, kc, vc, idx, cnt, L, 64, wl.scale, out, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        kv = int(cnt.sum().item()) * 64 * wl.d * 2 * 2
+        sketch_bytes = wl.Hkv * nb * wl.d * 4
+        us = float(np.median(ts))
+        rows.append({"L": L, "k": k, "blocks_per_group": int(cnt[0, 0, 0].item()),
+                     "kept_fraction": round(int(cnt[0, 0, 0].item()) / nb, 4), "select_plus_decode_us": round(us, 2),
+                     "bytes": kv + sketch_bytes, "GB_s": round((kv + sketch_bytes) / us / 1e3, 1)})
+        del q, kc, vc, sk, out, ws
+        torch.cuda.empty_cache()
+    if sa.sa_device_status() != 0:
+        raise RuntimeError("device status word set during the length sweep")
+    return {"sweep": "length-aware budget", "budget": "k(L) = ceil(%d * (L / %d)^%g)" % (k_ref, L_ref, exponent),
+            "workload": "decode B=1 T=4 Hq=32 Hkv=8 d=128 block 64, bf16, 0.5%% needle blocks", "rows": rows}
+
+
 def _kernel_hash():
     import hashlib
     h = hashlib.sha256()
@@ -593,6 +650,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5,
                     help="steps of each prefill leg (c5 sketch-selected, c4 oracle-mass); 0 skips them")
     ap.add_argument("--prefill-only", action="store_true", help="run only the prefill legs (profiling)")
+    ap.add_argument("--sweep-length", action="store_true",
+                    help="decode across context lengths with the length-aware budget (separate report)")
     ap.add_argument("--prefill-B", type=int, default=0, help="override the prefill legs' batch (profiling)")
     ap.add_argument("--prefill-L", type=int, default=0, help="override the prefill legs' context (profiling)")
     args = ap.parse_args()
@@ -618,7 +677,11 @@ def main():
                 w = w.replace(L=args.prefill_L)
             return w
 
-        if args.prefill_only:
+        if args.sweep_length:
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            res = bench_length_sweep([16384, 32768, 65536, 131072, 262144], 80, 262144, 0.5)
+        elif args.prefill_only:
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
             peaks, src = load_peaks()

@@ -167,6 +167,19 @@ sa_status_t sa_select_topdelta(const void* q, int dtype, const float* sketch, fl
                                int Hq, int Hkv, int d, int L, int L_stride, int block, float delta,
                                int cap, float scale, int32_t* idx, int32_t* cnt, int kmax, void* stream);
 
+/*
+ * Length-aware block budget ("The Sparse Frontier" RQ3: longer sequences
+ * tolerate more sparsity, so the budget should grow sublinearly with the
+ * length; "How Much Dense Attention is Necessary?" Sec. 3.1: shared supports
+ * need budgets that scale with the length).  Returns
+ *   k(L) = ceil(k_ref * (L / L_ref)^exponent),
+ * clamped to the candidates available (ceil(L / block) - 2, at least 0):
+ * exponent 0 keeps k_ref blocks at every length, 1 keeps a fixed fraction.
+ * Host-only; returns -1 for L, block, L_ref < 1, k_ref < 0 or an exponent
+ * outside [0, 1].  Pass the result as `k` (decode) to sa_select_topk.
+ */
+int sa_budget_sublinear(int L, int block, int k_ref, int L_ref, float exponent);
+
 /* Smallest kmax that holds every selection of the given problem (or -1 if invalid). */
 int sa_select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num, int frac_den);
 

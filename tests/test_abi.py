@@ -58,6 +58,23 @@ def test_kmax_queries(sa):
     assert sa.sa_select_kmax(0, 64, 0, False, 8) == -1
 
 
+def test_budget_sublinear(sa):
+    """k(L) = ceil(k_ref * (L/L_ref)^e), clamped to the candidate blocks (closed forms)."""
+    f = sa.sa_budget_sublinear
+    assert f(262144, 64, 80, 262144, 0.5) == 80            # the reference point
+    assert f(65536, 64, 80, 262144, 0.5) == 40             # a quarter of the length: half the budget
+    assert f(65536, 64, 80, 262144, 1.0) == 20             # exponent 1: a fixed fraction
+    assert f(65536, 64, 80, 262144, 0.0) == 80             # exponent 0: a fixed budget
+    assert f(32768, 64, 80, 262144, 0.5) == 29             # ceil(80 / sqrt(8)) = ceil(28.28)
+    assert f(1024, 64, 80, 262144, 0.0) == 14              # clamped to nb - 2 candidates
+    assert f(64, 64, 5, 64, 0.5) == 0                      # one block: no candidates
+    ks = [f(L, 64, 80, 262144, 0.5) for L in (4096, 8192, 16384, 32768, 65536, 131072, 262144)]
+    assert ks == sorted(ks)                                 # monotone in L
+    for L in (8192, 32768):                                 # doubling L scales by 2^e (up to the ceiling)
+        assert abs(f(2 * L, 64, 80, 262144, 0.5) - f(L, 64, 80, 262144, 0.5) * 2 ** 0.5) <= 2
+    assert f(0, 64, 80, 262144, 0.5) == -1 and f(4096, 64, 80, 262144, 1.5) == -1
+
+
 def test_workspace_queries(sa):
     assert sa.sa_decode_workspace_bytes(8, 1, 32, 8, 128, 34) >= 8 * 8 * 34 * 4 * 130 * 4
     assert sa.sa_decode_workspace_bytes(1, 1, 3, 2, 128, 10) == 0  # Hq not a multiple of Hkv

@@ -51,6 +51,7 @@ SIGNATURES = {
                         _vp, _vp, _i, _vp], _i),
     "sa_select_topdelta": ([_vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _f, _vp, _vp, _i, _vp], _i),
     "sa_select_kmax": ([_i, _i, _i, _i, _i, _i, _i], _i),
+    "sa_budget_sublinear": ([_i, _i, _i, _i, _f], _i),
     "sa_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "sa_decode": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "sa_decode_noalloc": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
@@ -121,6 +122,11 @@ def sa_append_kv(k_new, v_new, k_cache, v_cache, pos, block, sketch, stream=None
     Ls = k_cache.shape[2]
     _check(lib.sa_append_kv(_ptr(k_new), _ptr(v_new), _dtype(k_new), B, Hkv, T, d, _ptr(k_cache), _ptr(v_cache),
                             Ls, pos, block, _ptr(sketch), _stream(stream)))
+
+
+def sa_budget_sublinear(L, block, k_ref, L_ref, exponent) -> int:
+    """Length-aware block budget k(L) = ceil(k_ref * (L / L_ref)^exponent), clamped to the candidates."""
+    return lib.sa_budget_sublinear(L, block, k_ref, L_ref, float(exponent))
 
 
 def sa_select_kmax(L, block, qtile, prefill, k, frac_num=0, frac_den=1) -> int:

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -725,6 +726,14 @@ sa_status_t sa_append_kv(const void* k_new, const void* v_new, int dtype, int B,
                                 as_stream(stream));
   return launch_append<__nv_bfloat16>(k_new, v_new, B, Hkv, T, d, k_cache, v_cache, L_stride, pos, block, sketch,
                                       as_stream(stream));
+}
+
+int sa_budget_sublinear(int L, int block, int k_ref, int L_ref, float exponent) {
+  if (L < 1 || block < 1 || k_ref < 0 || L_ref < 1 || !(exponent >= 0.f && exponent <= 1.f)) return -1;
+  const int nb = cdiv(L, block);
+  const double k = std::ceil(static_cast<double>(k_ref) * std::pow(static_cast<double>(L) / L_ref, exponent) - 1e-9);
+  const double cap = std::max(nb - 2, 0);
+  return static_cast<int>(std::min(std::max(k, 0.0), cap));
 }
 
 int sa_select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num, int frac_den) {
