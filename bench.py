@@ -578,7 +578,7 @@ def bench_length_sweep(lengths, k_ref, L_ref, exponent, reps=20):
     if sa.sa_device_status() != 0:
         raise RuntimeError("device status word set during the length sweep")
     return {"sweep": "length-aware budget", "budget": "k(L) = ceil(%d * (L / %d)^%g)" % (k_ref, L_ref, exponent),
-            "workload": "decode B=1 T=4 Hq=32 Hkv=8 d=128 block 64, bf16, 0.5%% needle blocks", "rows": rows}
+            "workload": "decode B=1 T=4 Hq=32 Hkv=8 d=128 block 64, bf16, 0.5% needle blocks", "rows": rows}
 
 
 def _kernel_hash():
