@@ -11,192 +11,240 @@
 // top-k then picks exactly those candidates (they are the highest ones).
 //
 // Top-k is an exact MSB-first radix select on order-preserving 32-bit keys of
-// the float32 scores (four 8-bit digit passes over a 256-bin shared-memory
-// histogram), followed by an index-ordered scan that resolves ties at the
-// threshold key and compacts the selection in ascending order.
+// the float32 scores (four 8-bit digit passes over 256-bin shared-memory
+// histograms), followed by an index-ordered pass that admits ties at the
+// threshold key lowest index first and writes the selection in ascending order.
 #pragma once
+
+#include <cstddef>
+#include <type_traits>
 
 #include "sa_ptx.cuh"
 
 namespace sa {
 
 constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
 
 constexpr int kTopkMaxN = 16384;  // candidates per selection (blocks per sequence)
 
 struct TopkShared {
-  uint32_t hist[kSelThreads / 32][256];  // per-warp digit histograms
-  uint32_t tot[256];
-  uint32_t warp_tot[kSelThreads / 32];
-  uint32_t dsel, rem_next, cnt_dsel;
-  uint32_t bits[kTopkMaxN / 32];    // selection bitmap, index order
-  uint32_t eqbits[kTopkMaxN / 32];  // candidates tied with the threshold key
+  uint32_t hist[4][256];     // one digit histogram per radix pass (8-bit digits, MSB first)
+  uint32_t wdef[kSelWarps];  // per-warp count of selections decided without ties
+  uint32_t weq[kSelWarps];   // per-warp count of candidates tied with the threshold key
 };
 
-// Exclusive block-wide prefix sum of v (all kSelThreads threads); *total gets the sum.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, TopkShared& S, uint32_t* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  uint32_t inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-    if (lane >= o) inc += y;
-  }
-  if (lane == 31) S.warp_tot[w] = inc;
-  __syncthreads();
-  uint32_t before = 0, all = 0;
-#pragma unroll
-  for (int i = 0; i < kSelThreads / 32; ++i) {
-    const uint32_t x = S.warp_tot[i];
-    before += (i < w) ? x : 0u;
-    all += x;
-  }
-  __syncthreads();
-  *total = all;
-  return before + inc - v;
+// Shared-memory accesses by 32-bit shared-window address (explicit state space,
+// so that no access falls back to generic addressing).
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 lds_f32x2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u32x4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
-// Select from scores sc[0:n) (shared memory, n <= kTopkMaxN): the forced blocks
-// are the first and the last (0 and n-1, one block when n == 1); the candidates
-// are 1..n-2; keep min(budget, n-2) of them with the highest scores, ties to the
-// lower index.  Writes idx_out[0:kmax] (ascending, -1 padded) and *cnt_out.
-// All kSelThreads threads call.
+// Select from scores at shared address sc (n floats, n <= kTopkMaxN): the forced
+// blocks are the first and the last (0 and n-1, one block when n == 1); the
+// candidates are 1..n-2; keep min(budget, n-2) of them with the highest scores,
+// ties to the lower index.  Writes idx_out[0:kmax] (ascending, -1 padded) and
+// *cnt_out.  S: shared address of a TopkShared.  All kSelThreads threads call;
+// six block barriers in all.
 //
-// Exact radix select of the threshold key (4 x 8-bit digits, per-warp
-// histograms), then a selection bitmap built with warp ballots (keys above the
-// threshold, plus the lowest-index ties at it), compacted in index order.
-__device__ void block_topk(const float* sc, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
-                           int32_t* __restrict__ cnt_out, TopkShared& S) {
+// Threshold: exact MSB-first radix select of the take-th largest order-preserving
+// key (four 8-bit digit passes, each into its own 256-bin histogram; every warp
+// then finds the digit itself, so a pass costs one barrier).  Output: each warp
+// owns a contiguous span of indices, counts its keys above the threshold and its
+// ties, and after one barrier writes its selections at their ascending
+// positions; ties at the threshold are admitted in index order until the budget
+// is met.
+__device__ __forceinline__ void block_topk(uint32_t sc, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
+                                           int32_t* __restrict__ cnt_out, uint32_t S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t hist = S + static_cast<uint32_t>(offsetof(TopkShared, hist));
+  const uint32_t wdef = S + static_cast<uint32_t>(offsetof(TopkShared, wdef));
+  const uint32_t weq = S + static_cast<uint32_t>(offsetof(TopkShared, weq));
   const int last = n - 1;                      // forced local / diagonal block
   const int ncand = n > 2 ? n - 2 : 0;         // candidates 1 .. n-2
   const int take = budget <= 0 ? 0 : (budget < ncand ? budget : ncand);
-  const int take_all = take == ncand ? 1 : 0;
-  uint32_t thr = 0xFFFFFFFFu, need_eq = 0, cnt_eq = 0;
-  if (take_all == 0 && take > 0) {
-    uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(take);
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&S.hist[0][0])[i] = 0;
-      __syncthreads();
+  const bool by_key = take > 0 && take < ncand;
+  uint32_t thr = 0u, need_eq = 0u;
+  if (by_key) {
+    for (int i = tid; i < 4 * 256 / 4; i += kSelThreads)
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(hist + 16u * i), "r"(0u) : "memory");
+    __syncthreads();
+    uint32_t prefix = 0u, mask = 0u, remaining = static_cast<uint32_t>(take);
+    for (int p = 0; p < 4; ++p) {
+      const int shift = 24 - 8 * p;
+      const uint32_t hp = hist + 1024u * p;
       for (int b = 1 + tid; b < last; b += kSelThreads) {
-        const uint32_t key = float_key(sc[b]);
-        if ((key & mask) == prefix) atomicAdd(&S.hist[warp][(key >> shift) & 255u], 1u);
+        const uint32_t key = float_key(lds_f32(sc + 4u * b));
+        if ((key & mask) == prefix) red_add_shared(hp + 4u * ((key >> shift) & 255u), 1u);
       }
       __syncthreads();
-      {
-        uint32_t t = 0;
+      // lane l holds digits 255-8l .. 248-8l (descending); the chosen digit is the
+      // one where the count of keys above it stays below `remaining` and the count
+      // including it reaches it (exactly one (lane, e) qualifies)
+      const uint4 lo4 = lds_u32x4(hp + 4u * (248 - 8 * lane)), hi4 = lds_u32x4(hp + 4u * (252 - 8 * lane));
+      const uint32_t c[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
+      uint32_t sum = 0u;
 #pragma unroll
-        for (int w = 0; w < kSelThreads / 32; ++w) t += S.hist[w][tid];
-        S.tot[tid] = t;
+      for (int e = 0; e < 8; ++e) sum += c[e];
+      uint32_t inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
       }
-      __syncthreads();
-      if (warp == 0) {
-        // lane l holds digits 255-8l .. 248-8l (descending); find the digit at
-        // which the count of keys above it, plus its own, reaches `remaining`
-        uint32_t c[8], s = 0;
+      uint32_t run = inc - sum, hit = 0u, dsel = 0u, rem = 0u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          c[e] = S.tot[255 - 8 * lane - e];
-          s += c[e];
+      for (int e = 0; e < 8; ++e) {
+        if (hit == 0u && run < remaining && remaining <= run + c[e]) {
+          hit = 1u;
+          dsel = 255u - 8u * static_cast<uint32_t>(lane) - static_cast<uint32_t>(e);
+          rem = remaining - run;
         }
-        uint32_t inc = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-          if (lane >= o) inc += y;
-        }
-        uint32_t run = inc - s;  // keys in higher digits than this lane's first
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (run < remaining && remaining <= run + c[e]) {  // exactly one (lane, e) matches
-            S.dsel = 255u - 8u * static_cast<uint32_t>(lane) - static_cast<uint32_t>(e);
-            S.rem_next = remaining - run;
-            S.cnt_dsel = c[e];
-          }
-          run += c[e];
-        }
+        run += c[e];
       }
-      __syncthreads();
-      prefix |= S.dsel << shift;
+      const int src = (__ffs(__ballot_sync(0xFFFFFFFFu, hit != 0u)) - 1) & 31;
+      dsel = __shfl_sync(0xFFFFFFFFu, dsel, src);
+      rem = __shfl_sync(0xFFFFFFFFu, rem, src);
+      prefix |= dsel << shift;
       mask |= 255u << shift;
-      remaining = S.rem_next;
-      cnt_eq = S.cnt_dsel;
-      __syncthreads();  // S.dsel is rewritten by the next pass
+      remaining = rem;
     }
     thr = prefix;
-    need_eq = remaining;  // ties at the threshold still to take (lowest indices first)
+    need_eq = remaining;  // ties at the threshold key to admit, lowest indices first
   }
-  const int surplus = (cnt_eq > need_eq) ? 1 : 0;  // more ties than places: resolve by index
-  const int nwords = (n + 31) >> 5;
-  for (int base = 0; base < n; base += kSelThreads) {
-    const int b = base + tid;
-    bool sel = false, eq = false;
-    if (b < n) {
-      if (b == 0 || b == last || take_all != 0) {
-        sel = true;
-      } else if (take > 0) {
-        const uint32_t key = float_key(sc[b]);
-        sel = key > thr || (key == thr && surplus == 0);
-        eq = surplus != 0 && key == thr;
+  // classes of index b: `def` = kept regardless of ties, `eq` = tied with the threshold key
+  auto classify = [&](int b, bool& def, bool& eq) {
+    def = false;
+    eq = false;
+    if (b >= n) return;
+    if (b == 0 || b == last) {
+      def = true;
+    } else if (take > 0) {
+      if (!by_key) {
+        def = true;
+      } else {
+        const uint32_t key = float_key(lds_f32(sc + 4u * b));
+        def = key > thr;
+        eq = key == thr;
       }
     }
-    const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
-    const uint32_t be = __ballot_sync(0xFFFFFFFFu, eq);
-    const int word = (base >> 5) + warp;
-    if (lane == 0 && word < nwords) {
-      S.bits[word] = bs;
-      S.eqbits[word] = be;
-    }
+  };
+  const int span = ((n + kSelThreads - 1) / kSelThreads) * 32;  // indices per warp, a multiple of 32
+  const int w0 = warp * span;
+  uint32_t ndef = 0u, neq = 0u;
+  for (int base = w0; base < w0 + span; base += 32) {
+    bool d, e;
+    classify(base + lane, d, e);
+    ndef += __popc(__ballot_sync(0xFFFFFFFFu, d));
+    neq += __popc(__ballot_sync(0xFFFFFFFFu, e));
+  }
+  if (lane == 0) {
+    sts_u32(wdef + 4u * warp, ndef);
+    sts_u32(weq + 4u * warp, neq);
   }
   __syncthreads();
-  if (surplus != 0 && tid == 0) {
-    uint32_t need = need_eq;
-    for (int w = 0; w < nwords && need > 0; ++w) {
-      uint32_t e = S.eqbits[w];
-      while (e && need > 0) {
-        const uint32_t lo = e & (~e + 1u);
-        S.bits[w] |= lo;
-        e ^= lo;
-        --need;
-      }
-    }
+  uint32_t def_before = 0u, eq_before = 0u, def_all = 0u, eq_all = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    const uint32_t a = lds_u32(wdef + 4u * w), e = lds_u32(weq + 4u * w);
+    def_before += w < warp ? a : 0u;
+    eq_before += w < warp ? e : 0u;
+    def_all += a;
+    eq_all += e;
   }
-  __syncthreads();
-  uint32_t running = 0;
-  for (int wb = 0; wb < nwords; wb += kSelThreads) {
-    const int w = wb + tid;
-    uint32_t word = w < nwords ? S.bits[w] : 0u;
-    uint32_t total;
-    uint32_t pos = running + block_excl_scan(static_cast<uint32_t>(__popc(word)), S, &total);
-    while (word) {
-      const int bit = __ffs(word) - 1;
-      if (pos < static_cast<uint32_t>(kmax)) idx_out[pos] = w * 32 + bit;
-      ++pos;
-      word &= word - 1u;
+  const uint32_t total = def_all + min(eq_all, need_eq);
+  uint32_t pos = def_before + min(eq_before, need_eq);
+  uint32_t eq_seen = eq_before;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = w0; base < w0 + span; base += 32) {
+    bool d, e;
+    classify(base + lane, d, e);
+    const uint32_t eb = __ballot_sync(0xFFFFFFFFu, e);
+    const bool sel = d || (e && eq_seen + static_cast<uint32_t>(__popc(eb & lt)) < need_eq);
+    const uint32_t sb = __ballot_sync(0xFFFFFFFFu, sel);
+    if (sel) {
+      const uint32_t at = pos + static_cast<uint32_t>(__popc(sb & lt));
+      if (at < static_cast<uint32_t>(kmax)) idx_out[at] = base + lane;
     }
-    running += total;
+    pos += static_cast<uint32_t>(__popc(sb));
+    eq_seen += static_cast<uint32_t>(__popc(eb));
   }
-  for (int i = static_cast<int>(running) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
-  if (tid == 0) *cnt_out = static_cast<int32_t>(running);
+  for (int i = static_cast<int>(total) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
+  if (tid == 0) *cnt_out = static_cast<int32_t>(total);
 }
 
 // --------------------------------------------------------------------------
 // Decode selection.  grid (CS, groups), cluster (CS, 1, 1), kSelThreads.
-// Each CTA of a group's cluster scores blocks [rank*per, rank*per + per) from
-// a TMA-staged, 128B-swizzled sketch tile (thread per block, q broadcast from
-// shared memory); CTA rank 0 then gathers the group's scores through
-// distributed shared memory and runs the top-k.
-constexpr int kSelTileRows = 256;
+// CTA rank r of group g's cluster scores blocks [r*per, r*per + per) of the
+// group's sketch; the scores go straight into CTA rank 0's shared memory
+// (distributed shared memory), and after one cluster barrier rank 0 runs the
+// top-k over all nb scores.
+//
+// The sketch rows arrive by TMA in chunks of 64 rows (one mbarrier per chunk,
+// 128-byte swizzle, one box per 32 columns), so scoring starts on the first
+// chunk while the rest are in flight.  bf16 queries: the scores are a small
+// matrix product S[row, r] = sketch[row, :] . q[r, :] on the tensor cores
+// (mma.sync m16n8k16, fp32 accumulation), with the fp32 sketch split into
+// three bf16 parts (hi, mid, lo: each the rounded remainder of the previous)
+// so that the product keeps float32 accuracy while q (bf16) is exact; one warp
+// per 16-row M tile, the max over the group's R rows taken from the
+// accumulator fragments.  fp32 queries: one thread per row, FMA dot products.
+constexpr int kSelTileRows = 256;  // rows staged per pass (at most 4 chunks)
+constexpr int kSelChunkRows = 64;
 
-// Shared layout (runtime): staged sketch tile | q rows | gathered scores (rank 0) | top-k scratch | mbarrier
+// bytes of the staged query rows: bf16 rows (whole n8 tiles; rows past the
+// group's R only feed accumulator columns that are never read), or fp32 rows
+// with the scale folded in for fp32 queries
+__host__ __device__ constexpr int sel_q_bytes(int D, int RMAX, bool bf16) {
+  return bf16 ? ((RMAX + 7) / 8) * 8 * D * 2 : RMAX * D * 4;
+}
+
+// Shared layout (runtime): staged sketch chunks | q rows | gathered scores (rank 0) | top-k scratch |
+// mbarriers (one per sketch chunk, then one for q)
 struct SelDecodeLayout {
   int tile_bytes, q_bytes, nb;
   __host__ __device__ int q_off() const { return tile_bytes; }
   __host__ __device__ int all_off() const { return tile_bytes + q_bytes; }
   __host__ __device__ int topk_off() const { return all_off() + ((nb * 4 + 15) / 16) * 16; }
   __host__ __device__ int bar_off() const { return topk_off() + static_cast<int>(((sizeof(TopkShared) + 15) / 16) * 16); }
-  __host__ __device__ int bytes() const { return bar_off() + 16 + 1024; }
+  __host__ __device__ int bytes() const { return bar_off() + 64 + 1024; }
 };
+
+// staged bytes for a pass of tile_rows rows with D fp32 columns
+__host__ __device__ constexpr int sel_tile_bytes(int tile_rows, int D) {
+  return ((tile_rows + kSelChunkRows - 1) / kSelChunkRows) * (D * 4 / 128) * kSelChunkRows * 128;
+}
 
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
@@ -208,28 +256,57 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-// grid (CS, groups), cluster (CS, 1, 1), kSelThreads threads.  CTA rank r of
-// group g's cluster scores blocks [r*per, r*per + per): its sketch rows come in
-// by TMA (128B-swizzled tiles of tile_rows rows), one thread per block, q rows
-// broadcast from shared memory.  Each score is stored straight into CTA rank
-// 0's gather array (distributed shared memory); after one cluster barrier rank
-// 0 holds all nb scores and runs the top-k.
+// c += a * b, m16n8k16, bf16 inputs, fp32 accumulators
+__device__ __forceinline__ void sel_mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (x0, x1) = hi + mid + lo, each a bf16 pair (x0 in the low half), each part
+// the bf16 rounding of what the previous parts leave (the remainders are exact
+// in fp32), so the three carry 24 significant bits of each value.
+__device__ __forceinline__ void split3_bf16(float x0, float x1, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  hi = pack_bf16x2(x0, x1);
+  const float r0 = x0 - __uint_as_float(hi << 16), r1 = x1 - __uint_as_float(hi & 0xFFFF0000u);
+  mid = pack_bf16x2(r0, r1);
+  const float s0 = r0 - __uint_as_float(mid << 16), s1 = r1 - __uint_as_float(mid & 0xFFFF0000u);
+  lo = pack_bf16x2(s0, s1);
+}
+
+// byte offset of fp32 column c (even) of staged row r in the chunked, swizzled tile
+template <int D>
+__device__ __forceinline__ uint32_t sel_tile_off(int r, int c) {
+  constexpr int kBoxes = D * 4 / 128;
+  const int rr = r & (kSelChunkRows - 1), cb = c & 31;
+  return static_cast<uint32_t>((((r >> 6) * kBoxes + (c >> 5)) * kSelChunkRows + rr) * 128 +
+                               ((((cb >> 2) ^ (rr & 7))) << 4) + (cb & 3) * 4);
+}
+
+// grid (CS, groups), cluster (CS, 1, 1), kSelThreads threads.
 template <typename TE, int D, int RMAX>
 __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
     const __grid_constant__ CUtensorMap sk_map, const TE* __restrict__ q, int T, int Hq, int Hkv, int nb,
     int nb_cap, float scale, int per, int tile_rows, int k, float* __restrict__ scores_out,
     int32_t* __restrict__ idx, int32_t* __restrict__ cnt, int kmax, int topdelta, float delta) {
   constexpr int kBoxes = D * 4 / 128;
+  constexpr bool kTc = std::is_same<TE, __nv_bfloat16>::value;
+  constexpr int NT = ((RMAX + 7) / 8) * 8;  // query rows padded to whole n8 tiles
+  constexpr uint32_t kChunkBytes = kBoxes * kSelChunkRows * 128;
   extern __shared__ __align__(1024) uint8_t smem_sel_dec[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_sel_dec) + 1023) & ~uintptr_t(1023));
-  const SelDecodeLayout lay{kBoxes * tile_rows * 128, RMAX * D * 4, nb};
-  float* q_s = reinterpret_cast<float*>(smem + lay.q_off());
-  float* all = reinterpret_cast<float*>(smem + lay.all_off());
-  TopkShared& S = *reinterpret_cast<TopkShared*>(smem + lay.topk_off());
-  const uint32_t bar = smem_u32(smem + lay.bar_off());
+  // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
+  uint8_t* smem = smem_sel_dec + ((1024u - (smem_u32(smem_sel_dec) & 1023u)) & 1023u);
+  const SelDecodeLayout lay{sel_tile_bytes(tile_rows, D), sel_q_bytes(D, RMAX, kTc), nb};
+  const uint32_t tile = smem_u32(smem);
+  const uint32_t q_sh = tile + lay.q_off();
+  const uint32_t all = tile + lay.all_off();     // rank 0: the group's nb scores
+  const uint32_t topk_s = tile + lay.topk_off();  // TopkShared
+  const uint32_t bar0 = tile + lay.bar_off();     // chunk c's mbarrier at bar0 + 8c
 
   cluster_arrive_relaxed();  // paired with the wait before the first remote store
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.y;
   const uint32_t rank = cluster_ctarank();
   const int G = Hq / Hkv, R = G * T;
@@ -237,88 +314,187 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
   const int b0 = static_cast<int>(rank) * per;
   const int b1 = min(nb, b0 + per);
 
-  auto issue_tile = [&](int t0) {  // thread 0: the sketch rows t0 .. t0 + tile_rows - 1 of this group
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(lay.tile_bytes));
-#pragma unroll
-    for (int bx = 0; bx < kBoxes; ++bx)
-      tma_g2s_2d(smem_u32(smem + bx * tile_rows * 128), &sk_map, bx * 32, g * nb_cap + t0, bar);
-  };
+  constexpr int kChunks = kSelTileRows / kSelChunkRows;
+  const uint32_t qbar = bar0 + 8 * kChunks;
   pdl_launch_dependents();
   if (tid == 0) {
     prefetch_tmap(&sk_map);
-    mbar_init(bar, 1);
+#pragma unroll
+    for (int c = 0; c <= kChunks; ++c) mbar_init(bar0 + 8 * c, 1);
     fence_mbar_init();
   }
   pdl_wait();  // the sketch and q may come from the previous kernel
-  if (tid == 0 && b0 < b1) issue_tile(b0);  // the first tile's copy overlaps the q staging below
-  for (int i = tid; i < RMAX * D; i += kSelThreads) {
-    const int r = i / D, c = i % D;
-    float v = 0.f;
-    if (r < R) {
-      const int t = r / G, hh = r % G;
-      v = static_cast<float>(q[((static_cast<size_t>(b) * T + t) * Hq + kvh * G + hh) * D + c]) * scale;
-    }
-    q_s[i] = v;
-  }
-  __syncthreads();
-  const uint32_t all0 = map_cluster(smem_u32(all), 0);  // rank 0's gather array
-  bool waited = false;
 
+  auto issue_pass = [&](int t0) {  // thread 0: the sketch chunks of the pass starting at row t0
+    const int nch = (min(tile_rows, b1 - t0) + kSelChunkRows - 1) / kSelChunkRows;
+    for (int c = 0; c < nch; ++c) {
+      mbar_arrive_expect_tx(bar0 + 8 * c, kChunkBytes);
+#pragma unroll
+      for (int bx = 0; bx < kBoxes; ++bx)
+        tma_g2s_2d(tile + (c * kBoxes + bx) * kSelChunkRows * 128, &sk_map, bx * 32,
+                   g * nb_cap + t0 + c * kSelChunkRows, bar0 + 8 * c);
+    }
+  };
+  // q rows of this group (row r = t * G + head; the G heads of a token are
+  // contiguous): bf16 rows come in by bulk copies queued ahead of the sketch
+  if constexpr (kTc) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(R * D * 2));
+      for (int t = 0; t < T; ++t)
+        bulk_g2s(q_sh + t * G * D * 2,
+                 q + ((static_cast<size_t>(b) * T + t) * Hq + kvh * G) * D, G * D * 2, qbar);
+      if (b0 < b1) issue_pass(b0);
+    }
+  } else {
+    if (tid == 0 && b0 < b1) issue_pass(b0);
+    for (int i = tid; i < RMAX * D; i += kSelThreads) {
+      const int r = i / D, c = i % D;
+      float v = 0.f;
+      if (r < R) {
+        const int t = r / G, hh = r % G;
+        v = static_cast<float>(q[((static_cast<size_t>(b) * T + t) * Hq + kvh * G + hh) * D + c]) * scale;
+      }
+      sts_f32(q_sh + 4u * i, v);
+    }
+  }
+  const uint32_t all0 = map_cluster(all, 0);  // rank 0's gather array
+  __syncthreads();  // fp32 q staged
+  cluster_wait();   // every CTA of the cluster is running: remote stores are safe
   bool ok = true;
-  uint32_t phase = 0;
-  for (int t0 = b0; t0 < b1; t0 += tile_rows) {
-    if (tid == 0 && t0 != b0) issue_tile(t0);
-    ok = mbar_wait(bar, phase);
-    phase ^= 1;
-    if (__syncthreads_or(!ok)) break;
-    const int row = t0 + tid;
-    float s = -INFINITY;
-    if (tid < tile_rows && row < b1) {
-      float acc[RMAX];
+  const int gq = lane >> 2, tq = lane & 3;
+  // B fragments (q, k16 x n8, two bf16 along k per register) held in registers
+  uint32_t bq[kTc ? NT / 8 : 1][kTc ? D / 16 : 1][2];
+  if constexpr (kTc) {
+    ok = mbar_wait(qbar, 0);
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < D / 4; ++c) {
-        const int bx = c >> 3, cc = c & 7;
-        const float4 kv =
-            *reinterpret_cast<const float4*>(smem + bx * tile_rows * 128 + tid * 128 + ((cc ^ (tid & 7)) << 4));
+    for (int nt = 0; nt < NT / 8; ++nt) {
 #pragma unroll
-        for (int r = 0; r < RMAX; ++r) {
-          const float4 qv = *reinterpret_cast<const float4*>(q_s + r * D + c * 4);
-          acc[r] = fmaf(qv.x, kv.x, acc[r]);
-          acc[r] = fmaf(qv.y, kv.y, acc[r]);
-          acc[r] = fmaf(qv.z, kv.z, acc[r]);
-          acc[r] = fmaf(qv.w, kv.w, acc[r]);
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t qb = q_sh + 2u * ((nt * 8 + gq) * D + ks * 16 + 2 * tq);
+        bq[nt][ks][0] = lds_u32(qb);
+        bq[nt][ks][1] = lds_u32(qb + 16u);
+      }
+    }
+  }
+  int pass = 0;
+  for (int t0 = b0; t0 < b1; t0 += tile_rows, ++pass) {
+    const int rows = min(tile_rows, b1 - t0);
+    const int nch = (rows + kSelChunkRows - 1) / kSelChunkRows;
+    const uint32_t parity = static_cast<uint32_t>(pass & 1);
+    if (tid == 0 && pass > 0) issue_pass(t0);
+    if constexpr (kTc) {
+      int have = -1;  // chunk this warp has waited for
+      for (int m = warp; m * 16 < rows; m += kSelWarps) {
+        const int ch = (m * 16) / kSelChunkRows;
+        if (ch != have) {
+          ok = mbar_wait(bar0 + 8 * ch, parity) && ok;
+          have = ch;
+        }
+        // hi, mid and lo products accumulate separately (three independent MMA chains)
+        float acc[3][NT / 8][4];
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+#pragma unroll
+          for (int nt = 0; nt < NT / 8; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
+        const int r0 = m * 16 + gq, r1 = r0 + 8;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int c0 = ks * 16 + 2 * tq;
+          const float2 x00 = lds_f32x2(tile + sel_tile_off<D>(r0, c0));
+          const float2 x10 = lds_f32x2(tile + sel_tile_off<D>(r1, c0));
+          const float2 x01 = lds_f32x2(tile + sel_tile_off<D>(r0, c0 + 8));
+          const float2 x11 = lds_f32x2(tile + sel_tile_off<D>(r1, c0 + 8));
+          uint32_t ah[4], am[4], al[4];
+          split3_bf16(x00.x, x00.y, ah[0], am[0], al[0]);
+          split3_bf16(x10.x, x10.y, ah[1], am[1], al[1]);
+          split3_bf16(x01.x, x01.y, ah[2], am[2], al[2]);
+          split3_bf16(x11.x, x11.y, ah[3], am[3], al[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT / 8; ++nt) {
+            sel_mma_bf16(acc[0][nt], ah, bq[nt][ks][0], bq[nt][ks][1]);
+            sel_mma_bf16(acc[1][nt], am, bq[nt][ks][0], bq[nt][ks][1]);
+            sel_mma_bf16(acc[2][nt], al, bq[nt][ks][0], bq[nt][ks][1]);
+          }
+        }
+        // row max over the group's R query rows (accumulator columns n < R)
+        float s0 = -INFINITY, s1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT / 8; ++nt) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (nt * 8 + 2 * tq + j < R) {
+              s0 = fmaxf(s0, scale * (acc[0][nt][j] + (acc[1][nt][j] + acc[2][nt][j])));
+              s1 = fmaxf(s1, scale * (acc[0][nt][2 + j] + (acc[1][nt][2 + j] + acc[2][nt][2 + j])));
+            }
+          }
+        }
+        s0 = fmaxf(s0, __shfl_xor_sync(0xFFFFFFFFu, s0, 1));
+        s0 = fmaxf(s0, __shfl_xor_sync(0xFFFFFFFFu, s0, 2));
+        s1 = fmaxf(s1, __shfl_xor_sync(0xFFFFFFFFu, s1, 1));
+        s1 = fmaxf(s1, __shfl_xor_sync(0xFFFFFFFFu, s1, 2));
+        if (tq == 0) {
+          if (r0 < rows) {
+            if (scores_out) scores_out[static_cast<size_t>(g) * nb + t0 + r0] = s0;
+            st_cluster_f32(all0 + 4u * static_cast<uint32_t>(t0 + r0), s0);
+          }
+          if (r1 < rows) {
+            if (scores_out) scores_out[static_cast<size_t>(g) * nb + t0 + r1] = s1;
+            st_cluster_f32(all0 + 4u * static_cast<uint32_t>(t0 + r1), s1);
+          }
         }
       }
+      // chunks this warp never waited for: their copies have still landed before
+      // the buffer is reused (the barrier below orders every warp after them)
+      if (tid == 0) {
+        for (int c = 0; c < nch; ++c) ok = mbar_wait(bar0 + 8 * c, parity) && ok;
+      }
+    } else {
+      const int r = tid;
+      if (r < rows) {
+        ok = mbar_wait(bar0 + 8 * (r / kSelChunkRows), parity) && ok;
+        float acc[RMAX];
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r)
-        if (r < R) s = fmaxf(s, acc[r]);
-      if (scores_out) scores_out[static_cast<size_t>(g) * nb + row] = s;
+        for (int i = 0; i < RMAX; ++i) acc[i] = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D / 4; ++c) {
+          const float4 kv = lds_f32x4(tile + sel_tile_off<D>(r, c * 4));
+#pragma unroll
+          for (int i = 0; i < RMAX; ++i) {
+            const float4 qv = lds_f32x4(q_sh + 4u * (i * D + c * 4));
+            acc[i] = fmaf(qv.x, kv.x, acc[i]);
+            acc[i] = fmaf(qv.y, kv.y, acc[i]);
+            acc[i] = fmaf(qv.z, kv.z, acc[i]);
+            acc[i] = fmaf(qv.w, kv.w, acc[i]);
+          }
+        }
+        float s = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < RMAX; ++i)
+          if (i < R) s = fmaxf(s, acc[i]);
+        if (scores_out) scores_out[static_cast<size_t>(g) * nb + t0 + r] = s;
+        st_cluster_f32(all0 + 4u * static_cast<uint32_t>(t0 + r), s);
+      }
+      if (tid == 0) {
+        for (int c = 0; c < nch; ++c) ok = mbar_wait(bar0 + 8 * c, parity) && ok;
+      }
     }
-    if (!waited) {
-      cluster_wait();  // every CTA of the cluster is running: remote stores are safe
-      waited = true;
-    }
-    if (tid < tile_rows && row < b1) st_cluster_f32(all0 + 4u * static_cast<uint32_t>(row), s);
-    __syncthreads();  // the tile buffer is refilled next iteration
+    if (__syncthreads_or(!ok)) break;  // the staged chunks are refilled next pass
   }
-  if (!waited) cluster_wait();
   cluster_sync();  // all scores have landed in rank 0
   if (rank != 0) return;
   int budget = k;
   if (topdelta) {
     // top-delta ("Faster Than Flash" Sec. 2): the candidates scoring at least the
     // pseudo-maximum (over the sink and local blocks) minus delta, at most k of them
-    const float thr = fmaxf(all[0], all[nb - 1]) - delta;
+    const float thr = fmaxf(lds_f32(all), lds_f32(all + 4u * (nb - 1))) - delta;
     int c = 0;
     for (int base = 0; base < nb; base += kSelThreads) {
-      const int b = base + tid;
-      c += __syncthreads_count(b >= 1 && b < nb - 1 && all[b] >= thr);
+      const int bb = base + tid;
+      c += __syncthreads_count(bb >= 1 && bb < nb - 1 && lds_f32(all + 4u * bb) >= thr);
     }
     budget = min(c, k);
   }
-  block_topk(all, nb, budget, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, S);
+  block_topk(all, nb, budget, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, topk_s);
 }
 
 // --------------------------------------------------------------------------
@@ -331,9 +507,8 @@ __global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* 
                                                                    int32_t* __restrict__ idx,
                                                                    int32_t* __restrict__ cnt, int kmax) {
   extern __shared__ __align__(1024) uint8_t smem_sel_given[];
-  uint8_t* smem_raw = smem_sel_given;
-  TopkShared& S = *reinterpret_cast<TopkShared*>(smem_raw);
-  float* sc = reinterpret_cast<float*>(smem_raw + ((sizeof(TopkShared) + 15) / 16) * 16);
+  const uint32_t topk_s = smem_u32(smem_sel_given);
+  const uint32_t sc = topk_s + static_cast<uint32_t>(((sizeof(TopkShared) + 15) / 16) * 16);
   const int i = blockIdx.x, g = blockIdx.y, nq = gridDim.x;
   int nvalid = nb, budget = k;
   if (prefill) {
@@ -342,9 +517,9 @@ __global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* 
     if (frac_num > 0) budget = k + (frac_num * nvalid + frac_den - 1) / frac_den;
   }
   const size_t u = static_cast<size_t>(g) * nq + i;
-  for (int bb = threadIdx.x; bb < nvalid; bb += kSelThreads) sc[bb] = scores[u * nb + bb];
+  for (int bb = threadIdx.x; bb < nvalid; bb += kSelThreads) sts_f32(sc + 4u * bb, scores[u * nb + bb]);
   __syncthreads();
-  block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, S);
+  block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, topk_s);
 }
 
 }  // namespace sa

@@ -270,9 +270,11 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
   const int nb = cdiv(a.L, a.block);
   const int nb_cap = cdiv(a.Ls, a.block);
   auto kern = sa::select_decode_kernel<TE, D, RMAX>;
+  constexpr bool kBf16 = std::is_same<TE, __nv_bfloat16>::value;
   static int max_cs = 0;  // per instantiation
   if (max_cs == 0) {
-    sa::SelDecodeLayout big{(D * 4 / 128) * sa::kSelTileRows * 128, RMAX * D * 4, sa::kTopkMaxN};
+    sa::SelDecodeLayout big{sa::sel_tile_bytes(sa::kSelTileRows, D), sa::sel_q_bytes(D, RMAX, kBf16),
+                            sa::kTopkMaxN};
     SA_TRY(set_smem(kern, big.bytes()));
     cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     max_cs = std::max(1, std::min(16, max_cluster_size(reinterpret_cast<const void*>(kern), big.bytes(), groups, st)));
@@ -283,15 +285,16 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
   SA_SUP(cs <= max_cs, "decode selection over %d blocks needs a cluster of %d CTAs (device allows %d)", nb, cs,
          max_cs);
   cs = std::min(cs, nb);
-  const int per = cdiv(nb, cs);
+  // whole 64-row chunks per CTA (only the group's last CTA stages a partial one)
+  const int per = cdiv(cdiv(nb, cs), sa::kSelChunkRows) * sa::kSelChunkRows;
   cs = cdiv(nb, per);
-  const int tile_rows = std::min(sa::kSelTileRows, cdiv(per, 8) * 8);
-  const sa::SelDecodeLayout lay{(D * 4 / 128) * tile_rows * 128, RMAX * D * 4, nb};
+  const int tile_rows = std::min(sa::kSelTileRows, per);
+  const sa::SelDecodeLayout lay{sa::sel_tile_bytes(tile_rows, D), sa::sel_q_bytes(D, RMAX, kBf16), nb};
   const int smem = lay.bytes();
   SA_TRY(set_smem(kern, smem));
   CUtensorMap map;
   SA_TRY(make_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.sketch, D, static_cast<uint64_t>(groups) * nb_cap,
-                     D * 4, 32, tile_rows, CU_TENSOR_MAP_SWIZZLE_128B));
+                     D * 4, 32, sa::kSelChunkRows, CU_TENSOR_MAP_SWIZZLE_128B));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, groups);
   cfg.blockDim = dim3(sa::kSelThreads);
@@ -575,6 +578,7 @@ sa_status_t validate_select(const SelectArgs& a) {
   SA_ARG(aligned16(a.sketch), "sketch must be 16-byte aligned");
   if (!a.prefill) {
     SA_ARG(a.Tq >= 1, "Tq must be >= 1");
+    SA_ARG(a.dtype != SA_BF16 || aligned16(a.q), "bf16 q must be 16-byte aligned");
     SA_SUP((a.Hq / a.Hkv) * a.Tq <= 32, "G*Tq (%d) must be <= 32 for decode selection", (a.Hq / a.Hkv) * a.Tq);
   } else {
     SA_SUP(a.dtype == SA_BF16 && a.d == 128 && a.qtile == 128 && a.block == 128,
