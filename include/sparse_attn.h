@@ -143,8 +143,9 @@ sa_status_t sa_append_kv(const void* k_new, const void* v_new, int dtype, int B,
  *   q and sketch are not read.
  * idx: [B, Hkv, nq, kmax] int32 written (ascending, -1 padded), cnt:
  *   [B, Hkv, nq] int32 written.  kmax must be >= sa_select_kmax(...).
- * Requires d in {64, 128}; G * Tq <= 32 for decode; qtile == Bk == 128,
- * d == 128, bf16 q and scale > 0 for prefill in SKETCH mode.
+ * Requires d in {64, 128}; G * Tq <= 32 and (bf16) a 16-byte-aligned q for
+ * decode; qtile == Bk == 128, d == 128, bf16 q and scale > 0 for prefill in
+ * SKETCH mode.
  */
 sa_status_t sa_select_topk(int mode, const void* q, int dtype, const float* sketch, float* scores,
                            int B, int Tq, int Hq, int Hkv, int d, int L, int L_stride, int block,
