@@ -248,3 +248,34 @@ def prefill_select(q, k, wl, units, kmax=None, sketch=None, scores=None):
     kmax = kmax or int(budget.max() + 2)
     idx, cnt = select(scores, nvalid, nvalid - 1, budget, kmax)
     return idx, cnt, scores, sketch
+
+
+# ------------------------------------------------ head-collapsed token-level support
+
+def token_mass_decode(q, k, Hkv, L, scale):
+    """Head-collapsed token importance for decode ("How Much Dense Attention is Necessary?" Sec. 2.1
+    and 2.2: the dense attention distribution of each query, averaged over the query heads into one
+    distribution shared by every head; the T decode queries share one support, so they are averaged
+    too).  P[b, j] = mean over all Hq heads and the T queries of the dense causal softmax probability
+    of key j (query t sits at key position L - T + t).  Composed from `mass` at one-token blocks."""
+    B, T, Hq, _ = q.shape
+    units = [(g, 0) for g in range(B * Hkv)]
+    m = mass(q, k, Hkv, L, L - T, T, 1, scale, units)  # [B*Hkv, L]: summed over each group's heads and rows
+    return m.reshape(B, Hkv, L).sum(axis=1) / (Hq * T)
+
+
+def token_select(P, k, kmax=None):
+    """Token-level top-k on the shared distribution P [B, L]: the sink token 0 and the newest token
+    L - 1 are forced, plus the k highest of the others (ties -> lower index), ascending."""
+    B, L = P.shape
+    kmax = kmax or (k + 2)
+    return select(P, L, L - 1, k, kmax)
+
+
+def token_attend(q, k, v, Hkv, L, scale, idx, cnt, rows):
+    """Exact attention of (b, t, h) rows over the selected tokens idx [B, kmax] (shared by every kv
+    head of batch row b); query t sits at key position L - T + t and is causal."""
+    T = q.shape[1]
+    idx_g = np.repeat(np.asarray(idx, dtype=np.int32), Hkv, axis=0)
+    cnt_g = np.repeat(np.asarray(cnt, dtype=np.int32), Hkv)
+    return attend(q, k, v, Hkv, L, L - T, 1, scale, rows, idx_g, cnt_g)

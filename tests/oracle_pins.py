@@ -395,3 +395,72 @@ def pin_select_delta_special_cases():
     assert idx[0, : cnt[0]].tolist() == [0, 2, 3]
 
 ALL_PINS += [pin_select_delta_brute_force, pin_select_delta_special_cases]
+
+
+# ------------------------------------------------ head-collapsed token-level support
+
+def pin_token_mass_matches_library_softmax():
+    """Token mass == mean over all heads and decode rows of torch.softmax of the causal logits."""
+    r = _rng(11)
+    B, T, Hq, Hkv, d, L = 2, 3, 4, 2, 8, 37
+    G = Hq // Hkv
+    q = r.standard_normal((B, T, Hq, d))
+    k = r.standard_normal((B, Hkv, L, d))
+    scale = 0.45
+    P = oracle.token_mass_decode(q, k, Hkv, L, scale)
+    assert P.shape == (B, L)
+    for b in range(B):
+        ref = np.zeros(L)
+        for t in range(T):
+            for h in range(Hq):
+                logits = torch.from_numpy(scale * (k[b, h // G] @ q[b, t, h]))
+                logits[L - T + t + 1:] = -float("inf")
+                ref += torch.softmax(logits, 0).numpy()
+        np.testing.assert_allclose(P[b], ref / (Hq * T), rtol=1e-12, atol=1e-15)
+        assert abs(P[b].sum() - 1.0) < 1e-12 and np.all(P[b] >= 0.0)
+
+
+def pin_token_mass_uniform_closed_form():
+    """Identical keys: each row is uniform over its causal keys, so P[b, j] = mean_t [j <= L-T+t] / (L-T+t+1)."""
+    B, T, Hq, Hkv, d, L = 1, 4, 2, 1, 4, 19
+    r = _rng(12)
+    q = r.standard_normal((B, T, Hq, d))
+    k = np.tile(r.standard_normal(d), (B, Hkv, L, 1))
+    P = oracle.token_mass_decode(q, k, Hkv, L, 0.7)
+    ref = np.zeros(L)
+    for t in range(T):
+        n = L - T + t + 1
+        ref[:n] += 1.0 / n
+    np.testing.assert_allclose(P[0], ref / T, rtol=1e-12, atol=1e-15)
+
+
+def pin_token_select_and_attend_match_library():
+    """Shared token support: the selected tokens are the top-k of P (brute force) plus tokens 0 and L-1,
+    and attention over them equals SDPA with that token mask applied to every head."""
+    r = _rng(13)
+    B, T, Hq, Hkv, d, L, k = 2, 2, 4, 2, 8, 41, 7
+    G = Hq // Hkv
+    q = r.standard_normal((B, T, Hq, d))
+    kk = r.standard_normal((B, Hkv, L, d))
+    v = r.standard_normal((B, Hkv, L, d))
+    scale = 0.5
+    P = oracle.token_mass_decode(q, kk, Hkv, L, scale)
+    idx, cnt = oracle.token_select(P, k)
+    allowed = np.zeros((B, Hq, T, L), dtype=bool)
+    for b in range(B):
+        cands = sorted(range(1, L - 1), key=lambda j: (-P[b, j], j))[:k]
+        ref = sorted({0, L - 1} | set(cands))
+        assert idx[b, : cnt[b]].tolist() == ref
+        for t in range(T):
+            for j in ref:
+                if j <= L - T + t:
+                    allowed[b, :, t, j] = True
+    rows = [(b, t, h) for b in range(B) for t in range(T) for h in range(Hq)]
+    out, _ = oracle.token_attend(q, kk, v, Hkv, L, scale, idx, cnt, rows)
+    ref_o = _sdpa(q, kk, v, Hkv, allowed, scale)
+    for n, (b, t, h) in enumerate(rows):
+        np.testing.assert_allclose(out[n], ref_o[b, t, h], rtol=1e-10, atol=1e-12)
+
+
+ALL_PINS += [pin_token_mass_matches_library_softmax, pin_token_mass_uniform_closed_form,
+             pin_token_select_and_attend_match_library]
