@@ -581,6 +581,76 @@ def bench_length_sweep(lengths, k_ref, L_ref, exponent, reps=20):
             "workload": "decode B=1 T=4 Hq=32 Hkv=8 d=128 block 64, bf16, 0.5% needle blocks", "rows": rows}
 
 
+def bench_tokens(reps, peaks, peak_src):
+    """Head-collapsed token-level decode ("How Much Dense Attention is Necessary?" Sec. 2.1-2.2) on one
+    256K-token sequence (B=1, T=4, Hq=32, Hkv=8, d=128): dense token mass averaged over all heads and
+    queries, top-2048 tokens (+ sink and newest), attention over them shared by every kv head.  Each
+    rep flushes L2 (256 MB write, untimed) and times each call with CUDA events."""
+    import numpy as np
+    import torch
+
+    import synth
+    import top_block_sparse_pooled_b300 as sa
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = synth.WORKLOADS["c3"].replace(k=2048)
+    x = synth.make_inputs(wl)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, kc, vc = up(x.q), up(x.k), up(x.v)
+    del x
+    B, T, Hq, Hkv, d, L = wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, wl.L
+    R = (Hq // Hkv) * T
+    tws = torch.empty(sa.sa_token_mass_workspace_bytes(B, T, Hq, Hkv, L), dtype=torch.uint8, device=dev)
+    mass = torch.empty((B, L), dtype=torch.float32, device=dev)
+    kmax = sa.sa_select_kmax(L, 1, 0, False, wl.k)
+    idx = torch.empty((B, 1, 1, kmax), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, 1, 1), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    dws = torch.zeros(sa.sa_decode_workspace_bytes(B, T, Hq, Hkv, d, kmax), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    calls = {
+        "token_mass": lambda: sa.sa_token_mass_decode(q, kc, L, wl.scale, mass, tws),
+        "token_select": lambda: sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, mass.reshape(B, 1, 1, L), 1, L, L, 1,
+                                                  0, False, wl.k, 0, 1, 1.0, idx, cnt, d=d, dtype=sa.SA_F32, B=B,
+                                                  Tq=1, Hq=1),
+        "decode_tokens": lambda: sa.sa_decode_tokens(q, kc, vc, idx.reshape(B, kmax), cnt.reshape(B), L, wl.scale,
+                                                     out, dws),
+    }
+    ts = {name: [] for name in calls}
+    for r in range(reps + 2):
+        for name, fn in calls.items():
+            flush.fill_(r & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts[name].append(e0.elapsed_time(e1) * 1e3)
+    if sa.sa_device_status() != 0:
+        raise RuntimeError("device status word set during the token-level leg")
+    us = {name: round(float(np.median(v)), 2) for name, v in ts.items()}
+    mass_bytes = B * Hkv * L * d * 2 + 2 * B * Hkv * R * L * 4 + B * L * 4
+    sel = int(cnt.sum().item())
+    dec_bytes = sel * Hkv * d * 2 * 2
+    ach = mass_bytes / (us["token_mass"] * 1e-6) / 1e9
+    return {
+        "workload": "token-level head-collapsed decode: B=%d T=%d Hq=%d Hkv=%d d=%d L=%d, top-%d tokens + sink + "
+                    "newest, shared by the kv heads (bf16)" % (B, T, Hq, Hkv, d, L, wl.k),
+        "kernels_us": us,
+        "step_us": round(sum(us.values()), 2),
+        "token_mass_roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                                "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                                "bytes": mass_bytes,
+                                "bytes_note": "K read once + base-2 logits written and read back + mass written"},
+        "decode_tokens": {"tokens_per_row": sel // B, "bytes": dec_bytes,
+                          "GB_s": round(dec_bytes / (us["decode_tokens"] * 1e-6) / 1e9, 1)},
+        "l2": "flushed before every timed call (256 MB write, untimed)",
+    }
+
+
 def _kernel_hash():
     import hashlib
     h = hashlib.sha256()
@@ -654,6 +724,9 @@ def main():
                     help="decode across context lengths with the length-aware budget (separate report)")
     ap.add_argument("--prefill-B", type=int, default=0, help="override the prefill legs' batch (profiling)")
     ap.add_argument("--prefill-L", type=int, default=0, help="override the prefill legs' context (profiling)")
+    ap.add_argument("--tokens-reps", type=int, default=5,
+                    help="timed reps of the token-level decode leg (0 skips it)")
+    ap.add_argument("--tokens-only", action="store_true", help="run only the token-level decode leg")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -681,6 +754,11 @@ def main():
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
             res = bench_length_sweep([16384, 32768, 65536, 131072, 262144], 80, 262144, 0.5)
+        elif args.tokens_only:
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            peaks, src = load_peaks()
+            res = {"tokens": bench_tokens(max(1, args.tokens_reps), peaks, src)}
         elif args.prefill_only:
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
@@ -692,6 +770,9 @@ def main():
                 peaks, src = load_peaks()
                 res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src) for n in ("c5", "c4")]
                 res["gpu_launches"] += 4 * args.prefill_steps * 2
+            if args.tokens_reps > 0 and res is not None:
+                peaks, src = load_peaks()
+                res["tokens"] = bench_tokens(args.tokens_reps, peaks, src)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

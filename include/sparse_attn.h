@@ -139,8 +139,10 @@ sa_status_t sa_append_kv(const void* k_new, const void* v_new, int dtype, int B,
  *   ([B, Hkv, nq, nb]; non-causal entries are -inf); the tile scores are
  *   computed on the tensor cores (q bf16 times the fp32 sketch split into
  *   three bf16 parts, fp32 accumulation), then each tile's top-k is taken.
- * mode SA_SELECT_MASS: `scores` is an input (e.g. from sa_oracle_mass);
- *   q and sketch are not read.
+ * mode SA_SELECT_MASS: `scores` is an input (e.g. from sa_oracle_mass or,
+ *   with block == 1 and Hkv == 1, from sa_token_mass_decode); q and sketch
+ *   are not read.  Decode score arrays longer than 16384 entries are read
+ *   from global memory (one CTA per unit); prefill ones are limited to 16384.
  * idx: [B, Hkv, nq, kmax] int32 written (ascending, -1 padded), cnt:
  *   [B, Hkv, nq] int32 written.  kmax must be >= sa_select_kmax(...).
  * Requires d in {64, 128}; G * Tq <= 32 and (bf16) a 16-byte-aligned q for
@@ -261,6 +263,46 @@ size_t sa_oracle_mass_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int 
 sa_status_t sa_oracle_mass(const void* q, const void* k, int dtype, int B, int L, int Hq, int Hkv,
                            int d, int qtile, int block, float scale, float* mass, void* workspace,
                            size_t ws_bytes, void* stream);
+
+/*
+ * Head-collapsed token importance for decode ("How Much Dense Attention is
+ * Necessary?" Sec. 2.1: the dense attention distribution of each query,
+ * averaged over the query heads; Sec. 2.2: one distribution shared by all
+ * heads).  The T decode queries of a batch row share one support, so they
+ * are averaged too:
+ *   mass[b, j] = 1/(Hq*T) * sum over heads h and queries t of P_{b,t,h}(j),
+ * P_{b,t,h} the dense softmax of scale * q[b,t,h] . k[b, h/G, :] over the
+ * causal keys j <= L - T + t (0 for the others); each row of mass sums to 1.
+ * q: [B, T, Hq, d]; k_cache: [B, Hkv, L_stride, d]; mass: [B, L] float32
+ * written.  workspace: >= sa_token_mass_workspace_bytes(...) bytes of device
+ * memory (base-2 logits [B*Hkv, G*T, L] float32 and per-row partials).
+ * Requires dtype SA_BF16, d in {64, 128}, G*T <= 16, T <= L, 16-byte-aligned
+ * q, k_cache, mass and workspace.  Select tokens from it with sa_select_topk
+ * (mode SA_SELECT_MASS, Hkv 1, block 1) and attend with sa_decode_tokens.
+ */
+size_t sa_token_mass_workspace_bytes(int B, int T, int Hq, int Hkv, int L);
+sa_status_t sa_token_mass_decode(const void* q, const void* k_cache, int dtype, int B, int T, int Hq,
+                                 int Hkv, int d, int L, int L_stride, float scale, float* mass,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * a4 at token granularity, shared across the kv heads ("How Much Dense
+ * Attention is Necessary?" Sec. 2.1: recompute exactly on the selected
+ * support; Sec. 2.2: one head-collapsed support for every head).  For query
+ * row (b, t, h):
+ *   out[b,t,h] = sum_j softmax_j(scale * q[b,t,h] . k[b,h/G,j]) v[b,h/G,j]
+ * over the distinct tokens j in idx[b, 0:cnt[b]] with j < L and
+ * j <= L - T + t (entries out of range are ignored; order is free).
+ * idx: [B, kmax] int32, cnt: [B] int32 (e.g. from sa_select_topk in MASS
+ * mode with block 1).  workspace: >= sa_decode_workspace_bytes(B, T, Hq,
+ * Hkv, d, kmax), zero-filled before first use, as for sa_decode.  Requires
+ * dtype SA_BF16, d in {64, 128}, G*T <= 16, T <= L, 16-byte-aligned q and
+ * caches.
+ */
+sa_status_t sa_decode_tokens(const void* q, const void* k_cache, const void* v_cache, int dtype,
+                             const int32_t* idx, const int32_t* cnt, int kmax, int B, int T, int Hq,
+                             int Hkv, int d, int L, int L_stride, float scale, void* out,
+                             void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * One decode step: a1 append (k_new, v_new at cache rows L-T..L-1, sketch

@@ -137,6 +137,27 @@ def test_invalid_arguments_rejected_on_host(sa):
     st = L.sa_select_topdelta(16, sa.SA_BF16, 16, None, 8, 1, 32, 8, 128, 32768, 32768, 64, 0.5, -2, 0.088, 16, 16,
                               34, None)
     assert st == sa.SA_ERR_INVALID_ARG
+    # token mass: fp32 unsupported, G*T > 16 unsupported, a short workspace rejected
+    st = L.sa_token_mass_decode(16, 16, sa.SA_F32, 1, 1, 8, 2, 128, 64, 64, 0.1, 16, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_UNSUPPORTED
+    st = L.sa_token_mass_decode(16, 16, sa.SA_BF16, 1, 4, 32, 4, 128, 64, 64, 0.1, 16, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_UNSUPPORTED and b"G*T" in L.sa_last_error()
+    st = L.sa_token_mass_decode(16, 16, sa.SA_BF16, 1, 1, 8, 2, 128, 64, 64, 0.1, 16, 16, 64, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"workspace" in L.sa_last_error()
+    st = L.sa_token_mass_decode(16, 16, sa.SA_BF16, 1, 8, 8, 8, 128, 4, 64, 0.1, 16, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_INVALID_ARG  # T > L
+    # token decode: bf16 only, null pointers rejected
+    st = L.sa_decode_tokens(16, 16, 16, sa.SA_F32, 16, 16, 8, 1, 1, 8, 2, 128, 64, 64, 0.1, 16, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_UNSUPPORTED
+    st = L.sa_decode_tokens(16, None, 16, sa.SA_BF16, 16, 16, 8, 1, 1, 8, 2, 128, 64, 64, 0.1, 16, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_INVALID_ARG
+    # given decode scores may be longer than the shared-memory limit; given prefill scores may not
+    st = L.sa_select_topk(sa.SA_SELECT_MASS, None, sa.SA_BF16, None, None, 1, 1, 1, 1, 128, 262144, 262144, 1, 0, 0,
+                          2048, 0, 1, 1.0, 16, 16, 2050, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"scores" in L.sa_last_error()  # only the missing array is wrong
+    st = L.sa_select_topk(sa.SA_SELECT_MASS, None, sa.SA_BF16, None, 16, 1, 262144, 1, 1, 128, 262144, 262144, 1, 128,
+                          1, 8, 0, 1, 1.0, 16, 16, 2050, None)
+    assert st == sa.SA_ERR_UNSUPPORTED
     # device status needs an output pointer
     assert L.sa_device_status(None, 0) == sa.SA_ERR_INVALID_ARG
 

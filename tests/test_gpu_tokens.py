@@ -1,0 +1,170 @@
+"""GPU parity of the head-collapsed token-level decode path against the CPU oracle:
+token mass (dense distribution averaged over all heads and decode queries), token
+top-k (given-score selection, including arrays longer than shared memory holds) and
+attention over the selected tokens shared by every kv head."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import assert_close, assert_selection, dev, host
+
+pytestmark = pytest.mark.gpu
+
+# mass: |gpu - oracle| <= MASS_RTOL * oracle + MASS_ATOL.  The GPU logits carry
+# fp32 rounding (about 1e-6 of |logit|, logits up to ~20 in base 2), which exp2
+# turns into a relative error of about 2e-5 of the probability.
+MASS_RTOL = 1e-4
+MASS_ATOL = 1e-9
+
+
+@pytest.fixture(scope="module")
+def sa():
+    import top_block_sparse_pooled_b300 as m
+    return m
+
+
+def _check_status(sa):
+    assert sa.sa_device_status(clear=True) == 0
+
+
+TOKEN_CASES = {
+    # GQA decode with four queries (G*T = 16), odd L (scalar logit stores)
+    "g4t4_odd": synth.WORKLOADS["c3"].replace(L=8192 + 5, k=256, needles=6, seed=91),
+    # d = 64, two batch rows, one query
+    "d64_b2": synth.WORKLOADS["c2"].replace(B=2, Hq=8, Hkv=4, d=64, L=3000, k=100, needles=3, seed=92),
+    # longer than the shared-memory top-k (scores read from L2), G*T = 16 with G = 8
+    "long_g8": synth.WORKLOADS["c3"].replace(T=2, Hq=16, Hkv=2, L=20000, k=512, needles=8, seed=93),
+}
+
+
+def _token_mass(sa, wl, x):
+    q, k = dev(x.q), dev(x.k)
+    ws = torch.empty(sa.sa_token_mass_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.L), dtype=torch.uint8,
+                     device="cuda")
+    mass = torch.empty((wl.B, wl.L), dtype=torch.float32, device="cuda")
+    sa.sa_token_mass_decode(q, k, wl.L, wl.scale, mass, ws)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    return mass
+
+
+def _token_select(sa, wl, mass, k):
+    kmax = sa.sa_select_kmax(wl.L, 1, 0, False, k)
+    idx = torch.full((wl.B, 1, 1, kmax), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((wl.B, 1, 1), dtype=torch.int32, device="cuda")
+    sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, mass.reshape(wl.B, 1, 1, wl.L), 1, wl.L, wl.L, 1, 0, False, k,
+                      0, 1, 1.0, idx, cnt, d=wl.d, dtype=sa.SA_F32, B=wl.B, Tq=1, Hq=1)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    return idx.reshape(wl.B, kmax), cnt.reshape(wl.B)
+
+
+def _token_decode(sa, wl, x, idx, cnt):
+    q, k, v = dev(x.q), dev(x.k), dev(x.v)
+    kmax = idx.shape[-1]
+    ws = torch.zeros(sa.sa_decode_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, kmax), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.full_like(q, float("nan"))
+    sa.sa_decode_tokens(q, k, v, idx, cnt, wl.L, wl.scale, out, ws)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    return out
+
+
+def _rows(wl):
+    return [(b, t, h) for b in range(wl.B) for t in range(wl.T) for h in range(wl.Hq)]
+
+
+@pytest.mark.parametrize("name", sorted(TOKEN_CASES))
+def test_token_mass_matches_oracle(sa, name):
+    wl = TOKEN_CASES[name]
+    x = synth.make_inputs(wl)
+    got = host(_token_mass(sa, wl, x))
+    ref = oracle.token_mass_decode(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    assert_close(got, ref, atol=MASS_ATOL, rtol=MASS_RTOL, what="token mass")
+    assert np.all(np.abs(got.sum(axis=1) - 1.0) < 1e-4)
+
+
+@pytest.mark.parametrize("name", sorted(TOKEN_CASES))
+def test_token_select_matches_oracle(sa, name):
+    wl = TOKEN_CASES[name]
+    x = synth.make_inputs(wl)
+    mass = _token_mass(sa, wl, x)
+    idx, cnt = _token_select(sa, wl, mass, wl.k)
+    P = oracle.token_mass_decode(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    o_idx, o_cnt = oracle.token_select(P, wl.k, kmax=idx.shape[-1])
+    assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, P, what=name)
+
+
+@pytest.mark.parametrize("n", [3, 16384, 16385, 40000, 262144])
+def test_long_given_selection_exact(sa, n):
+    """Given float32 scores with many exact ties: the GPU selection equals the oracle's, bit for bit."""
+    r = np.random.default_rng(n)
+    B = 3
+    s = (r.integers(-40, 41, size=(B, n)) * 0.25).astype(np.float32)
+    s[2] = 1.5  # all equal: the lowest indices win
+    for k in (0, 1, 37, 2048, n):
+        kmax = max(1, min(k, max(n - 2, 0)) + 2)
+        idx = torch.full((B, 1, 1, kmax), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.zeros((B, 1, 1), dtype=torch.int32, device="cuda")
+        sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, torch.from_numpy(s).cuda().reshape(B, 1, 1, n), 1, n, n, 1,
+                          0, False, k, 0, 1, 1.0, idx, cnt, d=128, dtype=sa.SA_F32, B=B, Tq=1, Hq=1)
+        torch.cuda.synchronize()
+        _check_status(sa)
+        o_idx, o_cnt = oracle.select(s.astype(np.float64), n, n - 1, k, kmax)
+        g_idx, g_cnt = idx.cpu().numpy().reshape(B, kmax), cnt.cpu().numpy().reshape(B)
+        assert np.array_equal(g_cnt, o_cnt), (k, g_cnt, o_cnt)
+        assert np.array_equal(g_idx, o_idx), k
+
+
+@pytest.mark.parametrize("name", sorted(TOKEN_CASES))
+def test_token_decode_matches_oracle(sa, name):
+    wl = TOKEN_CASES[name]
+    x = synth.make_inputs(wl)
+    P = oracle.token_mass_decode(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    o_idx, o_cnt = oracle.token_select(P, wl.k)
+    out = _token_decode(sa, wl, x, torch.from_numpy(o_idx).cuda(), torch.from_numpy(o_cnt).cuda())
+    rows = _rows(wl)
+    ref, _ = oracle.token_attend(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, o_idx, o_cnt, rows)
+    got = host(out).reshape(-1, wl.d)
+    assert_close(got, ref, what="token decode " + name)
+
+
+def test_token_decode_short_and_out_of_range_lists(sa):
+    """Counts below kmax, a partial last chunk, entries at or past L, and a single token."""
+    wl = TOKEN_CASES["d64_b2"]
+    x = synth.make_inputs(wl)
+    r = np.random.default_rng(5)
+    kmax = 150
+    idx = np.full((wl.B, kmax), -1, dtype=np.int32)
+    cnt = np.array([1, 97], dtype=np.int32)
+    idx[0, 0] = wl.L - 1
+    sel = np.sort(r.choice(wl.L, size=96, replace=False)).astype(np.int32)
+    idx[1, :96] = sel
+    idx[1, 96] = wl.L + 5  # past the cache: ignored
+    out = _token_decode(sa, wl, x, torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda())
+    o_idx = idx.copy()
+    o_cnt = cnt.copy()
+    o_cnt[1] = 96  # the oracle is given only the in-range entries
+    ref, _ = oracle.token_attend(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, o_idx, o_cnt, _rows(wl))
+    assert_close(host(out).reshape(-1, wl.d), ref, what="short token lists")
+
+
+def test_token_pipeline_full_size(sa):
+    """One sequence of 256K tokens, 32 query heads on 8 kv heads, four decode queries, 2048 selected
+    tokens: token mass everywhere, the selection (near-tie rule) and the outputs over the GPU's own
+    selection."""
+    wl = synth.WORKLOADS["c3"].replace(k=2048)
+    x = synth.make_inputs(wl)
+    mass = _token_mass(sa, wl, x)
+    idx, cnt = _token_select(sa, wl, mass, wl.k)
+    P = oracle.token_mass_decode(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    assert_close(host(mass), P, atol=MASS_ATOL, rtol=MASS_RTOL, what="token mass (full size)")
+    o_idx, o_cnt = oracle.token_select(P, wl.k, kmax=idx.shape[-1])
+    g_idx, g_cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    assert_selection(g_idx, g_cnt, o_idx, o_cnt, P, what="full size")
+    out = _token_decode(sa, wl, x, idx, cnt)
+    ref, _ = oracle.token_attend(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, g_idx, g_cnt, _rows(wl))
+    assert_close(host(out).reshape(-1, wl.d), ref, what="token decode (full size)")

@@ -58,6 +58,10 @@ SIGNATURES = {
     "sa_prefill": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp], _i),
     "sa_oracle_mass_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "sa_oracle_mass": ([_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "sa_token_mass_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "sa_token_mass_decode": ([_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "sa_decode_tokens": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp],
+                         _i),
     "sa_decode_step_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "sa_decode_step": ([_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _i,
                         _vp, _vp, _i, _vp, _sz, _vp], _i),
@@ -199,6 +203,28 @@ def sa_oracle_mass(q, k, qtile, block, scale, mass, workspace, stream=None):
     nbytes = workspace.numel() if workspace is not None else 0
     _check(lib.sa_oracle_mass(_ptr(q), _ptr(k), _dtype(q), B, L, Hq, Hkv, d, qtile, block, float(scale), _ptr(mass),
                               ws, nbytes, _stream(stream)))
+
+
+def sa_token_mass_workspace_bytes(B, T, Hq, Hkv, L) -> int:
+    return lib.sa_token_mass_workspace_bytes(B, T, Hq, Hkv, L)
+
+
+def sa_token_mass_decode(q, k_cache, L, scale, mass, workspace, stream=None):
+    """q: [B, T, Hq, d]; k_cache: [B, Hkv, L_stride, d]; mass: [B, L] float32 (written)."""
+    B, T, Hq, d = q.shape
+    Hkv, Ls = k_cache.shape[1], k_cache.shape[2]
+    _check(lib.sa_token_mass_decode(_ptr(q), _ptr(k_cache), _dtype(q), B, T, Hq, Hkv, d, L, Ls, float(scale),
+                                    _ptr(mass), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def sa_decode_tokens(q, k_cache, v_cache, idx, cnt, L, scale, out, workspace, stream=None):
+    """q, out: [B, T, Hq, d]; caches [B, Hkv, L_stride, d]; idx [B, kmax] tokens shared by the kv heads; cnt [B]."""
+    B, T, Hq, d = q.shape
+    Hkv, Ls = k_cache.shape[1], k_cache.shape[2]
+    kmax = idx.shape[-1]
+    _check(lib.sa_decode_tokens(_ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(q), _ptr(idx), _ptr(cnt), kmax, B, T,
+                                Hq, Hkv, d, L, Ls, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                _stream(stream)))
 
 
 def sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax) -> int:

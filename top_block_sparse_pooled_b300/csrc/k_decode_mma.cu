@@ -25,6 +25,15 @@
 // accumulate) with ldmatrix straight from the swizzled tiles; P stays in
 // registers (the QK accumulator fragment is the PV A fragment).  At the end of
 // a group's range the four warp states merge through shared memory.
+//
+// Token mode (kTok): the support is a list of single tokens per batch row,
+// shared by every kv head of that row ("How Much Dense Attention is
+// Necessary?" Sec. 2.2: one head-collapsed distribution selects the tokens
+// for all heads).  A unit is (group, chunk of 64 selected tokens); the
+// producer warp gathers the chunk's K and V rows with one 1-D bulk copy per
+// row into rows padded to 2*D + 16 bytes (ldmatrix stays conflict-free) and
+// records each row's key position for the causal mask; rows past the count
+// repeat the sink token with a position that no query sees.
 #pragma once
 
 #include "sa_ptx.cuh"
@@ -50,11 +59,16 @@ struct DmCfg {
   static constexpr int NT = D / 8;
 };
 
-// Shared-memory layout (runtime, from a 1024-aligned base).
+// Shared-memory layout (runtime, from a 1024-aligned base).  Block mode: each
+// stage is a K and a V tile of 64 swizzled 2*D-byte rows.  Token mode: rows
+// padded to 2*D + 16 bytes, then one int key position per row and stage.
 struct DmLayout {
-  int nstages, R, D, per;
-  __host__ __device__ int stage_off(int s) const { return s * 2 * kDmBk * D * 2; }
-  __host__ __device__ int merge_off() const { return nstages * 2 * kDmBk * D * 2; }
+  int nstages, R, D, per, tok;
+  __host__ __device__ int rowb() const { return tok ? D * 2 + 16 : D * 2; }
+  __host__ __device__ int stage_bytes() const { return 2 * kDmBk * rowb(); }
+  __host__ __device__ int stage_off(int s) const { return s * stage_bytes(); }
+  __host__ __device__ int pos_off() const { return nstages * stage_bytes(); }
+  __host__ __device__ int merge_off() const { return pos_off() + (tok ? nstages * kDmBk * 4 : 0); }
   __host__ __device__ int merge_bytes() const {
     const int warps = kDmConsumers * R * (D + 2) * 4;  // per-warp states
     const int parts = (8 + 2 * kDmMaxParts) * R * 4;  // mw, lw, then staged partial maxima / denominators
@@ -98,9 +112,11 @@ __device__ __forceinline__ uint32_t swz_chunk(uint32_t tile, int row, int chunk)
 
 struct DmParams {
   const __nv_bfloat16* q;
+  const __nv_bfloat16* kc;  // token mode: the caches, gathered row by row
+  const __nv_bfloat16* vc;
   const int32_t* idx;
   const int32_t* cnt;
-  int kmax, T, Hq, Hkv, L, Ls, R;
+  int kmax, upg, T, Hq, Hkv, L, Ls, R;  // upg: units per group (kmax blocks, or chunks of 64 tokens)
   float qscale;
   int per, U;
   float* part_o;   // [slots][R][D] (unnormalized numerators)
@@ -111,7 +127,16 @@ struct DmParams {
   DmLayout lay;
 };
 
-template <int D>
+__device__ __forceinline__ void dm_sts_s32(uint32_t a, int v) {
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ int dm_lds_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+template <int D, bool kTok>
 __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap vmap,
                                                                    const DmParams p) {
@@ -145,19 +170,71 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     fence_mbar_init();
   }
   pdl_wait();  // idx / cnt come from the selection kernel
-  // unit list: (group, block id or -1 when the unit is past the group's count);
-  // the count and the id are loaded together (the id slot is always in bounds)
+  // unit list: (group, block id -- token mode: chunk -- or -1 when the unit is
+  // past the count); the count and the id are loaded together (the id slot is
+  // always in bounds)
   for (int i = tid; i < nu; i += kDmThreads) {
     const int u = u0 + i;
-    const int g = u / p.kmax, s = u % p.kmax;
-    const int n = p.cnt[g];
-    int blk = p.idx[static_cast<size_t>(g) * p.kmax + s];
-    if (s >= min(n, p.kmax) || blk < 0 || blk * kDmBk >= p.L) blk = -1;
-    list[i] = make_int2(g, blk);
+    const int g = u / p.upg, s = u % p.upg;
+    if constexpr (kTok) {
+      const int n = min(p.cnt[g / p.Hkv], p.kmax);
+      list[i] = make_int2(g, s * kDmBk < n ? s : -1);
+    } else {
+      const int n = p.cnt[g];
+      int blk = p.idx[static_cast<size_t>(g) * p.kmax + s];
+      if (s >= min(n, p.kmax) || blk < 0 || blk * kDmBk >= p.L) blk = -1;
+      list[i] = make_int2(g, blk);
+    }
   }
   __syncthreads();
 
-  if (warp == kDmConsumers) {
+  if (kTok && warp == kDmConsumers) {
+    // ------------------------------------------------ producer, token gather (whole warp)
+    int vi = 0;
+    bool ok = true;
+    for (int i = 0; i < nu && ok; ++i) {
+      const int2 e = list[i];
+      if (e.y < 0) continue;
+      const int st = vi % NS;
+      if (vi >= NS) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((vi / NS) - 1) & 1);
+        ok = __shfl_sync(0xFFFFFFFFu, w ? 1 : 0, 0) != 0;
+      }
+      if (!ok) break;
+      const uint32_t full = full0 + 8 * st;
+      const int b = e.x / p.Hkv;
+      const int n = min(p.cnt[b], p.kmax);
+      const int32_t* sel = p.idx + static_cast<size_t>(b) * p.kmax;
+      const uint32_t kt = sbase + lay.stage_off(st), vt = kt + kDmBk * lay.rowb();
+      const uint32_t pos = sbase + lay.pos_off() + st * kDmBk * 4;
+      const __nv_bfloat16* kg = p.kc + static_cast<size_t>(e.x) * p.Ls * D;
+      const __nv_bfloat16* vg = p.vc + static_cast<size_t>(e.x) * p.Ls * D;
+      int tk[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = lane + 32 * h, s = e.y * kDmBk + row;
+        const int t = s < n ? sel[s] : -1;
+        const bool valid = t >= 0 && t < p.L;
+        dm_sts_s32(pos + 4 * row, valid ? t : 0x7FFFFFFF);
+        tk[h] = valid ? t : 0;  // filler rows repeat token 0 (finite values, never visible)
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(2 * kDmBk * D * 2));
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = lane + 32 * h;
+        bulk_g2s(kt + row * lay.rowb(), kg + static_cast<size_t>(tk[h]) * D, D * 2, full);
+        bulk_g2s(vt + row * lay.rowb(), vg + static_cast<size_t>(tk[h]) * D, D * 2, full);
+      }
+      ++vi;
+    }
+    if (lane == 0)
+      for (int k = max(0, vi - NS); k < vi; ++k) mbar_wait_drain(full0 + 8 * (k % NS), (k / NS) & 1);
+    return;
+  }
+  if (!kTok && warp == kDmConsumers) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int vi = 0;
@@ -275,8 +352,8 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     // loads from L2.
     __threadfence();
     asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
-    const int cf = (g * p.kmax) / p.per;
-    const int cl = min(p.nctas - 1, ((g + 1) * p.kmax - 1) / p.per);
+    const int cf = (g * p.upg) / p.per;
+    const int cl = min(p.nctas - 1, ((g + 1) * p.upg - 1) / p.per);
     const int np = cl - cf + 1;
     if (tid == 0) {
       const int old = atomicAdd(p.ctr + g, 1);
@@ -376,7 +453,12 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     ++vi;
     if (dead) continue;
     const uint32_t kt = sbase + lay.stage_off(st);
-    const uint32_t vt = kt + C::TILEB;
+    const uint32_t vt = kt + kDmBk * lay.rowb();
+    // 16-byte chunk `chunk` of row `row` of a staged K or V tile
+    auto chunk_addr = [&](uint32_t tile, int row, int chunk) -> uint32_t {
+      if constexpr (kTok) return tile + row * (D * 2 + 16) + chunk * 16;
+      else return swz_chunk(tile, row, chunk);
+    };
 
     // S = Q K^T for this warp's 16 keys (two n-tiles of 8)
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -386,7 +468,7 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
 #pragma unroll
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
         uint32_t b00, b01, b10, b11;
-        ldsm_x4(swz_chunk(kt, key, 2 * kk + (mi & 1)), b00, b01, b10, b11);
+        ldsm_x4(chunk_addr(kt, key, 2 * kk + (mi & 1)), b00, b01, b10, b11);
         mma_bf16(s[0], qa[kk], b00, b01);
         mma_bf16(s[1], qa[kk], b10, b11);
       }
@@ -394,11 +476,14 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     __syncwarp();
     // scale, causal / validity mask, online softmax (base 2)
     const int base = e.y * kDmBk + kb + 2 * tq;
+    const uint32_t posw = sbase + lay.pos_off() + (st * kDmBk + kb + 2 * tq) * 4;  // token mode
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const int key = base + nt * 8 + (x & 1);
+        int key;
+        if constexpr (kTok) key = dm_lds_s32(posw + (nt * 8 + (x & 1)) * 4);
+        else key = base + nt * 8 + (x & 1);
         const int lim = (x < 2) ? lim0 : lim1;
         s[nt][x] = (key <= lim) ? s[nt][x] * p.qscale : -INFINITY;
       }
@@ -442,7 +527,7 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
 #pragma unroll
       for (int jj = 0; jj < C::NT / 2; ++jj) {
         uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(swz_chunk(vt, key, 2 * jj + (mi >> 1)), v0, v1, v2, v3);
+        ldsm_x4_t(chunk_addr(vt, key, 2 * jj + (mi >> 1)), v0, v1, v2, v3);
         mma_bf16(o[2 * jj], pa, v0, v1);
         mma_bf16(o[2 * jj + 1], pa, v2, v3);
       }

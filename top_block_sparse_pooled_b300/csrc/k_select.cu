@@ -71,11 +71,12 @@ __device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
-// Select from scores at shared address sc (n floats, n <= kTopkMaxN): the forced
+// Select from scores score(0..n-1): the forced
 // blocks are the first and the last (0 and n-1, one block when n == 1); the
 // candidates are 1..n-2; keep min(budget, n-2) of them with the highest scores,
 // ties to the lower index.  Writes idx_out[0:kmax] (ascending, -1 padded) and
 // *cnt_out.  S: shared address of a TopkShared.  All kSelThreads threads call;
+// every score is read six times (four digit passes, two output passes);
 // six block barriers in all.
 //
 // Threshold: exact MSB-first radix select of the take-th largest order-preserving
@@ -85,8 +86,9 @@ __device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
 // ties, and after one barrier writes its selections at their ascending
 // positions; ties at the threshold are admitted in index order until the budget
 // is met.
-__device__ __forceinline__ void block_topk(uint32_t sc, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
-                                           int32_t* __restrict__ cnt_out, uint32_t S) {
+template <typename LoadF>
+__device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
+                                                int32_t* __restrict__ cnt_out, uint32_t S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t hist = S + static_cast<uint32_t>(offsetof(TopkShared, hist));
   const uint32_t wdef = S + static_cast<uint32_t>(offsetof(TopkShared, wdef));
@@ -105,7 +107,7 @@ __device__ __forceinline__ void block_topk(uint32_t sc, int n, int budget, int k
       const int shift = 24 - 8 * p;
       const uint32_t hp = hist + 1024u * p;
       for (int b = 1 + tid; b < last; b += kSelThreads) {
-        const uint32_t key = float_key(lds_f32(sc + 4u * b));
+        const uint32_t key = float_key(score(b));
         if ((key & mask) == prefix) red_add_shared(hp + 4u * ((key >> shift) & 255u), 1u);
       }
       __syncthreads();
@@ -154,7 +156,7 @@ __device__ __forceinline__ void block_topk(uint32_t sc, int n, int budget, int k
       if (!by_key) {
         def = true;
       } else {
-        const uint32_t key = float_key(lds_f32(sc + 4u * b));
+        const uint32_t key = float_key(score(b));
         def = key > thr;
         eq = key == thr;
       }
@@ -202,6 +204,13 @@ __device__ __forceinline__ void block_topk(uint32_t sc, int n, int budget, int k
   }
   for (int i = static_cast<int>(total) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
   if (tid == 0) *cnt_out = static_cast<int32_t>(total);
+}
+
+// scores at shared address sc
+__device__ __forceinline__ void block_topk(uint32_t sc, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
+                                           int32_t* __restrict__ cnt_out, uint32_t S) {
+  block_topk_impl([&](int b) { return lds_f32(sc + 4u * static_cast<uint32_t>(b)); }, n, budget, kmax, idx_out,
+                  cnt_out, S);
 }
 
 // --------------------------------------------------------------------------
@@ -520,6 +529,19 @@ __global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* 
   for (int bb = threadIdx.x; bb < nvalid; bb += kSelThreads) sts_f32(sc + 4u * bb, scores[u * nb + bb]);
   __syncthreads();
   block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, topk_s);
+}
+
+// Selection from a given score array too large for shared memory (one-token
+// blocks over a long context): the same selection, with every score read from
+// global memory (L2) in each pass.  grid (nq, groups), kSelThreads.
+__global__ void __launch_bounds__(kSelThreads, 1) select_given_global_kernel(const float* __restrict__ scores, int nb,
+                                                                          int k, int32_t* __restrict__ idx,
+                                                                          int32_t* __restrict__ cnt, int kmax) {
+  extern __shared__ __align__(16) uint8_t smem_sel_global[];
+  const size_t u = static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+  const float* sc = scores + u * nb;
+  block_topk_impl([&](int b) { return __ldg(sc + b); }, nb, k, kmax, idx + u * kmax, cnt + u,
+                  smem_u32(smem_sel_global));
 }
 
 }  // namespace sa

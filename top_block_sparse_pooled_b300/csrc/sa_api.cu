@@ -36,6 +36,7 @@
 #include "k_select.cu"
 #include "k_score.cu"
 #include "k_sketch.cu"
+#include "k_tokmass.cu"
 
 namespace {
 
@@ -332,6 +333,13 @@ sa_status_t run_select(const SelectArgs& a, cudaStream_t st) {
   const int nb = cdiv(a.L, a.block);
   if (a.mode == SA_SELECT_MASS) {
     const int nq = a.prefill ? cdiv(a.L, a.qtile) : 1;
+    if (nb > sa::kTopkMaxN) {  // decode only (validated): scores stay in global memory
+      const int gsmem = static_cast<int>(sizeof(sa::TopkShared));
+      sa::select_given_global_kernel<<<dim3(1, groups), sa::kSelThreads, gsmem, st>>>(a.scores, nb, a.k, a.idx,
+                                                                                       a.cnt, a.kmax);
+      SA_CUDA(cudaGetLastError());
+      return SA_OK;
+    }
     const int smem = static_cast<int>(((sizeof(sa::TopkShared) + 15) / 16) * 16) + nb * 4;
     SA_TRY(set_smem(sa::select_given_kernel, smem));
     sa::select_given_kernel<<<dim3(nq, groups), sa::kSelThreads, smem, st>>>(
@@ -390,6 +398,7 @@ struct DecodeArgs {
   void* out;
   void* ws;
   size_t ws_bytes;
+  int tok = 0;  // token mode: idx [B, kmax] single tokens shared by the kv heads of a batch row
 };
 
 size_t decode_ws_bytes(int groups, int R, int d, int kmax) {
@@ -404,33 +413,37 @@ size_t decode_ws_bytes(int groups, int R, int d, int kmax) {
   return v1 > v2 ? v1 : v2;
 }
 
-template <int D>
+template <int D, bool kTok>
 sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream_t st) {
-  using Cfg = sa::DmCfg<D>;
   const int groups = a.B * a.Hkv;
   const int R = (a.Hq / a.Hkv) * a.T;
-  const long long U = static_cast<long long>(groups) * a.kmax;
+  const int upg = kTok ? cdiv(a.kmax, sa::kDmBk) : a.kmax;  // units per group
+  const long long U = static_cast<long long>(groups) * upg;
   SA_ARG(U < (1LL << 31), "too many (group, block) units");
   // two CTAs per SM; equal contiguous ranges of units
   const long long target = static_cast<long long>(SA_DM_WAVES) * SA_DM_CTAS_PER_SM * di.sms;
   long long per = (U + target - 1) / target;
-  per = std::max<long long>(per, (a.kmax + sa::kDmMaxParts - 2) / (sa::kDmMaxParts - 1));  // <= 64 partials per group
+  per = std::max<long long>(per, (upg + sa::kDmMaxParts - 2) / (sa::kDmMaxParts - 1));  // <= 64 partials per group
   per = std::min<long long>(std::max<long long>(per, 1), sa::kDmMaxList);
   const int nctas = static_cast<int>((U + per - 1) / per);
-  sa::DmLayout lay{2, R, D, static_cast<int>(per)};
+  sa::DmLayout lay{2, R, D, static_cast<int>(per), kTok ? 1 : 0};
   const int budget = (227 * 1024) / SA_DM_CTAS_PER_SM - 1024;  // the CTAs of one SM share its shared memory
-  const int fixed = lay.bytes() - 2 * Cfg::STAGEB;
-  lay.nstages = std::max(2, std::min(SA_DM_MAXSTAGES, (budget - fixed) / Cfg::STAGEB));
+  const int per_stage = lay.stage_bytes() + (kTok ? sa::kDmBk * 4 : 0);
+  const int fixed = lay.bytes() - 2 * per_stage;
+  lay.nstages = std::max(2, std::min(SA_DM_MAXSTAGES, (budget - fixed) / per_stage));
   const int smem = lay.bytes();
-  auto kern = sa::decode_mma_kernel<D>;
+  auto kern = sa::decode_mma_kernel<D, kTok>;
   SA_TRY(set_smem(kern, smem));
   const size_t slots = static_cast<size_t>(nctas) + groups;
   auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
   sa::DmParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.kc = static_cast<const __nv_bfloat16*>(a.kc);
+  p.vc = static_cast<const __nv_bfloat16*>(a.vc);
   p.idx = a.idx;
   p.cnt = a.cnt;
   p.kmax = a.kmax;
+  p.upg = upg;
   p.T = a.T;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -504,8 +517,9 @@ sa_status_t dispatch_decode_r(const DecodeArgs& a, const DevInfo& di, cudaStream
 sa_status_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   DevInfo di;
   SA_TRY(dev_info(&di));
+  if (a.tok) return a.d == 128 ? launch_decode_mma<128, true>(a, di, st) : launch_decode_mma<64, true>(a, di, st);
   if (a.dtype == SA_BF16 && (a.Hq / a.Hkv) * a.T <= 16)
-    return a.d == 128 ? launch_decode_mma<128>(a, di, st) : launch_decode_mma<64>(a, di, st);
+    return a.d == 128 ? launch_decode_mma<128, false>(a, di, st) : launch_decode_mma<64, false>(a, di, st);
   if (a.dtype == SA_F32)
     return a.d == 128 ? dispatch_decode_r<float, 128>(a, di, st) : dispatch_decode_r<float, 64>(a, di, st);
   return a.d == 128 ? dispatch_decode_r<__nv_bfloat16, 128>(a, di, st) : dispatch_decode_r<__nv_bfloat16, 64>(a, di, st);
@@ -526,9 +540,15 @@ sa_status_t validate_decode(const DecodeArgs& a) {
   SA_ARG(a.q && a.kc && a.vc && a.idx && a.cnt && a.out, "null pointer argument");
   SA_ARG(a.T >= 1, "T must be >= 1");
   SA_ARG(a.L >= 1 && a.L <= a.Ls, "need 1 <= L (%d) <= L_stride (%d)", a.L, a.Ls);
-  SA_SUP(a.block == sa::kDecBk, "decode supports block == %d, got %d", sa::kDecBk, a.block);
-  SA_ARG(a.T <= a.block && a.T <= a.L, "T (%d) must be <= block and <= L", a.T);
-  SA_SUP((a.Hq / a.Hkv) * a.T <= 32, "G*T (%d) must be <= 32", (a.Hq / a.Hkv) * a.T);
+  if (a.tok) {
+    SA_SUP(a.dtype == SA_BF16, "token decode supports bf16 only");
+    SA_SUP((a.Hq / a.Hkv) * a.T <= 16, "token decode: G*T (%d) must be <= 16", (a.Hq / a.Hkv) * a.T);
+    SA_ARG(a.T <= a.L, "T (%d) must be <= L", a.T);
+  } else {
+    SA_SUP(a.block == sa::kDecBk, "decode supports block == %d, got %d", sa::kDecBk, a.block);
+    SA_ARG(a.T <= a.block && a.T <= a.L, "T (%d) must be <= block and <= L", a.T);
+    SA_SUP((a.Hq / a.Hkv) * a.T <= 32, "G*T (%d) must be <= 32", (a.Hq / a.Hkv) * a.T);
+  }
   SA_ARG(a.kmax >= 1, "kmax must be >= 1");
   SA_ARG(aligned16(a.kc) && aligned16(a.vc) && aligned16(a.q), "q and the k/v caches must be 16-byte aligned");
   SA_ARG(static_cast<long long>(a.B) * a.Hkv * a.Ls < (1LL << 31), "B*Hkv*L_stride too large");
@@ -567,7 +587,10 @@ sa_status_t validate_select(const SelectArgs& a) {
   SA_ARG(need >= 1, "bad selection parameters");
   SA_ARG(a.kmax >= need, "kmax (%d) too small: the selection needs %d", a.kmax, need);
   const int nb = cdiv(a.L, a.block);
-  SA_SUP(nb <= sa::kTopkMaxN, "at most %d blocks per sequence (got %d)", sa::kTopkMaxN, nb);
+  if (a.mode == SA_SELECT_MASS && !a.prefill)  // given decode scores: any length (long ones are read from L2)
+    SA_ARG(static_cast<long long>(a.B) * a.Hkv * nb < (1LL << 40), "score array too large");
+  else
+    SA_SUP(nb <= sa::kTopkMaxN, "at most %d blocks per sequence (got %d)", sa::kTopkMaxN, nb);
   if (a.prefill) SA_ARG(a.qtile >= 1 && a.Tq == a.L, "prefill: qtile >= 1 and Tq == L required");
   if (a.mode == SA_SELECT_MASS) {
     SA_ARG(a.scores != nullptr, "MASS mode needs the scores array");
@@ -669,6 +692,53 @@ sa_status_t mass_impl(const void* q, const void* k, int B, int L, int Hq, int Hk
 }  // namespace
 
 // ========================================================================= ABI
+// ------------------------------------------------ head-collapsed token mass (decode)
+namespace {
+
+struct TokMassWs {
+  size_t logits, part, lse, total;
+};
+
+// logits [groups][R][L] f32 | partials [groups][<= ceil(L/32)][R] float2 | lse [groups][R] f32
+TokMassWs tokmass_ws(int B, int T, int Hq, int Hkv, int L) {
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  const size_t groups = static_cast<size_t>(B) * Hkv, R = static_cast<size_t>(Hq / Hkv) * T;
+  TokMassWs w;
+  w.logits = 0;
+  w.part = up(groups * R * L * 4);
+  w.lse = w.part + up(groups * static_cast<size_t>(cdiv(L, 32)) * R * 8);
+  w.total = w.lse + up(groups * R * 4);
+  return w;
+}
+
+template <int D>
+sa_status_t launch_token_mass(const void* q, const void* kc, int B, int T, int Hq, int Hkv, int L, int Ls, float scale,
+                              float* mass, void* ws, const DevInfo& di, cudaStream_t st) {
+  const int groups = B * Hkv, R = (Hq / Hkv) * T;
+  const TokMassWs w = tokmass_ws(B, T, Hq, Hkv, L);
+  char* base = static_cast<char*>(ws);
+  float* logits = reinterpret_cast<float*>(base + w.logits);
+  float2* part = reinterpret_cast<float2*>(base + w.part);
+  float* lse2 = reinterpret_cast<float*>(base + w.lse);
+  // about four CTAs of kTmThreads per SM over all groups; warp ranges of a multiple of 32 keys
+  const long long keys = static_cast<long long>(L) * groups;
+  const long long want = static_cast<long long>(di.sms) * 4 * sa::kTmWarps;
+  const int kpw = static_cast<int>(std::max<long long>(32, ((keys + want - 1) / want + 31) / 32 * 32));
+  const int nchunk = cdiv(L, sa::kTmWarps * kpw);
+  sa::token_logits_kernel<D><<<dim3(nchunk, groups), sa::kTmThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc), T, Hq, Hkv, L, Ls,
+      scale * 1.4426950408889634f, kpw, logits, part);
+  SA_CUDA(cudaGetLastError());
+  sa::token_lse_kernel<<<groups, R * 32, 0, st>>>(part, nchunk * sa::kTmWarps, R, lse2);
+  SA_CUDA(cudaGetLastError());
+  sa::token_mass_kernel<<<dim3(cdiv(L, 4 * sa::kTmThreads), B), sa::kTmThreads, 0, st>>>(
+      logits, lse2, Hkv, R, L, 1.f / static_cast<float>(Hq * T), mass);
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int sa_version(void) { return 100; }
@@ -782,6 +852,16 @@ sa_status_t sa_decode(const void* q, const void* k_cache, const void* v_cache, i
   return run_decode(a, as_stream(stream));
 }
 
+sa_status_t sa_decode_tokens(const void* q, const void* k_cache, const void* v_cache, int dtype, const int32_t* idx,
+                             const int32_t* cnt, int kmax, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
+                             float scale, void* out, void* workspace, size_t ws_bytes, void* stream) {
+  t_err.clear();
+  DecodeArgs a{q, k_cache, v_cache, dtype, idx, cnt, kmax, B, T, Hq, Hkv, d, L, L_stride, 1, scale, out,
+               workspace, ws_bytes, 1};
+  SA_TRY(validate_decode(a));
+  return run_decode(a, as_stream(stream));
+}
+
 sa_status_t sa_prefill(const void* q, const void* k, const void* v, int dtype, const int32_t* idx, const int32_t* cnt,
                        int kmax, int B, int L, int Hq, int Hkv, int d, int qtile, int block, float scale, void* out,
                        float* lse_out, void* stream) {
@@ -796,6 +876,33 @@ sa_status_t sa_prefill(const void* q, const void* k, const void* v, int dtype, c
   SA_ARG(static_cast<long long>(B) * L * Hq < (1LL << 31) && static_cast<long long>(B) * Hkv * L < (1LL << 31),
          "B*L*Hq and B*Hkv*L must be < 2^31");
   return prefill_impl(q, k, v, idx, cnt, kmax, B, L, Hq, Hkv, scale, out, lse_out, as_stream(stream));
+}
+
+
+size_t sa_token_mass_workspace_bytes(int B, int T, int Hq, int Hkv, int L) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || L < 1) return 0;
+  return tokmass_ws(B, T, Hq, Hkv, L).total;
+}
+
+sa_status_t sa_token_mass_decode(const void* q, const void* k_cache, int dtype, int B, int T, int Hq, int Hkv, int d,
+                                 int L, int L_stride, float scale, float* mass, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  t_err.clear();
+  SA_TRY(check_common(dtype, B, Hq, Hkv, d));
+  SA_SUP(dtype == SA_BF16, "token mass supports bf16 only");
+  SA_ARG(q && k_cache && mass && workspace, "null pointer argument");
+  SA_ARG(T >= 1 && L >= T && L <= L_stride, "need 1 <= T <= L <= L_stride");
+  SA_SUP((Hq / Hkv) * T <= 16, "token mass: G*T (%d) must be <= 16", (Hq / Hkv) * T);
+  SA_ARG(aligned16(q) && aligned16(k_cache) && aligned16(mass) && aligned16(workspace),
+         "q, k_cache, mass and workspace must be 16-byte aligned");
+  SA_ARG(static_cast<long long>(B) * Hkv * L_stride < (1LL << 31), "B*Hkv*L_stride too large");
+  SA_ARG(ws_bytes >= tokmass_ws(B, T, Hq, Hkv, L).total, "workspace too small: %zu < %zu bytes", ws_bytes,
+         tokmass_ws(B, T, Hq, Hkv, L).total);
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  cudaStream_t st = as_stream(stream);
+  return d == 128 ? launch_token_mass<128>(q, k_cache, B, T, Hq, Hkv, L, L_stride, scale, mass, workspace, di, st)
+                  : launch_token_mass<64>(q, k_cache, B, T, Hq, Hkv, L, L_stride, scale, mass, workspace, di, st);
 }
 
 size_t sa_oracle_mass_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int qtile, int block) {
