@@ -98,7 +98,7 @@ def test_token_select_matches_oracle(sa, name):
     assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, P, what=name)
 
 
-@pytest.mark.parametrize("n", [3, 16384, 16385, 40000, 262144])
+@pytest.mark.parametrize("n", [3, 16384, 16385, 40000, 262144, 300000])
 def test_long_given_selection_exact(sa, n):
     """Given float32 scores with many exact ties: the GPU selection equals the oracle's, bit for bit."""
     r = np.random.default_rng(n)

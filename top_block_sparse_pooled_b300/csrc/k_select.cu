@@ -526,7 +526,19 @@ __global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* 
     if (frac_num > 0) budget = k + (frac_num * nvalid + frac_den - 1) / frac_den;
   }
   const size_t u = static_cast<size_t>(g) * nq + i;
-  for (int bb = threadIdx.x; bb < nvalid; bb += kSelThreads) sts_f32(sc + 4u * bb, scores[u * nb + bb]);
+  for (int b0 = threadIdx.x; b0 < nvalid; b0 += 8 * kSelThreads) {  // eight loads in flight per thread
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int bb = b0 + j * kSelThreads;
+      v[j] = bb < nvalid ? __ldg(scores + u * nb + bb) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int bb = b0 + j * kSelThreads;
+      if (bb < nvalid) sts_f32(sc + 4u * bb, v[j]);
+    }
+  }
   __syncthreads();
   block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, topk_s);
 }
@@ -542,6 +554,210 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_given_global_kernel(con
   const float* sc = scores + u * nb;
   block_topk_impl([&](int b) { return __ldg(sc + b); }, nb, k, kmax, idx + u * kmax, cnt + u,
                   smem_u32(smem_sel_global));
+}
+
+// --------------------------------------------------------------------------
+// Selection from a long given score array (one-token blocks over a long
+// context) by a cluster of CS CTAs per unit: CTA rank r holds the scores
+// [r*per, r*per + per) in shared memory.  The radix passes build a histogram
+// per CTA, add it into CTA rank 0's through distributed shared memory, and
+// after one cluster barrier every CTA reads the cluster total and derives the
+// same digit; the output pass adds the CTAs' counts the same way, so each CTA
+// writes its own selections at their ascending positions.  Same selection
+// as block_topk.  grid (CS, units), cluster (CS, 1, 1), kSelThreads.
+constexpr int kSelClusterPer = 16384;  // scores per CTA
+
+struct SelClusterShared {
+  uint32_t lhist[4][256];  // this CTA's digit counts per pass
+  uint32_t ghist[4][256];  // rank 0: the cluster's
+  uint32_t cdef[16], ceq[16];  // rank 0: per-CTA output counts
+  uint32_t wdef[kSelWarps], weq[kSelWarps];
+};
+
+__device__ __forceinline__ void red_add_cluster(uint32_t a, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_cluster_u32x4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kSelThreads, 1) select_given_cluster_kernel(const float* __restrict__ scores, int nb,
+                                                                           int per, int k, int32_t* __restrict__ idx,
+                                                                           int32_t* __restrict__ cnt, int kmax) {
+  extern __shared__ __align__(16) uint8_t smem_sel_cl[];
+  const uint32_t S = smem_u32(smem_sel_cl);
+  const uint32_t lhist = S + static_cast<uint32_t>(offsetof(SelClusterShared, lhist));
+  const uint32_t ghist = S + static_cast<uint32_t>(offsetof(SelClusterShared, ghist));
+  const uint32_t wdef = S + static_cast<uint32_t>(offsetof(SelClusterShared, wdef));
+  const uint32_t weq = S + static_cast<uint32_t>(offsetof(SelClusterShared, weq));
+  const uint32_t sc = S + static_cast<uint32_t>(((sizeof(SelClusterShared) + 15) / 16) * 16);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int CS = gridDim.x;
+  const size_t u = blockIdx.y;
+  const int b0 = static_cast<int>(rank) * per, b1 = min(nb, b0 + per), m = max(0, b1 - b0);
+  const uint32_t ghist0 = map_cluster(ghist, 0);
+  const uint32_t cdef0 = map_cluster(S + static_cast<uint32_t>(offsetof(SelClusterShared, cdef)), 0);
+  const uint32_t ceq0 = map_cluster(S + static_cast<uint32_t>(offsetof(SelClusterShared, ceq)), 0);
+
+  const float* src = scores + u * nb + b0;
+  for (int i0 = tid; i0 < m; i0 += 16 * kSelThreads) {  // sixteen loads in flight per thread
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int i = i0 + j * kSelThreads;
+      v[j] = i < m ? __ldg(src + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int i = i0 + j * kSelThreads;
+      if (i < m) sts_f32(sc + 4u * i, v[j]);
+    }
+  }
+  for (int i = tid; i < 2 * 4 * 256 / 4; i += kSelThreads)  // lhist and ghist are adjacent
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(lhist + 16u * i), "r"(0u) : "memory");
+  cluster_sync();  // every slice staged and every histogram zeroed before any remote add
+
+  const int n = nb, last = n - 1;
+  const int ncand = n > 2 ? n - 2 : 0;
+  const int take = k <= 0 ? 0 : (k < ncand ? k : ncand);
+  const bool by_key = take > 0 && take < ncand;
+  uint32_t thr = 0u, need_eq = 0u;
+  if (by_key) {
+    uint32_t prefix = 0u, mask = 0u, remaining = static_cast<uint32_t>(take);
+    for (int p = 0; p < 4; ++p) {
+      const int shift = 24 - 8 * p;
+      const uint32_t lp = lhist + 1024u * p;
+      for (int i = tid; i < m; i += kSelThreads) {
+        const int gi = b0 + i;
+        const uint32_t key = float_key(lds_f32(sc + 4u * i));
+        if (gi >= 1 && gi < last && (key & mask) == prefix) red_add_shared(lp + 4u * ((key >> shift) & 255u), 1u);
+      }
+      __syncthreads();
+      {
+        const uint32_t v = lds_u32(lp + 4u * tid);
+        if (v) red_add_cluster(ghist0 + 1024u * p + 4u * tid, v);
+      }
+      cluster_sync();  // the cluster's counts for this pass are complete in rank 0
+      const uint32_t gp = ghist0 + 1024u * p;
+      const uint4 lo4 = ld_cluster_u32x4(gp + 4u * (248 - 8 * lane)), hi4 = ld_cluster_u32x4(gp + 4u * (252 - 8 * lane));
+      const uint32_t c[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
+      uint32_t sum = 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += c[e];
+      uint32_t inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      uint32_t run = inc - sum, hit = 0u, dsel = 0u, rem = 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (hit == 0u && run < remaining && remaining <= run + c[e]) {
+          hit = 1u;
+          dsel = 255u - 8u * static_cast<uint32_t>(lane) - static_cast<uint32_t>(e);
+          rem = remaining - run;
+        }
+        run += c[e];
+      }
+      const int srcl = (__ffs(__ballot_sync(0xFFFFFFFFu, hit != 0u)) - 1) & 31;
+      dsel = __shfl_sync(0xFFFFFFFFu, dsel, srcl);
+      rem = __shfl_sync(0xFFFFFFFFu, rem, srcl);
+      prefix |= dsel << shift;
+      mask |= 255u << shift;
+      remaining = rem;
+    }
+    thr = prefix;
+    need_eq = remaining;
+  }
+  auto classify = [&](int i, bool& def, bool& eq) {  // local index i, global index b0 + i
+    def = false;
+    eq = false;
+    if (i >= m) return;
+    const int gi = b0 + i;
+    if (gi == 0 || gi == last) {
+      def = true;
+    } else if (take > 0) {
+      if (!by_key) {
+        def = true;
+      } else {
+        const uint32_t key = float_key(lds_f32(sc + 4u * i));
+        def = key > thr;
+        eq = key == thr;
+      }
+    }
+  };
+  const int span = ((m + kSelThreads - 1) / kSelThreads) * 32;
+  const int w0 = warp * span;
+  uint32_t ndef = 0u, neq = 0u;
+  for (int base = w0; base < w0 + span; base += 32) {
+    bool d, e;
+    classify(base + lane, d, e);
+    ndef += __popc(__ballot_sync(0xFFFFFFFFu, d));
+    neq += __popc(__ballot_sync(0xFFFFFFFFu, e));
+  }
+  if (lane == 0) {
+    sts_u32(wdef + 4u * warp, ndef);
+    sts_u32(weq + 4u * warp, neq);
+  }
+  __syncthreads();
+  uint32_t def_before = 0u, eq_before = 0u, cta_def = 0u, cta_eq = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    const uint32_t a = lds_u32(wdef + 4u * w), e = lds_u32(weq + 4u * w);
+    def_before += w < warp ? a : 0u;
+    eq_before += w < warp ? e : 0u;
+    cta_def += a;
+    cta_eq += e;
+  }
+  if (tid == 0) {
+    st_cluster_u32(cdef0 + 4u * rank, cta_def);
+    st_cluster_u32(ceq0 + 4u * rank, cta_eq);
+  }
+  cluster_sync();  // every CTA's counts are in rank 0
+  uint32_t def_all = 0u, eq_all = 0u;
+  for (int r = 0; r < CS; ++r) {
+    const uint32_t a = ld_cluster_u32(cdef0 + 4u * r), e = ld_cluster_u32(ceq0 + 4u * r);
+    def_before += r < static_cast<int>(rank) ? a : 0u;
+    eq_before += r < static_cast<int>(rank) ? e : 0u;
+    def_all += a;
+    eq_all += e;
+  }
+  const uint32_t total = def_all + min(eq_all, need_eq);
+  uint32_t pos = def_before + min(eq_before, need_eq);
+  uint32_t eq_seen = eq_before;
+  const uint32_t lt = (1u << lane) - 1u;
+  int32_t* out = idx + u * kmax;
+  for (int base = w0; base < w0 + span; base += 32) {
+    bool d, e;
+    classify(base + lane, d, e);
+    const uint32_t eb = __ballot_sync(0xFFFFFFFFu, e);
+    const bool sel = d || (e && eq_seen + static_cast<uint32_t>(__popc(eb & lt)) < need_eq);
+    const uint32_t sb = __ballot_sync(0xFFFFFFFFu, sel);
+    if (sel) {
+      const uint32_t at = pos + static_cast<uint32_t>(__popc(sb & lt));
+      if (at < static_cast<uint32_t>(kmax)) out[at] = b0 + base + lane;
+    }
+    pos += static_cast<uint32_t>(__popc(sb));
+    eq_seen += static_cast<uint32_t>(__popc(eb));
+  }
+  if (rank == 0) {
+    for (int i = static_cast<int>(total) + tid; i < kmax; i += kSelThreads) out[i] = -1;
+    if (tid == 0) cnt[u] = static_cast<int32_t>(total);
+  }
+  cluster_sync();  // rank 0's shared memory stays until every CTA has read it
 }
 
 }  // namespace sa

@@ -333,7 +333,37 @@ sa_status_t run_select(const SelectArgs& a, cudaStream_t st) {
   const int nb = cdiv(a.L, a.block);
   if (a.mode == SA_SELECT_MASS) {
     const int nq = a.prefill ? cdiv(a.L, a.qtile) : 1;
-    if (nb > sa::kTopkMaxN) {  // decode only (validated): scores stay in global memory
+    if (nb > sa::kTopkMaxN) {  // decode only (validated)
+      // a cluster of CTAs holds the scores in shared memory, 16384 per CTA
+      auto ck = sa::select_given_cluster_kernel;
+      const int head = static_cast<int>(((sizeof(sa::SelClusterShared) + 15) / 16) * 16);
+      static int max_cs_cl = 0;
+      if (max_cs_cl == 0) {
+        SA_TRY(set_smem(ck, head + sa::kSelClusterPer * 4));
+        cudaFuncSetAttribute(reinterpret_cast<const void*>(ck), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        max_cs_cl = std::max(1, std::min(16, max_cluster_size(reinterpret_cast<const void*>(ck),
+                                                               head + sa::kSelClusterPer * 4, groups, st)));
+      }
+      const int cs = cdiv(nb, sa::kSelClusterPer);
+      if (cs <= max_cs_cl) {
+        const int per = cdiv(nb, cs);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs, groups);
+        cfg.blockDim = dim3(sa::kSelThreads);
+        cfg.dynamicSmemBytes = head + per * 4;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        SA_CUDA(cudaLaunchKernelEx(&cfg, ck, static_cast<const float*>(a.scores), nb, per, a.k, a.idx, a.cnt,
+                                   a.kmax));
+        return SA_OK;
+      }
+      // longer still: one CTA per unit, scores read from global memory in every pass
       const int gsmem = static_cast<int>(sizeof(sa::TopkShared));
       sa::select_given_global_kernel<<<dim3(1, groups), sa::kSelThreads, gsmem, st>>>(a.scores, nb, a.k, a.idx,
                                                                                        a.cnt, a.kmax);
@@ -699,14 +729,16 @@ struct TokMassWs {
   size_t logits, part, lse, total;
 };
 
-// logits [groups][R][L] f32 | partials [groups][<= ceil(L/32)][R] float2 | lse [groups][R] f32
+// logits [groups][R][L] f32 | partials [groups][nparts][R] float2 | lse [groups][R] f32, with
+// nparts = kTmWarps * ceil(L / (kTmWarps * kpw)) <= kTmWarps * ceil(L / (kTmWarps * 32)) (kpw >= 32)
 TokMassWs tokmass_ws(int B, int T, int Hq, int Hkv, int L) {
   auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
   const size_t groups = static_cast<size_t>(B) * Hkv, R = static_cast<size_t>(Hq / Hkv) * T;
   TokMassWs w;
   w.logits = 0;
   w.part = up(groups * R * L * 4);
-  w.lse = w.part + up(groups * static_cast<size_t>(cdiv(L, 32)) * R * 8);
+  const size_t nparts_max = static_cast<size_t>(sa::kTmWarps) * cdiv(L, sa::kTmWarps * 32);
+  w.lse = w.part + up(groups * nparts_max * R * 8);
   w.total = w.lse + up(groups * R * 4);
   return w;
 }
@@ -724,7 +756,7 @@ sa_status_t launch_token_mass(const void* q, const void* kc, int B, int T, int H
   const long long keys = static_cast<long long>(L) * groups;
   const long long want = static_cast<long long>(di.sms) * 4 * sa::kTmWarps;
   const int kpw = static_cast<int>(std::max<long long>(32, ((keys + want - 1) / want + 31) / 32 * 32));
-  const int nchunk = cdiv(L, sa::kTmWarps * kpw);
+  const int nchunk = cdiv(L, sa::kTmWarps * kpw);  // nchunk * kTmWarps partials per row fit the workspace (kpw >= 32)
   sa::token_logits_kernel<D><<<dim3(nchunk, groups), sa::kTmThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc), T, Hq, Hkv, L, Ls,
       scale * 1.4426950408889634f, kpw, logits, part);
