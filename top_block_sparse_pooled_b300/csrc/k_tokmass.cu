@@ -13,7 +13,7 @@
 //      the group against each key (mma.sync m16n8k16, bf16 in, fp32
 //      accumulate; K rows come straight from global memory into the B
 //      fragments, 16 bytes per lane), writes the base-2 logits [group][R][L]
-//      and one (max, sum of 2^(s - max)) partial per (row, warp);
+//      and one (max, sum of 2^(s - max)) partial per (row, CTA);
 //   2. token_lse_kernel: merges the partials of each row into its base-2
 //      log-sum-exp;
 //   3. token_mass_kernel: P[b, j] = sum over the rows of all of the row's
@@ -43,7 +43,7 @@ __device__ __forceinline__ void tm_mma_bf16(float* c, const uint32_t* a, uint32_
 // grid (chunks, groups), kTmThreads.  CTA x covers keys [x * kpc, (x+1) * kpc),
 // split into kTmWarps contiguous warp ranges of kpw keys (kpw a multiple of 32).
 // logits: [groups][R][L] base-2 scaled logits (-inf where the key is not
-// visible to the row); part: [groups][chunks * kTmWarps][R] float2 (max, sum).
+// visible to the row); part: [groups][chunks][R] float2 (max, sum).
 template <int D>
 __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfloat16* __restrict__ q,
                                                                   const __nv_bfloat16* __restrict__ kc, int T, int Hq,
@@ -155,10 +155,26 @@ __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfl
     m0 = n0;
     m1 = n1;
   }
+  // then the CTA's eight warps
+  __shared__ float2 wpart[kTmWarps][16];
   if (tq == 0) {
-    const size_t pw = static_cast<size_t>(g) * gridDim.x * kTmWarps + blockIdx.x * kTmWarps + warp;
-    if (gq < R) part[pw * R + gq] = make_float2(m0, s0);
-    if (gq + 8 < R) part[pw * R + gq + 8] = make_float2(m1, s1);
+    if (gq < R) wpart[warp][gq] = make_float2(m0, s0);
+    if (gq + 8 < R) wpart[warp][gq + 8] = make_float2(m1, s1);
+  }
+  __syncthreads();
+  if (threadIdx.x < R) {
+    const int r = threadIdx.x;
+    float m = -INFINITY, sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kTmWarps; ++w) {
+      const float2 v = wpart[w][r];
+      const float n = fmaxf(m, v.x);
+      if (n != -INFINITY) {
+        sum = sum * exp2f(m - n) + v.y * exp2f(v.x - n);
+        m = n;
+      }
+    }
+    part[(static_cast<size_t>(g) * gridDim.x + blockIdx.x) * R + r] = make_float2(m, sum);
   }
 }
 
@@ -194,18 +210,35 @@ __global__ void __launch_bounds__(kTmThreads) token_mass_kernel(const float* __r
   if (j >= L) return;
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   const bool vec = (L % 4 == 0);
-  for (int kvh = 0; kvh < Hkv; ++kvh) {
+  if (vec) {  // rows of eight, loads issued together
+    const int nrow = Hkv * R;
+    const float* lg = logits + static_cast<size_t>(b) * nrow * L + j;
+    const float* ls2 = lse2 + static_cast<size_t>(b) * nrow;
+    for (int r0 = 0; r0 < nrow; r0 += 8) {
+      float4 v[8];
+      float ls[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const bool in = r0 + i < nrow;
+        v[i] = in ? __ldcs(reinterpret_cast<const float4*>(lg + static_cast<size_t>(r0 + i) * L))
+                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        ls[i] = in ? __ldg(ls2 + r0 + i) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a0 += exp2f(v[i].x - ls[i]);
+        a1 += exp2f(v[i].y - ls[i]);
+        a2 += exp2f(v[i].z - ls[i]);
+        a3 += exp2f(v[i].w - ls[i]);
+      }
+    }
+  }
+  for (int kvh = 0; kvh < Hkv && !vec; ++kvh) {
     const int g = b * Hkv + kvh;
     for (int r = 0; r < R; ++r) {
       const float ls = __ldg(lse2 + static_cast<size_t>(g) * R + r);
       const float* row = logits + (static_cast<size_t>(g) * R + r) * L;
-      if (vec) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(row + j));
-        a0 += exp2f(v.x - ls);
-        a1 += exp2f(v.y - ls);
-        a2 += exp2f(v.z - ls);
-        a3 += exp2f(v.w - ls);
-      } else {
+      {
         a0 += exp2f(row[j] - ls);
         if (j + 1 < L) a1 += exp2f(row[j + 1] - ls);
         if (j + 2 < L) a2 += exp2f(row[j + 2] - ls);

@@ -730,14 +730,14 @@ struct TokMassWs {
 };
 
 // logits [groups][R][L] f32 | partials [groups][nparts][R] float2 | lse [groups][R] f32, with
-// nparts = kTmWarps * ceil(L / (kTmWarps * kpw)) <= kTmWarps * ceil(L / (kTmWarps * 32)) (kpw >= 32)
+// nparts = ceil(L / (kTmWarps * kpw)) <= ceil(L / (kTmWarps * 32)) (one per CTA; kpw >= 32)
 TokMassWs tokmass_ws(int B, int T, int Hq, int Hkv, int L) {
   auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
   const size_t groups = static_cast<size_t>(B) * Hkv, R = static_cast<size_t>(Hq / Hkv) * T;
   TokMassWs w;
   w.logits = 0;
   w.part = up(groups * R * L * 4);
-  const size_t nparts_max = static_cast<size_t>(sa::kTmWarps) * cdiv(L, sa::kTmWarps * 32);
+  const size_t nparts_max = static_cast<size_t>(cdiv(L, sa::kTmWarps * 32));
   w.lse = w.part + up(groups * nparts_max * R * 8);
   w.total = w.lse + up(groups * R * 4);
   return w;
@@ -756,12 +756,12 @@ sa_status_t launch_token_mass(const void* q, const void* kc, int B, int T, int H
   const long long keys = static_cast<long long>(L) * groups;
   const long long want = static_cast<long long>(di.sms) * 4 * sa::kTmWarps;
   const int kpw = static_cast<int>(std::max<long long>(32, ((keys + want - 1) / want + 31) / 32 * 32));
-  const int nchunk = cdiv(L, sa::kTmWarps * kpw);  // nchunk * kTmWarps partials per row fit the workspace (kpw >= 32)
+  const int nchunk = cdiv(L, sa::kTmWarps * kpw);  // one partial per CTA and row: fits the workspace (kpw >= 32)
   sa::token_logits_kernel<D><<<dim3(nchunk, groups), sa::kTmThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc), T, Hq, Hkv, L, Ls,
       scale * 1.4426950408889634f, kpw, logits, part);
   SA_CUDA(cudaGetLastError());
-  sa::token_lse_kernel<<<groups, R * 32, 0, st>>>(part, nchunk * sa::kTmWarps, R, lse2);
+  sa::token_lse_kernel<<<groups, R * 32, 0, st>>>(part, nchunk, R, lse2);
   SA_CUDA(cudaGetLastError());
   sa::token_mass_kernel<<<dim3(cdiv(L, 4 * sa::kTmThreads), B), sa::kTmThreads, 0, st>>>(
       logits, lse2, Hkv, R, L, 1.f / static_cast<float>(Hq * T), mass);
