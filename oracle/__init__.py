@@ -279,3 +279,35 @@ def token_attend(q, k, v, Hkv, L, scale, idx, cnt, rows):
     idx_g = np.repeat(np.asarray(idx, dtype=np.int32), Hkv, axis=0)
     cnt_g = np.repeat(np.asarray(cnt, dtype=np.int32), Hkv)
     return attend(q, k, v, Hkv, L, L - T, 1, scale, rows, idx_g, cnt_g)
+
+
+def token_mass_prefill(q, k, Hkv, L, scale):
+    """Per-query head-collapsed token importance for causal prefill ("How Much Dense Attention is
+    Necessary?" Sec. 2.1, per-query support b_sel = 1): P[b, t, j] = mean over all Hq heads of the dense
+    causal softmax probability of key j for query t (zero for j > t).  Composed from `mass` at one-token
+    blocks and one-query tiles."""
+    B, Lq, Hq, _ = q.shape
+    units = [(g, t) for g in range(B * Hkv) for t in range(Lq)]
+    m = mass(q, k, Hkv, L, 0, 1, 1, scale, units)  # [B*Hkv*Lq, L]: summed over each group's heads
+    return m.reshape(B, Hkv, Lq, L).sum(axis=1) / Hq
+
+
+def token_select_prefill(P, k, kmax=None):
+    """Per-query token top-k: for query t, tokens 0 and t forced plus the k highest of 1..t-1 (ties ->
+    lower index), ascending.  P: [B, L, L].  Returns idx [B, L, kmax], cnt [B, L]."""
+    B, Lq, L = P.shape
+    kmax = kmax or (k + 2)
+    t = np.arange(Lq, dtype=np.int64)
+    nvalid = np.tile(t + 1, B)
+    idx, cnt = select(P.reshape(B * Lq, L), nvalid, nvalid - 1, k, kmax)
+    return idx.reshape(B, Lq, kmax), cnt.reshape(B, Lq)
+
+
+def token_attend_prefill(q, k, v, Hkv, L, scale, idx, cnt, rows):
+    """Exact causal attention of (b, t, h) rows over each query's own tokens idx [B, L, kmax] (shared
+    by every kv head of batch row b)."""
+    B, Lq = q.shape[0], q.shape[1]
+    kmax = idx.shape[-1]
+    idx_g = np.repeat(np.asarray(idx, dtype=np.int32), Hkv, axis=0).reshape(B * Hkv * Lq, kmax)
+    cnt_g = np.repeat(np.asarray(cnt, dtype=np.int32), Hkv, axis=0).reshape(B * Hkv * Lq)
+    return attend(q, k, v, Hkv, L, 0, 1, scale, rows, idx_g, cnt_g, nsel=Lq, rows_per_sel=1)

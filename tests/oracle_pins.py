@@ -464,3 +464,41 @@ def pin_token_select_and_attend_match_library():
 
 ALL_PINS += [pin_token_mass_matches_library_softmax, pin_token_mass_uniform_closed_form,
              pin_token_select_and_attend_match_library]
+
+
+def pin_token_prefill_matches_library():
+    """Per-query support (b_sel = 1): P[b, t] = mean over heads of torch.softmax of the causal logits; the
+    selection is the brute-force top-k of 1..t-1 plus tokens 0 and t; attention equals SDPA with each
+    query's own token mask applied to every head."""
+    r = _rng(14)
+    B, Hq, Hkv, d, L, k = 2, 4, 2, 8, 23, 5
+    G = Hq // Hkv
+    q = r.standard_normal((B, L, Hq, d))
+    kk = r.standard_normal((B, Hkv, L, d))
+    v = r.standard_normal((B, Hkv, L, d))
+    scale = 0.6
+    P = oracle.token_mass_prefill(q, kk, Hkv, L, scale)
+    assert P.shape == (B, L, L)
+    allowed = np.zeros((B, Hq, L, L), dtype=bool)
+    idx, cnt = oracle.token_select_prefill(P, k)
+    for b in range(B):
+        for t in range(L):
+            ref = np.zeros(L)
+            for h in range(Hq):
+                logits = torch.from_numpy(scale * (kk[b, h // G] @ q[b, t, h]))
+                logits[t + 1:] = -float("inf")
+                ref += torch.softmax(logits, 0).numpy()
+            np.testing.assert_allclose(P[b, t], ref / Hq, rtol=1e-12, atol=1e-15)
+            assert abs(P[b, t].sum() - 1.0) < 1e-12 and np.all(P[b, t, t + 1:] == 0.0)
+            cands = sorted(range(1, t), key=lambda j: (-P[b, t, j], j))[:k]
+            want = sorted({0, t} | set(cands))
+            assert idx[b, t, : cnt[b, t]].tolist() == want, (b, t)
+            allowed[b, :, t, want] = True
+    rows = [(b, t, h) for b in range(B) for t in range(L) for h in range(Hq)]
+    out, _ = oracle.token_attend_prefill(q, kk, v, Hkv, L, scale, idx, cnt, rows)
+    ref_o = _sdpa(q, kk, v, Hkv, allowed, scale)
+    for n, (b, t, h) in enumerate(rows):
+        np.testing.assert_allclose(out[n], ref_o[b, t, h], rtol=1e-10, atol=1e-12)
+
+
+ALL_PINS += [pin_token_prefill_matches_library]
