@@ -651,6 +651,75 @@ def bench_tokens(reps, peaks, peak_src):
     }
 
 
+def bench_prefill_tokens(reps, peaks, peak_src):
+    """Per-query (b_sel = 1) head-collapsed prefill ("How Much Dense Attention is Necessary?" Sec. 2.1):
+    per-query token mass averaged over the heads, per-query top-256 tokens (+ token 0 and the query's
+    own), causal attention over each query's tokens; B=1, L=4096, Hq=32, Hkv=8, d=128.  L2 flushed
+    before every timed call (256 MB write, untimed)."""
+    import numpy as np
+    import torch
+
+    import synth
+    import top_block_sparse_pooled_b300 as sa
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = synth.WORKLOADS["c5"].replace(B=1, L=4096, k=256, needles=4)
+    x = synth.make_inputs(wl)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, kc, vc = up(x.q), up(x.k), up(x.v)
+    del x
+    B, Hq, Hkv, d, L = wl.B, wl.Hq, wl.Hkv, wl.d, wl.L
+    mws = torch.empty(sa.sa_token_mass_prefill_workspace_bytes(B, L, Hq, Hkv), dtype=torch.uint8, device=dev)
+    mass = torch.empty((B, L, L), dtype=torch.float32, device=dev)
+    kmax = sa.sa_select_kmax(L, 1, 1, True, wl.k)
+    idx = torch.empty((B, 1, L, kmax), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, 1, L), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    pws = torch.zeros(sa.sa_prefill_tokens_workspace_bytes(B, L, Hq, Hkv, d, kmax), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    calls = {
+        "token_mass_prefill": lambda: sa.sa_token_mass_prefill(q, kc, wl.scale, mass, mws),
+        "token_select": lambda: sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, mass.reshape(B, 1, L, L), 1, L, L,
+                                                  1, 1, True, wl.k, 0, 1, 1.0, idx, cnt, d=d, dtype=sa.SA_F32, B=B,
+                                                  Tq=L, Hq=1),
+        "prefill_tokens": lambda: sa.sa_prefill_tokens(q, kc, vc, idx.reshape(B, L, kmax), cnt.reshape(B, L),
+                                                       wl.scale, out, pws),
+    }
+    ts = {name: [] for name in calls}
+    for r in range(reps + 2):
+        for name, fn in calls.items():
+            flush.fill_(r & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts[name].append(e0.elapsed_time(e1) * 1e3)
+    if sa.sa_device_status() != 0:
+        raise RuntimeError("device status word set during the per-query prefill leg")
+    us = {name: round(float(np.median(v)), 2) for name, v in ts.items()}
+    mass_bytes = 2 * B * Hq * L * L * 4 + B * L * L * 4 + B * Hkv * L * d * 2  # logits out and back, mass, K
+    ach = mass_bytes / (us["token_mass_prefill"] * 1e-6) / 1e9
+    sel = int(cnt.sum().item())
+    gathered = sel * Hkv * d * 2 * 2
+    return {
+        "workload": "per-query (b_sel = 1) head-collapsed prefill: B=%d L=%d Hq=%d Hkv=%d d=%d, top-%d tokens per "
+                    "query + token 0 + the query's own (bf16)" % (B, L, Hq, Hkv, d, wl.k),
+        "kernels_us": us,
+        "step_us": round(sum(us.values()), 2),
+        "token_mass_roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                                "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                                "bytes": mass_bytes,
+                                "bytes_note": "base-2 logits written and read back, mass written, K read"},
+        "prefill_tokens": {"tokens_gathered_per_kv_head": sel, "bytes_gathered": gathered,
+                           "GB_s": round(gathered / (us["prefill_tokens"] * 1e-6) / 1e9, 1)},
+        "l2": "flushed before every timed call (256 MB write, untimed)",
+    }
+
+
 def _kernel_hash():
     import hashlib
     h = hashlib.sha256()
@@ -758,7 +827,8 @@ def main():
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
             peaks, src = load_peaks()
-            res = {"tokens": bench_tokens(max(1, args.tokens_reps), peaks, src)}
+            res = {"tokens": bench_tokens(max(1, args.tokens_reps), peaks, src),
+                   "prefill_tokens": bench_prefill_tokens(max(1, args.tokens_reps), peaks, src)}
         elif args.prefill_only:
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
@@ -773,6 +843,7 @@ def main():
             if args.tokens_reps > 0 and res is not None:
                 peaks, src = load_peaks()
                 res["tokens"] = bench_tokens(args.tokens_reps, peaks, src)
+                res["prefill_tokens"] = bench_prefill_tokens(args.tokens_reps, peaks, src)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

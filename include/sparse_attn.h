@@ -305,6 +305,44 @@ sa_status_t sa_decode_tokens(const void* q, const void* k_cache, const void* v_c
                              void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Per-query (b_sel = 1) head-collapsed token importance for causal prefill
+ * ("How Much Dense Attention is Necessary?" Sec. 2.1: each query position
+ * selects its own support from its dense attention distribution, averaged
+ * over the query heads):
+ *   mass[b, t, j] = 1/Hq * sum over heads h of P_{b,t,h}(j),
+ * P_{b,t,h} the dense softmax of scale * q[b,t,h] . k[b, h/G, :] over j <= t
+ * (0 for j > t); each row sums to 1.  q: [B, L, Hq, d]; k: [B, Hkv, L, d];
+ * mass: [B, L, L] float32 written.  workspace: >=
+ * sa_token_mass_prefill_workspace_bytes(...) bytes (base-2 logits
+ * [B*Hkv, G*L, L] float32: B*Hq*L*L*4 bytes, and per-row partials).  Requires
+ * dtype SA_BF16, d in {64, 128}, L <= 65535, 16-byte-aligned pointers.
+ * Select with sa_select_topk (mode SA_SELECT_MASS, prefill, Hkv 1,
+ * qtile 1, block 1: tokens 0 and t forced per query) and attend with
+ * sa_prefill_tokens.
+ */
+size_t sa_token_mass_prefill_workspace_bytes(int B, int L, int Hq, int Hkv);
+sa_status_t sa_token_mass_prefill(const void* q, const void* k, int dtype, int B, int L, int Hq, int Hkv,
+                                  int d, float scale, float* mass, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
+/*
+ * Causal prefill over per-query token supports (b_sel = 1), shared by the
+ * kv heads ("How Much Dense Attention is Necessary?" Sec. 2.1; Sec. 2.2 for
+ * the head-collapsed support).  For query row (b, t, h):
+ *   out[b,t,h] = sum_j softmax_j(scale * q[b,t,h] . k[b,h/G,j]) v[b,h/G,j]
+ * over the distinct tokens j in idx[b, t, 0:cnt[b, t]] with j <= t (others
+ * ignored; order free).  idx: [B, L, kmax] int32, cnt: [B, L] int32.
+ * q, out: [B, L, Hq, d]; k, v: [B, Hkv, L, d].  workspace: >=
+ * sa_prefill_tokens_workspace_bytes(...) bytes, zero-filled before first use,
+ * as for sa_decode.  Requires dtype SA_BF16, d in {64, 128}, G <= 16,
+ * B*L*Hkv <= 2^24, 16-byte-aligned q, k, v.
+ */
+size_t sa_prefill_tokens_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int kmax);
+sa_status_t sa_prefill_tokens(const void* q, const void* k, const void* v, int dtype, const int32_t* idx,
+                              const int32_t* cnt, int kmax, int B, int L, int Hq, int Hkv, int d,
+                              float scale, void* out, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * One decode step: a1 append (k_new, v_new at cache rows L-T..L-1, sketch
  * refreshed), a2+a3 sketch selection with budget k, a4 decode.  If
  * host_io != 0, q, k_new, v_new and out are HOST pointers (pinned memory for

@@ -168,3 +168,106 @@ def test_token_pipeline_full_size(sa):
     out = _token_decode(sa, wl, x, idx, cnt)
     ref, _ = oracle.token_attend(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, g_idx, g_cnt, _rows(wl))
     assert_close(host(out).reshape(-1, wl.d), ref, what="token decode (full size)")
+
+
+# ---------------------------------------------------------------- per-query prefill (b_sel = 1)
+
+PREFILL_CASES = {
+    # odd length, G = 4
+    "g4_odd": synth.WORKLOADS["c5"].replace(B=1, Hq=8, Hkv=2, L=300, k=16, needles=3, seed=101),
+    # d = 64, G = 1, two batch rows
+    "d64_g1_b2": synth.WORKLOADS["c5"].replace(B=2, Hq=4, Hkv=4, d=64, L=257, k=32, needles=2, seed=102),
+    # G = 16 (one M tile per query), budget past most rows' candidates
+    "g16": synth.WORKLOADS["c5"].replace(B=1, Hq=32, Hkv=2, L=200, k=150, needles=2, seed=103),
+}
+
+
+def _prefill_mass(sa, wl, x):
+    q, k = dev(x.q), dev(x.k)
+    ws = torch.empty(sa.sa_token_mass_prefill_workspace_bytes(wl.B, wl.L, wl.Hq, wl.Hkv), dtype=torch.uint8,
+                     device="cuda")
+    mass = torch.empty((wl.B, wl.L, wl.L), dtype=torch.float32, device="cuda")
+    sa.sa_token_mass_prefill(q, k, wl.scale, mass, ws)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    return mass
+
+
+def _prefill_select(sa, wl, mass, k):
+    kmax = sa.sa_select_kmax(wl.L, 1, 1, True, k)
+    idx = torch.full((wl.B, 1, wl.L, kmax), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((wl.B, 1, wl.L), dtype=torch.int32, device="cuda")
+    sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, mass.reshape(wl.B, 1, wl.L, wl.L), 1, wl.L, wl.L, 1, 1, True,
+                      k, 0, 1, 1.0, idx, cnt, d=wl.d, dtype=sa.SA_F32, B=wl.B, Tq=wl.L, Hq=1)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    return idx.reshape(wl.B, wl.L, kmax), cnt.reshape(wl.B, wl.L)
+
+
+def _prefill_tokens(sa, wl, x, idx, cnt):
+    q, k, v = dev(x.q), dev(x.k), dev(x.v)
+    kmax = idx.shape[-1]
+    ws = torch.zeros(sa.sa_prefill_tokens_workspace_bytes(wl.B, wl.L, wl.Hq, wl.Hkv, wl.d, kmax), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.full_like(q, float("nan"))
+    sa.sa_prefill_tokens(q, k, v, idx, cnt, wl.scale, out, ws)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    return out
+
+
+def _prefill_rows(wl):
+    return [(b, t, h) for b in range(wl.B) for t in range(wl.L) for h in range(wl.Hq)]
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_token_mass_prefill_matches_oracle(sa, name):
+    wl = PREFILL_CASES[name]
+    x = synth.make_inputs(wl)
+    got = host(_prefill_mass(sa, wl, x))
+    ref = oracle.token_mass_prefill(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    assert_close(got, ref, atol=MASS_ATOL, rtol=MASS_RTOL, what="per-query token mass")
+    assert np.all(np.abs(got.sum(axis=2) - 1.0) < 1e-4)
+    assert np.all(np.triu(got, 1) == 0.0)  # no mass on future keys
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_token_select_prefill_matches_oracle(sa, name):
+    wl = PREFILL_CASES[name]
+    x = synth.make_inputs(wl)
+    idx, cnt = _prefill_select(sa, wl, _prefill_mass(sa, wl, x), wl.k)
+    P = oracle.token_mass_prefill(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    o_idx, o_cnt = oracle.token_select_prefill(P, wl.k, kmax=idx.shape[-1])
+    kmax = idx.shape[-1]
+    assert_selection(idx.cpu().numpy().reshape(-1, kmax), cnt.cpu().numpy().reshape(-1),
+                     o_idx.reshape(-1, kmax), o_cnt.reshape(-1), P.reshape(-1, wl.L), what=name)
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_prefill_tokens_matches_oracle(sa, name):
+    wl = PREFILL_CASES[name]
+    x = synth.make_inputs(wl)
+    P = oracle.token_mass_prefill(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    o_idx, o_cnt = oracle.token_select_prefill(P, wl.k)
+    out = _prefill_tokens(sa, wl, x, torch.from_numpy(o_idx).cuda(), torch.from_numpy(o_cnt).cuda())
+    ref, _ = oracle.token_attend_prefill(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, o_idx, o_cnt, _prefill_rows(wl))
+    assert_close(host(out).reshape(-1, wl.d), ref, what="per-query prefill " + name)
+
+
+def test_prefill_tokens_pipeline_1k(sa):
+    """1024 queries, 32 heads on 8 kv heads, 64 tokens per query: the GPU's mass, its selection (near-tie
+    rule against the oracle) and the outputs over the GPU's own selection on every row."""
+    wl = synth.WORKLOADS["c5"].replace(B=1, L=1024, k=64, needles=4, seed=104)
+    x = synth.make_inputs(wl)
+    mass = _prefill_mass(sa, wl, x)
+    idx, cnt = _prefill_select(sa, wl, mass, wl.k)
+    P = oracle.token_mass_prefill(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    assert_close(host(mass), P, atol=MASS_ATOL, rtol=MASS_RTOL, what="per-query token mass (1k)")
+    kmax = idx.shape[-1]
+    o_idx, o_cnt = oracle.token_select_prefill(P, wl.k, kmax=kmax)
+    g_idx, g_cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    assert_selection(g_idx.reshape(-1, kmax), g_cnt.reshape(-1), o_idx.reshape(-1, kmax), o_cnt.reshape(-1),
+                     P.reshape(-1, wl.L), what="1k")
+    out = _prefill_tokens(sa, wl, x, idx, cnt)
+    ref, _ = oracle.token_attend_prefill(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, g_idx, g_cnt, _prefill_rows(wl))
+    assert_close(host(out).reshape(-1, wl.d), ref, what="per-query prefill (1k)")

@@ -62,6 +62,10 @@ SIGNATURES = {
     "sa_token_mass_decode": ([_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "sa_decode_tokens": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp],
                          _i),
+    "sa_token_mass_prefill_workspace_bytes": ([_i, _i, _i, _i], _sz),
+    "sa_token_mass_prefill": ([_vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "sa_prefill_tokens_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
+    "sa_prefill_tokens": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "sa_decode_step_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "sa_decode_step": ([_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _i,
                         _vp, _vp, _i, _vp, _sz, _vp], _i),
@@ -225,6 +229,31 @@ def sa_decode_tokens(q, k_cache, v_cache, idx, cnt, L, scale, out, workspace, st
     _check(lib.sa_decode_tokens(_ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(q), _ptr(idx), _ptr(cnt), kmax, B, T,
                                 Hq, Hkv, d, L, Ls, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
                                 _stream(stream)))
+
+
+def sa_token_mass_prefill_workspace_bytes(B, L, Hq, Hkv) -> int:
+    return lib.sa_token_mass_prefill_workspace_bytes(B, L, Hq, Hkv)
+
+
+def sa_token_mass_prefill(q, k, scale, mass, workspace, stream=None):
+    """q: [B, L, Hq, d]; k: [B, Hkv, L, d]; mass: [B, L, L] float32 (written)."""
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[1]
+    _check(lib.sa_token_mass_prefill(_ptr(q), _ptr(k), _dtype(q), B, L, Hq, Hkv, d, float(scale), _ptr(mass),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def sa_prefill_tokens_workspace_bytes(B, L, Hq, Hkv, d, kmax) -> int:
+    return lib.sa_prefill_tokens_workspace_bytes(B, L, Hq, Hkv, d, kmax)
+
+
+def sa_prefill_tokens(q, k, v, idx, cnt, scale, out, workspace, stream=None):
+    """q, out: [B, L, Hq, d]; k, v: [B, Hkv, L, d]; idx [B, L, kmax] per-query tokens; cnt [B, L]."""
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[1]
+    kmax = idx.shape[-1]
+    _check(lib.sa_prefill_tokens(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(idx), _ptr(cnt), kmax, B, L, Hq, Hkv,
+                                 d, float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax) -> int:

@@ -117,6 +117,7 @@ struct DmParams {
   const int32_t* idx;
   const int32_t* cnt;
   int kmax, upg, T, Hq, Hkv, L, Ls, R;  // upg: units per group (kmax blocks, or chunks of 64 tokens)
+  int qpb;  // token mode, per-query prefill: selection rows per batch row (row b' = b * qpb + t), else 0
   float qscale;
   int per, U;
   float* part_o;   // [slots][R][D] (unnormalized numerators)
@@ -208,8 +209,10 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
       const int32_t* sel = p.idx + static_cast<size_t>(b) * p.kmax;
       const uint32_t kt = sbase + lay.stage_off(st), vt = kt + kDmBk * lay.rowb();
       const uint32_t pos = sbase + lay.pos_off() + st * kDmBk * 4;
-      const __nv_bfloat16* kg = p.kc + static_cast<size_t>(e.x) * p.Ls * D;
-      const __nv_bfloat16* vg = p.vc + static_cast<size_t>(e.x) * p.Ls * D;
+      // the group's cache: per-query prefill rows b' = b * qpb + t read batch row b's
+      const size_t kvg = p.qpb ? static_cast<size_t>(b / p.qpb) * p.Hkv + e.x % p.Hkv : static_cast<size_t>(e.x);
+      const __nv_bfloat16* kg = p.kc + kvg * p.Ls * D;
+      const __nv_bfloat16* vg = p.vc + kvg * p.Ls * D;
       int tk[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -284,11 +287,11 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     lim0 = lim1 = -1;
     if (r0 < p.R) {
       q0 = p.q + ((static_cast<size_t>(b) * p.T + r0 / G) * p.Hq + kvh * G + r0 % G) * D;
-      lim0 = p.L - p.T + r0 / G;
+      lim0 = p.qpb ? b % p.qpb : p.L - p.T + r0 / G;  // per-query prefill: query t = b' % qpb sees keys <= t
     }
     if (r1 < p.R) {
       q1 = p.q + ((static_cast<size_t>(b) * p.T + r1 / G) * p.Hq + kvh * G + r1 % G) * D;
-      lim1 = p.L - p.T + r1 / G;
+      lim1 = p.qpb ? b % p.qpb : p.L - p.T + r1 / G;
     }
 #pragma unroll
     for (int kk = 0; kk < C::KSTEPS; ++kk) {

@@ -19,6 +19,11 @@
 //   3. token_mass_kernel: P[b, j] = sum over the rows of all of the row's
 //      groups of 2^(s - lse), times 1/(Hq*T).
 //
+// Per-query prefill (b_sel = 1): the same logits with T = L (query t at
+// position t), R = G*L rows tiled 16 at a time over grid.z, and
+// token_mass_rows_kernel averaging over the heads only, one distribution per
+// query.
+//
 // The dot product over d is order-free, so d is permuted consistently in the
 // A (q) and B (k) fragments: lane (g, t) of a warp holds d = 32p + 8t .. +7 of
 // its key row for k-steps 2p and 2p+1, one 16-byte load.
@@ -40,8 +45,10 @@ __device__ __forceinline__ void tm_mma_bf16(float* c, const uint32_t* a, uint32_
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// grid (chunks, groups), kTmThreads.  CTA x covers keys [x * kpc, (x+1) * kpc),
-// split into kTmWarps contiguous warp ranges of kpw keys (kpw a multiple of 32).
+// grid (chunks, groups, row tiles), kTmThreads.  CTA x covers keys
+// [x * kpc, (x+1) * kpc), split into kTmWarps contiguous warp ranges of kpw keys
+// (kpw a multiple of 32); CTA z the rows [16 z, 16 z + 16).  Keys past the
+// tile's last query are written as -inf without being computed.
 // logits: [groups][R][L] base-2 scaled logits (-inf where the key is not
 // visible to the row); part: [groups][chunks][R] float2 (max, sum).
 template <int D>
@@ -56,12 +63,13 @@ __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfl
   const int g = blockIdx.y, b = g / Hkv, kvh = g % Hkv;
   const int G = Hq / Hkv, R = G * T;
   const int j0 = (blockIdx.x * kTmWarps + warp) * kpw;
+  const int rbase = blockIdx.z * 16;
   // q rows gq and gq + 8 (row r = t * G + head), A fragments in the permuted d order
   uint32_t qa[D / 16][4];
   int lim0 = -1, lim1 = -1;  // last visible key of rows gq and gq + 8 (-1: no such row)
   {
     uint4 x0[KP], x1[KP];
-    const int r0 = gq, r1 = gq + 8;
+    const int r0 = rbase + gq, r1 = rbase + gq + 8;
 #pragma unroll
     for (int pc = 0; pc < KP; ++pc) {
       x0[pc] = make_uint4(0u, 0u, 0u, 0u);
@@ -92,11 +100,18 @@ __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfl
     }
   }
   const __nv_bfloat16* kg = kc + static_cast<size_t>(g) * Ls * D;
-  float* lg0 = logits + (static_cast<size_t>(g) * R + gq) * L;
-  float* lg1 = logits + (static_cast<size_t>(g) * R + gq + 8) * L;
+  const bool has0 = rbase + gq < R, has1 = rbase + gq + 8 < R;
+  float* lg0 = logits + (static_cast<size_t>(g) * R + rbase + gq) * L;
+  float* lg1 = logits + (static_cast<size_t>(g) * R + rbase + gq + 8) * L;
   float m0 = -INFINITY, m1 = -INFINITY, s0 = 0.f, s1 = 0.f;
   const int jend = min(L, j0 + kpw);
-  for (int jb = j0; jb < jend; jb += 8 * kTmNt) {
+  // keys no row of this tile sees: -inf, no loads or math
+  const int jvis = min(jend, L - T + min(R - 1, rbase + 15) / G + 1);
+  for (int key = max(j0, jvis) + lane; key < jend; key += 32) {
+    if (has0) lg0[key] = -INFINITY;
+    if (has1) lg1[key] = -INFINITY;
+  }
+  for (int jb = j0; jb < jvis; jb += 8 * kTmNt) {
     uint4 kv[kTmNt][KP];
 #pragma unroll
     for (int nt = 0; nt < kTmNt; ++nt) {
@@ -120,14 +135,14 @@ __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfl
       const float v10 = key <= lim1 ? c[2] * qscale2 : -INFINITY;
       const float v11 = key + 1 <= lim1 ? c[3] * qscale2 : -INFINITY;
       if (key + 1 < L && (L & 1) == 0) {  // rows start 8-byte aligned when L is even; key is even
-        if (gq < R) *reinterpret_cast<float2*>(lg0 + key) = make_float2(v00, v01);
-        if (gq + 8 < R) *reinterpret_cast<float2*>(lg1 + key) = make_float2(v10, v11);
+        if (has0) *reinterpret_cast<float2*>(lg0 + key) = make_float2(v00, v01);
+        if (has1) *reinterpret_cast<float2*>(lg1 + key) = make_float2(v10, v11);
       } else {
-        if (gq < R) {
+        if (has0) {
           if (key < L) lg0[key] = v00;
           if (key + 1 < L) lg0[key + 1] = v01;
         }
-        if (gq + 8 < R) {
+        if (has1) {
           if (key < L) lg1[key] = v10;
           if (key + 1 < L) lg1[key + 1] = v11;
         }
@@ -158,16 +173,16 @@ __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfl
   // then the CTA's eight warps
   __shared__ float2 wpart[kTmWarps][16];
   if (tq == 0) {
-    if (gq < R) wpart[warp][gq] = make_float2(m0, s0);
-    if (gq + 8 < R) wpart[warp][gq + 8] = make_float2(m1, s1);
+    wpart[warp][gq] = make_float2(m0, s0);
+    wpart[warp][gq + 8] = make_float2(m1, s1);
   }
   __syncthreads();
-  if (threadIdx.x < R) {
-    const int r = threadIdx.x;
+  if (threadIdx.x < 16 && rbase + static_cast<int>(threadIdx.x) < R) {
+    const int rl = threadIdx.x, r = rbase + rl;
     float m = -INFINITY, sum = 0.f;
 #pragma unroll
     for (int w = 0; w < kTmWarps; ++w) {
-      const float2 v = wpart[w][r];
+      const float2 v = wpart[w][rl];
       const float n = fmaxf(m, v.x);
       if (n != -INFINITY) {
         sum = sum * exp2f(m - n) + v.y * exp2f(v.x - n);
@@ -178,9 +193,9 @@ __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfl
   }
 }
 
-// grid (groups), R warps: row r's base-2 log-sum-exp from its nparts partials.
+// grid (groups, ceil(R / 16)), 16 warps: row r's base-2 log-sum-exp from its nparts partials.
 __global__ void token_lse_kernel(const float2* __restrict__ part, int nparts, int R, float* __restrict__ lse2) {
-  const int lane = threadIdx.x & 31, r = threadIdx.x >> 5, g = blockIdx.x;
+  const int lane = threadIdx.x & 31, r = blockIdx.y * 16 + (threadIdx.x >> 5), g = blockIdx.x;
   if (r >= R) return;
   float m = -INFINITY, s = 0.f;
   for (int i = lane; i < nparts; i += 32) {
@@ -255,6 +270,37 @@ __global__ void __launch_bounds__(kTmThreads) token_mass_kernel(const float* __r
     if (j + 2 < L) out[2] = a2 * inv_rows;
     if (j + 3 < L) out[3] = a3 * inv_rows;
   }
+}
+
+// Per-query prefill: grid (ceil(L / (4 * kTmThreads)), L queries, B).
+// P[b, t, j] = 1/Hq * sum over the Hkv groups and their G heads of 2^(s - lse)
+// for the rows (t, head); keys past t are 0 (their logits are -inf).
+__global__ void __launch_bounds__(kTmThreads) token_mass_rows_kernel(const float* __restrict__ logits,
+                                                                     const float* __restrict__ lse2, int Hkv, int G,
+                                                                     int L, float inv_heads,
+                                                                     float* __restrict__ mass) {
+  const int t = blockIdx.y, b = blockIdx.z;
+  const int j = (blockIdx.x * kTmThreads + threadIdx.x) * 4;
+  if (j >= L) return;
+  const size_t R = static_cast<size_t>(G) * L;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  if (j <= t) {
+    for (int kvh = 0; kvh < Hkv; ++kvh) {
+      const size_t g = static_cast<size_t>(b) * Hkv + kvh;
+      for (int hh = 0; hh < G; ++hh) {
+        const size_t r = static_cast<size_t>(t) * G + hh;
+        const float ls = __ldg(lse2 + g * R + r);
+        const float* row = logits + (g * R + r) * L;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e < L) a[e] += exp2f(__ldcs(row + j + e) - ls);
+      }
+    }
+  }
+  float* out = mass + (static_cast<size_t>(b) * L + t) * L + j;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (j + e < L) out[e] = a[e] * inv_heads;
 }
 
 }  // namespace sa

@@ -429,7 +429,15 @@ struct DecodeArgs {
   void* ws;
   size_t ws_bytes;
   int tok = 0;  // token mode: idx [B, kmax] single tokens shared by the kv heads of a batch row
+  int qpb = 0;  // token mode, per-query prefill: B counts (batch row, query) pairs, qpb queries per batch row
 };
+
+// token mode: counters, then (CTAs + groups) <= groups * (chunks + 1) partial slots of R rows
+size_t tok_ws_bytes(long long groups, int R, int d, int kmax) {
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  const size_t slots = static_cast<size_t>(groups) * (cdiv(kmax, sa::kDmBk) + 1);
+  return up(static_cast<size_t>(groups) * 4) + up(slots * R * d * 4) + up(slots * R * 8);
+}
 
 size_t decode_ws_bytes(int groups, int R, int d, int kmax) {
   auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
@@ -474,6 +482,7 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
   p.cnt = a.cnt;
   p.kmax = a.kmax;
   p.upg = upg;
+  p.qpb = a.qpb;
   p.T = a.T;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -491,7 +500,7 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lay = lay;
   CUtensorMap km, vm;
-  const uint64_t rows = static_cast<uint64_t>(groups) * a.Ls;
+  const uint64_t rows = static_cast<uint64_t>(a.qpb ? a.B / a.qpb * a.Hkv : groups) * a.Ls;  // the caches' rows
   SA_TRY(make_map_2d(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kc, D, rows, D * 2, 64, sa::kDmBk,
                      CU_TENSOR_MAP_SWIZZLE_128B));
   SA_TRY(make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.vc, D, rows, D * 2, 64, sa::kDmBk,
@@ -566,7 +575,7 @@ sa_status_t check_common(int dtype, int B, int Hq, int Hkv, int d) {
 }
 
 sa_status_t validate_decode(const DecodeArgs& a) {
-  SA_TRY(check_common(a.dtype, a.B, a.Hq, a.Hkv, a.d));
+  SA_TRY(check_common(a.dtype, a.qpb ? a.B / a.qpb : a.B, a.Hq, a.Hkv, a.d));
   SA_ARG(a.q && a.kc && a.vc && a.idx && a.cnt && a.out, "null pointer argument");
   SA_ARG(a.T >= 1, "T must be >= 1");
   SA_ARG(a.L >= 1 && a.L <= a.Ls, "need 1 <= L (%d) <= L_stride (%d)", a.L, a.Ls);
@@ -581,9 +590,10 @@ sa_status_t validate_decode(const DecodeArgs& a) {
   }
   SA_ARG(a.kmax >= 1, "kmax must be >= 1");
   SA_ARG(aligned16(a.kc) && aligned16(a.vc) && aligned16(a.q), "q and the k/v caches must be 16-byte aligned");
-  SA_ARG(static_cast<long long>(a.B) * a.Hkv * a.Ls < (1LL << 31), "B*Hkv*L_stride too large");
+  SA_ARG(static_cast<long long>(a.qpb ? a.B / a.qpb : a.B) * a.Hkv * a.Ls < (1LL << 31), "B*Hkv*L_stride too large");
   SA_ARG(a.ws && aligned16(a.ws), "workspace must be a 16-byte-aligned device pointer");
-  const size_t need = decode_ws_bytes(a.B * a.Hkv, (a.Hq / a.Hkv) * a.T, a.d, a.kmax);
+  const size_t need = a.tok ? tok_ws_bytes(static_cast<long long>(a.B) * a.Hkv, (a.Hq / a.Hkv) * a.T, a.d, a.kmax)
+                            : decode_ws_bytes(a.B * a.Hkv, (a.Hq / a.Hkv) * a.T, a.d, a.kmax);
   SA_ARG(a.ws_bytes >= need, "workspace too small: %zu < %zu bytes", a.ws_bytes, need);
   return SA_OK;
 }
@@ -745,26 +755,31 @@ TokMassWs tokmass_ws(int B, int T, int Hq, int Hkv, int L) {
 
 template <int D>
 sa_status_t launch_token_mass(const void* q, const void* kc, int B, int T, int Hq, int Hkv, int L, int Ls, float scale,
-                              float* mass, void* ws, const DevInfo& di, cudaStream_t st) {
+                              float* mass, void* ws, const DevInfo& di, cudaStream_t st, bool per_query) {
   const int groups = B * Hkv, R = (Hq / Hkv) * T;
+  const int rtiles = cdiv(R, 16);
   const TokMassWs w = tokmass_ws(B, T, Hq, Hkv, L);
   char* base = static_cast<char*>(ws);
   float* logits = reinterpret_cast<float*>(base + w.logits);
   float2* part = reinterpret_cast<float2*>(base + w.part);
   float* lse2 = reinterpret_cast<float*>(base + w.lse);
   // about four CTAs of kTmThreads per SM over all groups; warp ranges of a multiple of 32 keys
-  const long long keys = static_cast<long long>(L) * groups;
+  const long long keys = static_cast<long long>(L) * groups * rtiles;
   const long long want = static_cast<long long>(di.sms) * 4 * sa::kTmWarps;
   const int kpw = static_cast<int>(std::max<long long>(32, ((keys + want - 1) / want + 31) / 32 * 32));
   const int nchunk = cdiv(L, sa::kTmWarps * kpw);  // one partial per CTA and row: fits the workspace (kpw >= 32)
-  sa::token_logits_kernel<D><<<dim3(nchunk, groups), sa::kTmThreads, 0, st>>>(
+  sa::token_logits_kernel<D><<<dim3(nchunk, groups, rtiles), sa::kTmThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc), T, Hq, Hkv, L, Ls,
       scale * 1.4426950408889634f, kpw, logits, part);
   SA_CUDA(cudaGetLastError());
-  sa::token_lse_kernel<<<groups, R * 32, 0, st>>>(part, nchunk, R, lse2);
+  sa::token_lse_kernel<<<dim3(groups, rtiles), 16 * 32, 0, st>>>(part, nchunk, R, lse2);
   SA_CUDA(cudaGetLastError());
-  sa::token_mass_kernel<<<dim3(cdiv(L, 4 * sa::kTmThreads), B), sa::kTmThreads, 0, st>>>(
-      logits, lse2, Hkv, R, L, 1.f / static_cast<float>(Hq * T), mass);
+  if (per_query)
+    sa::token_mass_rows_kernel<<<dim3(cdiv(L, 4 * sa::kTmThreads), L, B), sa::kTmThreads, 0, st>>>(
+        logits, lse2, Hkv, Hq / Hkv, L, 1.f / static_cast<float>(Hq), mass);
+  else
+    sa::token_mass_kernel<<<dim3(cdiv(L, 4 * sa::kTmThreads), B), sa::kTmThreads, 0, st>>>(
+        logits, lse2, Hkv, R, L, 1.f / static_cast<float>(Hq * T), mass);
   SA_CUDA(cudaGetLastError());
   return SA_OK;
 }
@@ -933,8 +948,48 @@ sa_status_t sa_token_mass_decode(const void* q, const void* k_cache, int dtype, 
   DevInfo di;
   SA_TRY(dev_info(&di));
   cudaStream_t st = as_stream(stream);
-  return d == 128 ? launch_token_mass<128>(q, k_cache, B, T, Hq, Hkv, L, L_stride, scale, mass, workspace, di, st)
-                  : launch_token_mass<64>(q, k_cache, B, T, Hq, Hkv, L, L_stride, scale, mass, workspace, di, st);
+  return d == 128 ? launch_token_mass<128>(q, k_cache, B, T, Hq, Hkv, L, L_stride, scale, mass, workspace, di, st, false)
+                  : launch_token_mass<64>(q, k_cache, B, T, Hq, Hkv, L, L_stride, scale, mass, workspace, di, st, false);
+}
+
+size_t sa_token_mass_prefill_workspace_bytes(int B, int L, int Hq, int Hkv) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || L < 1) return 0;
+  return tokmass_ws(B, L, Hq, Hkv, L).total;
+}
+
+sa_status_t sa_token_mass_prefill(const void* q, const void* k, int dtype, int B, int L, int Hq, int Hkv, int d,
+                                  float scale, float* mass, void* workspace, size_t ws_bytes, void* stream) {
+  t_err.clear();
+  SA_TRY(check_common(dtype, B, Hq, Hkv, d));
+  SA_SUP(dtype == SA_BF16, "token mass supports bf16 only");
+  SA_ARG(q && k && mass && workspace, "null pointer argument");
+  SA_ARG(L >= 1 && L <= 65535, "need 1 <= L <= 65535");
+  SA_ARG(aligned16(q) && aligned16(k) && aligned16(mass) && aligned16(workspace),
+         "q, k, mass and workspace must be 16-byte aligned");
+  SA_ARG(static_cast<long long>(B) * Hkv * L < (1LL << 31), "B*Hkv*L too large");
+  SA_ARG(ws_bytes >= tokmass_ws(B, L, Hq, Hkv, L).total, "workspace too small: %zu < %zu bytes", ws_bytes,
+         tokmass_ws(B, L, Hq, Hkv, L).total);
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  cudaStream_t st = as_stream(stream);
+  return d == 128 ? launch_token_mass<128>(q, k, B, L, Hq, Hkv, L, L, scale, mass, workspace, di, st, true)
+                  : launch_token_mass<64>(q, k, B, L, Hq, Hkv, L, L, scale, mass, workspace, di, st, true);
+}
+
+size_t sa_prefill_tokens_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int kmax) {
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || kmax < 1) return 0;
+  return tok_ws_bytes(static_cast<long long>(B) * L * Hkv, Hq / Hkv, d, kmax);
+}
+
+sa_status_t sa_prefill_tokens(const void* q, const void* k, const void* v, int dtype, const int32_t* idx,
+                              const int32_t* cnt, int kmax, int B, int L, int Hq, int Hkv, int d, float scale,
+                              void* out, void* workspace, size_t ws_bytes, void* stream) {
+  t_err.clear();
+  SA_ARG(B >= 1 && L >= 1 && static_cast<long long>(B) * L * Hkv <= (1LL << 24), "B*L*Hkv must be in [1, 2^24]");
+  // each (batch row, query) pair is one selection row with a single query at position t
+  DecodeArgs a{q, k, v, dtype, idx, cnt, kmax, B * L, 1, Hq, Hkv, d, L, L, 1, scale, out, workspace, ws_bytes, 1, L};
+  SA_TRY(validate_decode(a));
+  return run_decode(a, as_stream(stream));
 }
 
 size_t sa_oracle_mass_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int qtile, int block) {
