@@ -701,7 +701,8 @@ def bench_prefill_tokens(reps, peaks, peak_src):
     if sa.sa_device_status() != 0:
         raise RuntimeError("device status word set during the per-query prefill leg")
     us = {name: round(float(np.median(v)), 2) for name, v in ts.items()}
-    mass_bytes = 2 * B * Hq * L * L * 4 + B * L * L * 4 + B * Hkv * L * d * 2  # logits out and back, mass, K
+    # causal logits written and read back (L(L+1)/2 per head), the mass written, K read
+    mass_bytes = 2 * B * Hq * (L * (L + 1) // 2) * 4 + B * L * L * 4 + B * Hkv * L * d * 2
     ach = mass_bytes / (us["token_mass_prefill"] * 1e-6) / 1e9
     sel = int(cnt.sum().item())
     gathered = sel * Hkv * d * 2 * 2
@@ -713,7 +714,7 @@ def bench_prefill_tokens(reps, peaks, peak_src):
         "token_mass_roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                                 "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
                                 "bytes": mass_bytes,
-                                "bytes_note": "base-2 logits written and read back, mass written, K read"},
+                                "bytes_note": "causal base-2 logits written and read back, mass written, K read"},
         "prefill_tokens": {"tokens_gathered_per_kv_head": sel, "bytes_gathered": gathered,
                            "GB_s": round(gathered / (us["prefill_tokens"] * 1e-6) / 1e9, 1)},
         "l2": "flushed before every timed call (256 MB write, untimed)",

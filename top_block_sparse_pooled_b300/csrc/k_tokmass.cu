@@ -48,14 +48,15 @@ __device__ __forceinline__ void tm_mma_bf16(float* c, const uint32_t* a, uint32_
 // grid (chunks, groups, row tiles), kTmThreads.  CTA x covers keys
 // [x * kpc, (x+1) * kpc), split into kTmWarps contiguous warp ranges of kpw keys
 // (kpw a multiple of 32); CTA z the rows [16 z, 16 z + 16).  Keys past the
-// tile's last query are written as -inf without being computed.
+// tile's last query are not computed; they are written as -inf only when
+// write_hidden is set (the per-query mass pass never reads them).
 // logits: [groups][R][L] base-2 scaled logits (-inf where the key is not
 // visible to the row); part: [groups][chunks][R] float2 (max, sum).
 template <int D>
 __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfloat16* __restrict__ q,
                                                                   const __nv_bfloat16* __restrict__ kc, int T, int Hq,
                                                                   int Hkv, int L, int Ls, float qscale2, int kpw,
-                                                                  float* __restrict__ logits,
+                                                                  int write_hidden, float* __restrict__ logits,
                                                                   float2* __restrict__ part) {
   constexpr int KP = D / 32;  // 16-byte pieces per lane per key row (each covers two k-steps)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kTmThreads) token_logits_kernel(const __nv_bfl
   const int jend = min(L, j0 + kpw);
   // keys no row of this tile sees: -inf, no loads or math
   const int jvis = min(jend, L - T + min(R - 1, rbase + 15) / G + 1);
-  for (int key = max(j0, jvis) + lane; key < jend; key += 32) {
+  for (int key = max(j0, jvis) + lane; write_hidden && key < jend; key += 32) {
     if (has0) lg0[key] = -INFINITY;
     if (has1) lg1[key] = -INFINITY;
   }
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kTmThreads) token_mass_kernel(const float* __r
 
 // Per-query prefill: grid (ceil(L / (4 * kTmThreads)), L queries, B).
 // P[b, t, j] = 1/Hq * sum over the Hkv groups and their G heads of 2^(s - lse)
-// for the rows (t, head); keys past t are 0 (their logits are -inf).
+// for the rows (t, head); keys past t are 0 (their logits are not read).
 __global__ void __launch_bounds__(kTmThreads) token_mass_rows_kernel(const float* __restrict__ logits,
                                                                      const float* __restrict__ lse2, int Hkv, int G,
                                                                      int L, float inv_heads,
@@ -285,15 +286,35 @@ __global__ void __launch_bounds__(kTmThreads) token_mass_rows_kernel(const float
   const size_t R = static_cast<size_t>(G) * L;
   float a[4] = {0.f, 0.f, 0.f, 0.f};
   if (j <= t) {
-    for (int kvh = 0; kvh < Hkv; ++kvh) {
-      const size_t g = static_cast<size_t>(b) * Hkv + kvh;
-      for (int hh = 0; hh < G; ++hh) {
-        const size_t r = static_cast<size_t>(t) * G + hh;
-        const float ls = __ldg(lse2 + g * R + r);
-        const float* row = logits + (g * R + r) * L;
+    const int nrow = Hkv * G;  // rows (kvh, head) of query t, eight loads in flight
+    const bool vec = (L % 4 == 0);
+    for (int i0 = 0; i0 < nrow; i0 += 8) {
+      float4 v[8];
+      float ls[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (j + e < L) a[e] += exp2f(__ldcs(row + j + e) - ls);
+      for (int i = 0; i < 8; ++i) {
+        const int ri = i0 + i;
+        const size_t g = static_cast<size_t>(b) * Hkv + (ri < nrow ? ri / G : 0);
+        const size_t r = static_cast<size_t>(t) * G + (ri < nrow ? ri % G : 0);
+        const float* row = logits + (g * R + r) * L + j;
+        ls[i] = ri < nrow ? __ldg(lse2 + g * R + r) : 0.f;
+        if (ri >= nrow) {
+          v[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        } else if (vec) {
+          v[i] = __ldcs(reinterpret_cast<const float4*>(row));
+        } else {
+          v[i].x = __ldcs(row);
+          v[i].y = j + 1 < L ? __ldcs(row + 1) : -INFINITY;
+          v[i].z = j + 2 < L ? __ldcs(row + 2) : -INFINITY;
+          v[i].w = j + 3 < L ? __ldcs(row + 3) : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a[0] += exp2f(v[i].x - ls[i]);
+        a[1] += j + 1 <= t ? exp2f(v[i].y - ls[i]) : 0.f;
+        a[2] += j + 2 <= t ? exp2f(v[i].z - ls[i]) : 0.f;
+        a[3] += j + 3 <= t ? exp2f(v[i].w - ls[i]) : 0.f;
       }
     }
   }

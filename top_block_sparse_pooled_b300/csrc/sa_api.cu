@@ -766,11 +766,12 @@ sa_status_t launch_token_mass(const void* q, const void* kc, int B, int T, int H
   // about four CTAs of kTmThreads per SM over all groups; warp ranges of a multiple of 32 keys
   const long long keys = static_cast<long long>(L) * groups * rtiles;
   const long long want = static_cast<long long>(di.sms) * 4 * sa::kTmWarps;
-  const int kpw = static_cast<int>(std::max<long long>(32, ((keys + want - 1) / want + 31) / 32 * 32));
+  int kpw = static_cast<int>(std::max<long long>(32, ((keys + want - 1) / want + 31) / 32 * 32));
+  kpw = std::min(kpw, std::max(32, (cdiv(L, sa::kTmWarps) + 31) / 32 * 32));  // every warp of a CTA gets keys
   const int nchunk = cdiv(L, sa::kTmWarps * kpw);  // one partial per CTA and row: fits the workspace (kpw >= 32)
   sa::token_logits_kernel<D><<<dim3(nchunk, groups, rtiles), sa::kTmThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc), T, Hq, Hkv, L, Ls,
-      scale * 1.4426950408889634f, kpw, logits, part);
+      scale * 1.4426950408889634f, kpw, per_query ? 0 : 1, logits, part);
   SA_CUDA(cudaGetLastError());
   sa::token_lse_kernel<<<dim3(groups, rtiles), 16 * 32, 0, st>>>(part, nchunk, R, lse2);
   SA_CUDA(cudaGetLastError());
