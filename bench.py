@@ -329,16 +329,15 @@ def bench_decode(args, wl, rank, world):
     hout = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
     ne = min(K, 2000)
     with torch.cuda.stream(stream):
+        # one prepared call per rotated input set (the binding marshals the arguments once)
+        steps = [sa.DecodeStep(hq, hkn, hvn, s["kc"], s["vc"], s["sk"], wl.L, wl.Bk, wl.k, wl.scale, s["idx"],
+                               s["cnt"], hout, s["ws"], host_io=True, stream=stream) for s in sets]
         for i in range(5):
-            s = sets[i % R]
-            sa.sa_decode_step(hq, hkn, hvn, s["kc"], s["vc"], s["sk"], wl.L, wl.Bk, wl.k, wl.scale, s["idx"],
-                              s["cnt"], hout, s["ws"], host_io=True)
+            steps[i % R]()
         stream.synchronize()
         t0 = time.perf_counter()
         for i in range(ne):
-            s = sets[i % R]
-            sa.sa_decode_step(hq, hkn, hvn, s["kc"], s["vc"], s["sk"], wl.L, wl.Bk, wl.k, wl.scale, s["idx"],
-                              s["cnt"], hout, s["ws"], host_io=True)
+            steps[i % R]()
             stream.synchronize()  # the next token needs this one's output
         t_e2e = (time.perf_counter() - t0) / ne
     es = wl.esize

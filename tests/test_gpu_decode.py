@@ -214,6 +214,47 @@ def test_decode_step_matches_oracle(sa, host_io):
     assert_close(host(out).reshape(ref.shape), ref, what="decode step")
 
 
+def test_decode_step_graph_replay_reads_new_inputs(sa):
+    """On a non-default stream the step is captured once and replayed: a second call with the same
+    buffers but new query contents gives the new query's exact result."""
+    wl = DECODE_CASES["c2"].replace(B=2, L=8192)
+    x = synth.make_inputs(wl)
+    pos = wl.L - wl.T
+    kfull, vfull = dev(x.k), dev(x.v)
+    kc, vc = kfull.clone(), vfull.clone()
+    kc[:, :, pos:] = 0
+    vc[:, :, pos:] = 0
+    sk = _sketch_buf(wl)
+    sa.sa_build_sketch(kc, pos, wl.Bk, sk)
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
+    idx = torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sa.sa_decode_step_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, sa.SA_BF16, kmax),
+                     dtype=torch.uint8, device="cuda")
+    q = dev(x.q).cpu().pin_memory()
+    k_new = kfull[:, :, pos:].permute(0, 2, 1, 3).contiguous().cpu().pin_memory()
+    v_new = vfull[:, :, pos:].permute(0, 2, 1, 3).contiguous().cpu().pin_memory()
+    out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    st = torch.cuda.Stream()
+    qs = [x.q, np.ascontiguousarray(x.q[:, :, ::-1, :])]  # second call: the heads in reverse order
+    step = sa.DecodeStep(q, k_new, v_new, kc, vc, sk, wl.L, wl.Bk, wl.k, wl.scale, idx, cnt, out, ws,
+                         host_io=True, stream=st)
+    for call, qn in enumerate(qs):
+        q.copy_(torch.from_numpy(qn.view(np.int16)).view(torch.bfloat16))
+        if call == 0:  # the plain call, then the prepared one on the same buffers
+            with torch.cuda.stream(st):
+                sa.sa_decode_step(q, k_new, v_new, kc, vc, sk, wl.L, wl.Bk, wl.k, wl.scale, idx, cnt, out, ws,
+                                  host_io=True)
+        else:
+            step()
+        st.synchronize()
+        _check_status(sa)
+        o_idx, o_cnt, o_s, _ = oracle.decode_select(qn, x.k, wl, kmax=kmax)
+        assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s, what="call %d" % call)
+        ref, _ = oracle.attend(qn, x.k, x.v, wl.Hkv, wl.L, pos, wl.Bk, wl.scale, _all_rows(wl), o_idx, o_cnt)
+        assert_close(host(out).reshape(ref.shape), ref, what="decode step, call %d" % call)
+
+
 def test_workspace_reuse_keeps_counters_clean(sa):
     """Back-to-back calls on one workspace (different selections) are each exact."""
     wl = DECODE_CASES["c3"].replace(L=16384, k=20, needles=5)

@@ -260,13 +260,37 @@ def sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax) -> int:
     return lib.sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax)
 
 
-def sa_decode_step(q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale, idx, cnt, out, workspace,
-                   scores=None, host_io=False, stream=None):
-    """Append + select + decode.  With host_io, q/k_new/v_new/out are pinned host tensors."""
+def _decode_step_args(q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale, idx, cnt, out, workspace,
+                      scores, host_io, stream):
     B, T, Hq, d = q.shape
     Hkv, Ls = k_cache.shape[1], k_cache.shape[2]
     kmax = idx.shape[-1]
-    _check(lib.sa_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _dtype(q), _ptr(k_cache), _ptr(v_cache),
-                              _ptr(sketch), B, T, Hq, Hkv, d, L, Ls, block, k, float(scale), _ptr(idx), _ptr(cnt),
-                              kmax, _ptr(scores), _ptr(out), 1 if host_io else 0, _ptr(workspace),
-                              workspace.numel(), _stream(stream)))
+    return (_ptr(q), _ptr(k_new), _ptr(v_new), _dtype(q), _ptr(k_cache), _ptr(v_cache), _ptr(sketch), B, T, Hq, Hkv,
+            d, L, Ls, block, k, float(scale), _ptr(idx), _ptr(cnt), kmax, _ptr(scores), _ptr(out),
+            1 if host_io else 0, _ptr(workspace), workspace.numel(), _stream(stream))
+
+
+def sa_decode_step(q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale, idx, cnt, out, workspace,
+                   scores=None, host_io=False, stream=None):
+    """Append + select + decode.  With host_io, q/k_new/v_new/out are pinned host tensors."""
+    _check(lib.sa_decode_step(*_decode_step_args(q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale, idx,
+                                                 cnt, out, workspace, scores, host_io, stream)))
+
+
+class DecodeStep:
+    """sa_decode_step with its arguments marshalled once, for a serving loop that calls the same
+    buffers every token: step() issues the call with the stored pointers and sizes.  The tensors must
+    stay alive, keep their shapes and stay where they are; their contents may change between calls.
+    The stream is fixed here (default: the current stream)."""
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale, idx, cnt, out, workspace,
+                 scores=None, host_io=False, stream=None):
+        self._keep = (q, k_new, v_new, k_cache, v_cache, sketch, idx, cnt, out, workspace, scores)
+        self._args = _decode_step_args(q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale, idx, cnt,
+                                       out, workspace, scores, host_io, stream)
+        self._fn = lib.sa_decode_step
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status != SA_OK:
+            _check(status)

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
+#include <vector>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -787,6 +789,57 @@ sa_status_t launch_token_mass(const void* q, const void* kc, int B, int T, int H
 
 }  // namespace
 
+// ------------------------------------------------ one decode step (a1 + a2 + a3 + a4)
+namespace {
+
+struct StepArgs {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  int dtype;
+  void* k_cache;
+  void* v_cache;
+  float* sketch;
+  int B, T, Hq, Hkv, d, L, L_stride, block, k;
+  float scale;
+  int32_t* idx;
+  int32_t* cnt;
+  int kmax;
+  float* scores;
+  void* out;
+  int host_io;
+  void* workspace;
+  size_t ws_bytes;
+};
+
+using StepKey = std::array<uint64_t, 26>;
+
+StepKey step_key(const StepArgs& a, int dev) {
+  auto P = [](const void* p) { return static_cast<uint64_t>(reinterpret_cast<uintptr_t>(p)); };
+  uint32_t sc;
+  std::memcpy(&sc, &a.scale, 4);
+  return StepKey{P(a.q), P(a.k_new), P(a.v_new), static_cast<uint64_t>(a.dtype), P(a.k_cache), P(a.v_cache),
+                 P(a.sketch), static_cast<uint64_t>(a.B), static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.Hq),
+                 static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.d), static_cast<uint64_t>(a.L),
+                 static_cast<uint64_t>(a.L_stride), static_cast<uint64_t>(a.block), static_cast<uint64_t>(a.k), sc,
+                 P(a.idx), P(a.cnt), static_cast<uint64_t>(a.kmax), P(a.scores), P(a.out),
+                 static_cast<uint64_t>(a.host_io), P(a.workspace), static_cast<uint64_t>(a.ws_bytes),
+                 static_cast<uint64_t>(dev)};
+}
+
+struct StepGraph {
+  StepKey key;
+  cudaGraphExec_t exec;
+  uint64_t last_use;
+};
+
+constexpr size_t kStepCacheMax = 32;
+std::mutex g_step_mu;
+std::vector<StepGraph> g_step_cache;
+uint64_t g_step_clock = 0;
+
+}  // namespace
+
 extern "C" {
 
 int sa_version(void) { return 100; }
@@ -1025,6 +1078,50 @@ size_t sa_decode_step_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int 
   return up(dec) + 2 * up(qb) + 2 * up(kb);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The step's copies and launches, in stream order (the body of sa_decode_step).
+sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  const size_t es = static_cast<size_t>(esize(a.dtype));
+  const size_t dec = up(sa_decode_workspace_bytes(a.B, a.T, a.Hq, a.Hkv, a.d, a.kmax));
+  const size_t qb = static_cast<size_t>(a.B) * a.T * a.Hq * a.d * es;
+  const size_t kb = static_cast<size_t>(a.B) * a.T * a.Hkv * a.d * es;
+  char* w = static_cast<char*>(a.workspace);
+  const void* qd = a.q;
+  const void* knd = a.k_new;
+  const void* vnd = a.v_new;
+  void* outd = a.out;
+  if (a.host_io) {
+    void* q_dev = w + dec;
+    void* out_dev = w + dec + up(qb);
+    void* kn_dev = w + dec + 2 * up(qb);
+    void* vn_dev = w + dec + 2 * up(qb) + up(kb);
+    SA_CUDA(cudaMemcpyAsync(q_dev, a.q, qb, cudaMemcpyHostToDevice, st));
+    SA_CUDA(cudaMemcpyAsync(kn_dev, a.k_new, kb, cudaMemcpyHostToDevice, st));
+    SA_CUDA(cudaMemcpyAsync(vn_dev, a.v_new, kb, cudaMemcpyHostToDevice, st));
+    qd = q_dev;
+    knd = kn_dev;
+    vnd = vn_dev;
+    outd = out_dev;
+  }
+  void* sp = static_cast<void*>(st);
+  SA_TRY(sa_append_kv(knd, vnd, a.dtype, a.B, a.Hkv, a.T, a.d, a.k_cache, a.v_cache, a.L_stride, a.L - a.T, a.block,
+                      a.sketch, sp));
+  SA_TRY(sa_select_topk(SA_SELECT_SKETCH, qd, a.dtype, a.sketch, a.scores, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
+                        a.L_stride, a.block, 0, 0, a.k, 0, 1, a.scale, a.idx, a.cnt, a.kmax, sp));
+  SA_TRY(sa_decode(qd, a.k_cache, a.v_cache, a.dtype, a.idx, a.cnt, a.kmax, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
+                   a.L_stride, a.block, a.scale, outd, w, dec, sp));
+  if (a.host_io) SA_CUDA(cudaMemcpyAsync(a.out, outd, qb, cudaMemcpyDeviceToHost, st));
+  return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, int dtype, void* k_cache,
                            void* v_cache, float* sketch, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
                            int block, int k, float scale, int32_t* idx, int32_t* cnt, int kmax, float* scores,
@@ -1035,36 +1132,56 @@ sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, 
   SA_ARG(L >= T && T >= 1, "need 1 <= T <= L");
   const size_t need = sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax);
   SA_ARG(need && ws_bytes >= need, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  const StepArgs a{q, k_new, v_new, dtype, k_cache, v_cache, sketch, B, T, Hq, Hkv, d, L, L_stride, block, k,
+                   scale, idx, cnt, kmax, scores, out, host_io, workspace, ws_bytes};
   cudaStream_t st = as_stream(stream);
-  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
-  const size_t es = static_cast<size_t>(esize(dtype));
-  const size_t dec = up(sa_decode_workspace_bytes(B, T, Hq, Hkv, d, kmax));
-  const size_t qb = static_cast<size_t>(B) * T * Hq * d * es;
-  const size_t kb = static_cast<size_t>(B) * T * Hkv * d * es;
-  char* w = static_cast<char*>(workspace);
-  const void* qd = q;
-  const void* knd = k_new;
-  const void* vnd = v_new;
-  void* outd = out;
-  if (host_io) {
-    void* q_dev = w + dec;
-    void* out_dev = w + dec + up(qb);
-    void* kn_dev = w + dec + 2 * up(qb);
-    void* vn_dev = w + dec + 2 * up(qb) + up(kb);
-    SA_CUDA(cudaMemcpyAsync(q_dev, q, qb, cudaMemcpyHostToDevice, st));
-    SA_CUDA(cudaMemcpyAsync(kn_dev, k_new, kb, cudaMemcpyHostToDevice, st));
-    SA_CUDA(cudaMemcpyAsync(vn_dev, v_new, kb, cudaMemcpyHostToDevice, st));
-    qd = q_dev;
-    knd = kn_dev;
-    vnd = vn_dev;
-    outd = out_dev;
+  // Replay one CUDA graph per argument set (copies and the three kernels in one launch); the
+  // legacy default stream and a stream that is already being captured take the direct path.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (st == nullptr || cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return step_enqueue(a, st);
   }
-  SA_TRY(sa_append_kv(knd, vnd, dtype, B, Hkv, T, d, k_cache, v_cache, L_stride, L - T, block, sketch, stream));
-  SA_TRY(sa_select_topk(SA_SELECT_SKETCH, qd, dtype, sketch, scores, B, T, Hq, Hkv, d, L, L_stride, block, 0, 0, k,
-                        0, 1, scale, idx, cnt, kmax, stream));
-  SA_TRY(sa_decode(qd, k_cache, v_cache, dtype, idx, cnt, kmax, B, T, Hq, Hkv, d, L, L_stride, block, scale, outd, w,
-                   dec, stream));
-  if (host_io) SA_CUDA(cudaMemcpyAsync(out, outd, qb, cudaMemcpyDeviceToHost, st));
+  int dev = 0;
+  SA_CUDA(cudaGetDevice(&dev));
+  const StepKey key = step_key(a, dev);
+  {
+    std::lock_guard<std::mutex> lk(g_step_mu);
+    for (auto& e : g_step_cache)
+      if (e.key == key) {
+        e.last_use = ++g_step_clock;
+        SA_CUDA(cudaGraphLaunch(e.exec, st));
+        return SA_OK;
+      }
+  }
+  SA_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+  const sa_status_t rc = step_enqueue(a, st);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(st, &graph);
+  if (rc != SA_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return rc;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (ec != cudaSuccess || graph == nullptr || cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    // not capturable (e.g. pageable host buffers): run the step directly
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return step_enqueue(a, st);
+  }
+  cudaGraphDestroy(graph);
+  {
+    std::lock_guard<std::mutex> lk(g_step_mu);
+    if (g_step_cache.size() >= kStepCacheMax) {
+      auto old = std::min_element(g_step_cache.begin(), g_step_cache.end(),
+                                  [](const StepGraph& x, const StepGraph& y) { return x.last_use < y.last_use; });
+      cudaGraphExecDestroy(old->exec);
+      g_step_cache.erase(old);
+    }
+    g_step_cache.push_back(StepGraph{key, exec, ++g_step_clock});
+  }
+  SA_CUDA(cudaGraphLaunch(exec, st));
   return SA_OK;
 }
 
