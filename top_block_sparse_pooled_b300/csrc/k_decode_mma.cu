@@ -30,10 +30,11 @@
 // shared by every kv head of that row ("How Much Dense Attention is
 // Necessary?" Sec. 2.2: one head-collapsed distribution selects the tokens
 // for all heads).  A unit is (group, chunk of 64 selected tokens); the
-// producer warp gathers the chunk's K and V rows with one 1-D bulk copy per
-// row into rows padded to 2*D + 16 bytes (ldmatrix stays conflict-free) and
-// records each row's key position for the causal mask; rows past the count
-// repeat the sink token with a position that no query sees.
+// producer warp gathers the chunk's K and V rows 16 bytes per lane and
+// instruction (cp.async, completion counted on the stage's mbarrier) into rows
+// padded to 2*D + 16 bytes (ldmatrix stays conflict-free) and records each
+// row's key position for the causal mask; rows past the count repeat the sink
+// token with a position that no query sees.
 #pragma once
 
 #include "sa_ptx.cuh"
@@ -128,6 +129,16 @@ struct DmParams {
   DmLayout lay;
 };
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the arrive-on that
+// fires on the mbarrier when all of this thread's earlier cp.async copies have
+// landed (.noinc: it is one of the barrier's expected arrivals).
+__device__ __forceinline__ void dm_cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void dm_cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void dm_sts_s32(uint32_t a, int v) {
   asm volatile("st.shared.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
@@ -165,7 +176,7 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, kTok ? 33 : 1);  // token mode: 32 copy arrivals + the producer's own
       mbar_init(empty0 + 8 * s, kDmConsumers);
     }
     fence_mbar_init();
@@ -223,14 +234,18 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
         tk[h] = valid ? t : 0;  // filler rows repeat token 0 (finite values, never visible)
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(2 * kDmBk * D * 2));
-      __syncwarp();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = lane + 32 * h;
-        bulk_g2s(kt + row * lay.rowb(), kg + static_cast<size_t>(tk[h]) * D, D * 2, full);
-        bulk_g2s(vt + row * lay.rowb(), vg + static_cast<size_t>(tk[h]) * D, D * 2, full);
+      if (lane == 0) mbar_arrive(full);  // releases the key positions written above
+      // 16-byte pieces: D/8 per row, K rows 0..63 then V rows; lane-strided
+      constexpr int kPpr = D / 8;
+#pragma unroll 4
+      for (int pc = lane; pc < 2 * kDmBk * kPpr; pc += 32) {
+        const int row = pc / kPpr, col = pc % kPpr, r64 = row & (kDmBk - 1);
+        const int t0 = __shfl_sync(0xFFFFFFFFu, tk[0], r64 & 31), t1 = __shfl_sync(0xFFFFFFFFu, tk[1], r64 & 31);
+        const int t = (r64 >> 5) ? t1 : t0;  // row r64's token is held by lane r64 % 32, in its half r64 / 32
+        const __nv_bfloat16* src = (row < kDmBk ? kg : vg) + static_cast<size_t>(t) * D + col * 8;
+        dm_cp_async16((row < kDmBk ? kt : vt) + r64 * lay.rowb() + col * 16, src);
       }
+      dm_cp_async_arrive(full);
       ++vi;
     }
     if (lane == 0)
