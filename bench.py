@@ -182,6 +182,23 @@ def cpu_oracle_decode(wl, x, budget_s):
 
 # ------------------------------------------------------------------ our arm
 
+def max_over_ranks(t_ms, device, world):
+    """The job's time is the slowest rank's (replicas run independent batches; no data-path
+    collective, only this reduction of the timing)."""
+    if world <= 1:
+        return float(t_ms)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(t_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_value(step_bytes_per_rank, world, ms_per_step):
+    """GB/s over all ranks: every rank moves step_bytes_per_rank per step (weak scaling)."""
+    return step_bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 def bench_decode(args, wl, rank, world):
     import numpy as np
     import torch
@@ -285,13 +302,9 @@ def bench_decode(args, wl, rank, world):
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    t_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1), dev, world)
     ms_per_step = t_ms / K
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_value(step_bytes, world, ms_per_step)
 
     # ---- per-kernel times, each from a CUDA graph of 4*R back-to-back calls
     def dec(s):
