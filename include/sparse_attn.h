@@ -343,6 +343,16 @@ sa_status_t sa_prefill_tokens(const void* q, const void* k, const void* v, int d
                               float scale, void* out, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Self-test of the failure path every pipeline kernel uses: one CTA waits on
+ * an mbarrier phase that nothing completes, gives up after limit_ns
+ * nanoseconds (1 ms .. 1 s), records SA_ERR_TIMEOUT in the device status word
+ * and returns; read it with sa_device_status.  The context stays usable.  The
+ * pages have no counterpart of this call; it exists so that the bounded-wait
+ * error reporting can be tested without faulting or hanging a GPU.
+ */
+sa_status_t sa_selftest_wait_timeout(long long limit_ns, void* stream);
+
+/*
  * One decode step: a1 append (k_new, v_new at cache rows L-T..L-1, sketch
  * refreshed), a2+a3 sketch selection with budget k, a4 decode.  If
  * host_io != 0, q, k_new, v_new and out are HOST pointers (pinned memory for

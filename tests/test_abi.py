@@ -158,6 +158,9 @@ def test_invalid_arguments_rejected_on_host(sa):
     st = L.sa_select_topk(sa.SA_SELECT_MASS, None, sa.SA_BF16, None, 16, 1, 262144, 1, 1, 128, 262144, 262144, 1, 128,
                           1, 8, 0, 1, 1.0, 16, 16, 2050, None)
     assert st == sa.SA_ERR_UNSUPPORTED
+    # the bounded-wait self-test rejects a limit outside [1 ms, 1 s] before any launch
+    assert L.sa_selftest_wait_timeout(5, None) == sa.SA_ERR_INVALID_ARG
+    assert L.sa_selftest_wait_timeout(5_000_000_000, None) == sa.SA_ERR_INVALID_ARG
     # device status needs an output pointer
     assert L.sa_device_status(None, 0) == sa.SA_ERR_INVALID_ARG
 

@@ -66,6 +66,7 @@ SIGNATURES = {
     "sa_token_mass_prefill": ([_vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "sa_prefill_tokens_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "sa_prefill_tokens": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "sa_selftest_wait_timeout": ([ctypes.c_longlong, _vp], _i),
     "sa_decode_step_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "sa_decode_step": ([_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _i,
                         _vp, _vp, _i, _vp, _sz, _vp], _i),
@@ -254,6 +255,11 @@ def sa_prefill_tokens(q, k, v, idx, cnt, scale, out, workspace, stream=None):
     kmax = idx.shape[-1]
     _check(lib.sa_prefill_tokens(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(idx), _ptr(cnt), kmax, B, L, Hq, Hkv,
                                  d, float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def sa_selftest_wait_timeout(limit_ns, stream=None):
+    """Launch the bounded-wait self-test (a wait that nothing completes, given up after limit_ns)."""
+    _check(lib.sa_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax) -> int:

@@ -39,6 +39,7 @@
 #include "k_score.cu"
 #include "k_sketch.cu"
 #include "k_tokmass.cu"
+#include "k_selftest.cu"
 
 namespace {
 
@@ -855,6 +856,14 @@ const char* sa_status_name(int s) {
     case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT";
     default: return "SA_UNKNOWN_STATUS";
   }
+}
+
+sa_status_t sa_selftest_wait_timeout(long long limit_ns, void* stream) {
+  t_err.clear();
+  SA_ARG(limit_ns >= 1000000 && limit_ns <= 1000000000LL, "limit_ns must be in [1e6, 1e9]");
+  sa::selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<unsigned long long>(limit_ns));
+  SA_CUDA(cudaGetLastError());
+  return SA_OK;
 }
 
 sa_status_t sa_device_status(int* code, int clear) {
