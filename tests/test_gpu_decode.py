@@ -181,9 +181,10 @@ def test_append_kv_updates_cache_and_sketch(sa):
     assert_close(got, ref, atol=1e-6, rtol=1e-5, what="sketch after append")
 
 
-@pytest.mark.parametrize("host_io", [False, True])
+@pytest.mark.parametrize("host_io", [False, True, "pageable"])
 def test_decode_step_matches_oracle(sa, host_io):
-    """append + select + decode in one call (device or pinned-host I/O)."""
+    """append + select + decode in one call: device I/O, pinned host I/O (new rows and the output
+    used in place), pageable host I/O (staged by copies)."""
     wl = DECODE_CASES["c2"].replace(B=2, L=8192)
     x = synth.make_inputs(wl)
     pos = wl.L - wl.T
@@ -202,10 +203,14 @@ def test_decode_step_matches_oracle(sa, host_io):
     k_new = kfull[:, :, pos:].permute(0, 2, 1, 3).contiguous()
     v_new = vfull[:, :, pos:].permute(0, 2, 1, 3).contiguous()
     out = torch.empty_like(q)
-    if host_io:
+    if host_io == "pageable":
+        q, k_new, v_new = (t.cpu() for t in (q, k_new, v_new))
+        out = torch.empty(q.shape, dtype=q.dtype)
+    elif host_io:
         q, k_new, v_new = (t.cpu().pin_memory() for t in (q, k_new, v_new))
         out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-    sa.sa_decode_step(q, k_new, v_new, kc, vc, sk, wl.L, wl.Bk, wl.k, wl.scale, idx, cnt, out, ws, host_io=host_io)
+    sa.sa_decode_step(q, k_new, v_new, kc, vc, sk, wl.L, wl.Bk, wl.k, wl.scale, idx, cnt, out, ws,
+                      host_io=bool(host_io))
     torch.cuda.synchronize()
     _check_status(sa)
     o_idx, o_cnt, o_s, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax)

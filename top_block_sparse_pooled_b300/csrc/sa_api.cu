@@ -1091,6 +1091,19 @@ size_t sa_decode_step_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int 
 
 namespace {
 
+// Device address of page-locked host memory mapped into the current device's address space
+// (cudaHostAlloc / cudaHostRegister with mapping, which unified addressing gives by default),
+// else nullptr (pageable memory, or memory the device cannot reach).
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+  return at.devicePointer;
+}
+
 // The step's copies and launches, in stream order (the body of sa_decode_step).
 sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
   auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
@@ -1103,18 +1116,35 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
   const void* knd = a.k_new;
   const void* vnd = a.v_new;
   void* outd = a.out;
+  bool out_mapped = false;
   if (a.host_io) {
+    // q is staged on the device (the selection reads it with bulk copies); k_new, v_new and out
+    // are used in place when they are page-locked host memory mapped into the device's address
+    // space (the append kernel reads them and the decode merge writes out with plain accesses),
+    // and staged by copies otherwise.
     void* q_dev = w + dec;
     void* out_dev = w + dec + up(qb);
     void* kn_dev = w + dec + 2 * up(qb);
     void* vn_dev = w + dec + 2 * up(qb) + up(kb);
     SA_CUDA(cudaMemcpyAsync(q_dev, a.q, qb, cudaMemcpyHostToDevice, st));
-    SA_CUDA(cudaMemcpyAsync(kn_dev, a.k_new, kb, cudaMemcpyHostToDevice, st));
-    SA_CUDA(cudaMemcpyAsync(vn_dev, a.v_new, kb, cudaMemcpyHostToDevice, st));
     qd = q_dev;
-    knd = kn_dev;
-    vnd = vn_dev;
-    outd = out_dev;
+    const void* kn_map = mapped_host(a.k_new);
+    const void* vn_map = mapped_host(a.v_new);
+    void* out_map = const_cast<void*>(mapped_host(a.out));
+    if (kn_map) {
+      knd = kn_map;
+    } else {
+      SA_CUDA(cudaMemcpyAsync(kn_dev, a.k_new, kb, cudaMemcpyHostToDevice, st));
+      knd = kn_dev;
+    }
+    if (vn_map) {
+      vnd = vn_map;
+    } else {
+      SA_CUDA(cudaMemcpyAsync(vn_dev, a.v_new, kb, cudaMemcpyHostToDevice, st));
+      vnd = vn_dev;
+    }
+    out_mapped = out_map != nullptr;
+    outd = out_mapped ? out_map : out_dev;
   }
   void* sp = static_cast<void*>(st);
   SA_TRY(sa_append_kv(knd, vnd, a.dtype, a.B, a.Hkv, a.T, a.d, a.k_cache, a.v_cache, a.L_stride, a.L - a.T, a.block,
@@ -1123,7 +1153,7 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
                         a.L_stride, a.block, 0, 0, a.k, 0, 1, a.scale, a.idx, a.cnt, a.kmax, sp));
   SA_TRY(sa_decode(qd, a.k_cache, a.v_cache, a.dtype, a.idx, a.cnt, a.kmax, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
                    a.L_stride, a.block, a.scale, outd, w, dec, sp));
-  if (a.host_io) SA_CUDA(cudaMemcpyAsync(a.out, outd, qb, cudaMemcpyDeviceToHost, st));
+  if (a.host_io && !out_mapped) SA_CUDA(cudaMemcpyAsync(a.out, outd, qb, cudaMemcpyDeviceToHost, st));
   return SA_OK;
 }
 
