@@ -285,9 +285,9 @@ def sa_decode_step(q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale
 
 class DecodeStep:
     """sa_decode_step with its arguments marshalled once, for a serving loop that calls the same
-    buffers every token: step() issues the call with the stored pointers and sizes.  The tensors must
-    stay alive, keep their shapes and stay where they are; their contents may change between calls.
-    The stream is fixed here (default: the current stream)."""
+    buffers every token: step() issues the call with the stored pointers and sizes, step(L) with a new
+    context length.  The tensors must stay alive, keep their shapes and stay where they are; their
+    contents may change between calls.  The stream is fixed here (default: the current stream)."""
 
     def __init__(self, q, k_new, v_new, k_cache, v_cache, sketch, L, block, k, scale, idx, cnt, out, workspace,
                  scores=None, host_io=False, stream=None):
@@ -296,7 +296,9 @@ class DecodeStep:
                                        out, workspace, scores, host_io, stream)
         self._fn = lib.sa_decode_step
 
-    def __call__(self):
+    def __call__(self, L=None):
+        if L is not None and L != self._args[12]:
+            self._args = self._args[:12] + (int(L),) + self._args[13:]
         status = self._fn(*self._args)
         if status != SA_OK:
             _check(status)

@@ -837,6 +837,7 @@ struct StepGraph {
 constexpr size_t kStepCacheMax = 32;
 std::mutex g_step_mu;
 std::vector<StepGraph> g_step_cache;
+std::vector<StepKey> g_step_seen;  // argument sets seen once (captured the second time)
 uint64_t g_step_clock = 0;
 
 }  // namespace
@@ -1174,8 +1175,9 @@ sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, 
   const StepArgs a{q, k_new, v_new, dtype, k_cache, v_cache, sketch, B, T, Hq, Hkv, d, L, L_stride, block, k,
                    scale, idx, cnt, kmax, scores, out, host_io, workspace, ws_bytes};
   cudaStream_t st = as_stream(stream);
-  // Replay one CUDA graph per argument set (copies and the three kernels in one launch); the
-  // legacy default stream and a stream that is already being captured take the direct path.
+  // Replay one CUDA graph per repeated argument set (copies and the three kernels in one launch);
+  // the first call with a set, the legacy default stream and a stream that is already being
+  // captured take the direct path.
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (st == nullptr || cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
     cudaGetLastError();
@@ -1192,6 +1194,15 @@ sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, 
         SA_CUDA(cudaGraphLaunch(e.exec, st));
         return SA_OK;
       }
+    // capture only argument sets that repeat: a loop whose context grows every token never
+    // pays for a capture
+    auto it = std::find(g_step_seen.begin(), g_step_seen.end(), key);
+    if (it == g_step_seen.end()) {
+      if (g_step_seen.size() >= 4 * kStepCacheMax) g_step_seen.erase(g_step_seen.begin());
+      g_step_seen.push_back(key);
+      return step_enqueue(a, st);
+    }
+    g_step_seen.erase(it);
   }
   SA_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
   const sa_status_t rc = step_enqueue(a, st);
