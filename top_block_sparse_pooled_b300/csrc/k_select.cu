@@ -28,10 +28,14 @@ constexpr int kSelWarps = kSelThreads / 32;
 
 constexpr int kTopkMaxN = 16384;  // candidates per selection (blocks per sequence)
 
+constexpr int kRankFinish = 64;  // rank the remaining keys once at most this many share the prefix
+
 struct TopkShared {
   uint32_t hist[4][256];     // one digit histogram per radix pass (8-bit digits, MSB first)
   uint32_t wdef[kSelWarps];  // per-warp count of selections decided without ties
   uint32_t weq[kSelWarps];   // per-warp count of candidates tied with the threshold key
+  uint32_t live[kRankFinish];  // rank finish: the keys still sharing the threshold's prefix
+  uint32_t nlive, fin_thr, fin_need;
 };
 
 // Shared-memory accesses by 32-bit shared-window address (explicit state space,
@@ -80,8 +84,12 @@ __device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
 // six block barriers in all.
 //
 // Threshold: exact MSB-first radix select of the take-th largest order-preserving
-// key (four 8-bit digit passes, each into its own 256-bin histogram; every warp
-// then finds the digit itself, so a pass costs one barrier).  Output: each warp
+// key (8-bit digit passes, each into its own 256-bin histogram; every warp then
+// finds the digit itself, so a pass costs one barrier).  As soon as at most
+// kRankFinish keys share the threshold's prefix, they are gathered and each
+// counts the keys above and equal to it: the one with count-above < remaining <=
+// count-above-or-equal is the threshold (two barriers instead of the remaining
+// passes).  Output: each warp
 // owns a contiguous span of indices, counts its keys above the threshold and its
 // ties, and after one barrier writes its selections at their ascending
 // positions; ties at the threshold are admitted in index order until the budget
@@ -91,6 +99,10 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
                                                 int32_t* __restrict__ cnt_out, uint32_t S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t hist = S + static_cast<uint32_t>(offsetof(TopkShared, hist));
+  const uint32_t live = S + static_cast<uint32_t>(offsetof(TopkShared, live));
+  const uint32_t nlive = S + static_cast<uint32_t>(offsetof(TopkShared, nlive));
+  const uint32_t fin_thr = S + static_cast<uint32_t>(offsetof(TopkShared, fin_thr));
+  const uint32_t fin_need = S + static_cast<uint32_t>(offsetof(TopkShared, fin_need));
   const uint32_t wdef = S + static_cast<uint32_t>(offsetof(TopkShared, wdef));
   const uint32_t weq = S + static_cast<uint32_t>(offsetof(TopkShared, weq));
   const int last = n - 1;                      // forced local / diagonal block
@@ -101,6 +113,7 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
   if (by_key) {
     for (int i = tid; i < 4 * 256 / 4; i += kSelThreads)
       asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(hist + 16u * i), "r"(0u) : "memory");
+    if (tid == 0) sts_u32(nlive, 0u);
     __syncthreads();
     uint32_t prefix = 0u, mask = 0u, remaining = static_cast<uint32_t>(take);
     for (int p = 0; p < 4; ++p) {
@@ -125,22 +138,68 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
         const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
         if (lane >= o) inc += y;
       }
-      uint32_t run = inc - sum, hit = 0u, dsel = 0u, rem = 0u;
+      uint32_t run = inc - sum, hit = 0u, dsel = 0u, rem = 0u, ceq = 0u;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         if (hit == 0u && run < remaining && remaining <= run + c[e]) {
           hit = 1u;
           dsel = 255u - 8u * static_cast<uint32_t>(lane) - static_cast<uint32_t>(e);
           rem = remaining - run;
+          ceq = c[e];
         }
         run += c[e];
       }
       const int src = (__ffs(__ballot_sync(0xFFFFFFFFu, hit != 0u)) - 1) & 31;
       dsel = __shfl_sync(0xFFFFFFFFu, dsel, src);
       rem = __shfl_sync(0xFFFFFFFFu, rem, src);
+      ceq = __shfl_sync(0xFFFFFFFFu, ceq, src);
       prefix |= dsel << shift;
       mask |= 255u << shift;
       remaining = rem;
+      if (p < 3 && ceq <= static_cast<uint32_t>(kRankFinish)) {
+        // rank finish: gather the ceq keys that share the prefix (warp-aggregated slots) ...
+        for (int base = 0; base < n; base += kSelThreads) {  // same trip count in every lane
+          const int b = base + tid;
+          const uint32_t key = (b >= 1 && b < last) ? float_key(score(b)) : 0u;
+          const bool in = b >= 1 && b < last && (key & mask) == prefix;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, in);
+          uint32_t slot0 = 0u;
+          if (lane == 0 && bal != 0u) {
+            asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(slot0) : "r"(nlive), "r"(__popc(bal)) : "memory");
+          }
+          slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+          if (in) sts_u32(live + 4u * (slot0 + __popc(bal & ((1u << lane) - 1u))), key);
+        }
+        __syncthreads();
+        // ... and the key with count-above < remaining <= count-above-or-equal is the threshold
+        if (tid < static_cast<int>(ceq)) {
+          const uint32_t kt = lds_u32(live + 4u * tid);
+          uint32_t above = 0u, same = 0u;
+          for (uint32_t j0 = 0; j0 < ceq; j0 += 16) {  // sixteen keys per round: four loads, then compares
+            uint4 x[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) x[v] = lds_u32x4(live + 4u * (j0 + 4u * v));
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t xv[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const bool ok = j0 + 4u * v + i < ceq;  // entries past ceq are stale
+                above += (ok && xv[i] > kt) ? 1u : 0u;
+                same += (ok && xv[i] == kt) ? 1u : 0u;
+              }
+            }
+          }
+          if (above < remaining && remaining <= above + same) {  // every such thread writes the same pair
+            sts_u32(fin_thr, kt);
+            sts_u32(fin_need, remaining - above);
+          }
+        }
+        __syncthreads();
+        prefix = lds_u32(fin_thr);
+        remaining = lds_u32(fin_need);
+        break;
+      }
     }
     thr = prefix;
     need_eq = remaining;  // ties at the threshold key to admit, lowest indices first
