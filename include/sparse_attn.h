@@ -44,11 +44,13 @@
  * launch and returns SA_ERR_INVALID_ARG / SA_ERR_UNSUPPORTED without touching
  * the device when they are bad; sa_last_error() then gives a message.  Calls
  * are asynchronous: they enqueue work on `stream` (a cudaStream_t; NULL = the
- * legacy default stream) and return.  The library allocates no device memory:
- * scratch space is passed in as `workspace` (sizes from the *_workspace_bytes
- * queries).  Kernels that wait on the tensor-memory-access (TMA) engine bound
- * every wait; a wait that gives up records SA_ERR_TIMEOUT in a device-side
- * status word that sa_device_status() reads.
+ * legacy default stream) and return.  The library allocates no device memory
+ * of its own: scratch space is passed in as `workspace` (sizes from the
+ * *_workspace_bytes queries).  Two exceptions, documented at their calls: the
+ * fixed scratch array of sa_decode_noalloc and the CUDA graphs that
+ * sa_decode_step keeps for repeated argument sets.  Kernels bound every wait
+ * (on copies, on other warps); a wait that gives up records SA_ERR_TIMEOUT in
+ * a device-side status word that sa_device_status() reads.
  */
 #ifndef SPARSE_ATTN_H
 #define SPARSE_ATTN_H
@@ -355,14 +357,20 @@ sa_status_t sa_selftest_wait_timeout(long long limit_ns, void* stream);
 /*
  * One decode step: a1 append (k_new, v_new at cache rows L-T..L-1, sketch
  * refreshed), a2+a3 sketch selection with budget k, a4 decode.  If
- * host_io != 0, q, k_new, v_new and out are HOST pointers (pinned memory for
- * asynchronous copies): the step copies the inputs to the device staging
- * area in `workspace`, runs, and copies `out` back, all on `stream`.
- * Otherwise they are device pointers.  sketch, caches, idx, cnt, scores
- * (optional) are device memory as above.  workspace: >=
- * sa_decode_step_workspace_bytes(...) bytes of device memory, zero-filled
- * before first use exactly as for sa_decode (its head is sa_decode's
- * workspace).
+ * host_io != 0, q, k_new, v_new and out are HOST pointers: q is copied to
+ * the device staging area in `workspace`; k_new, v_new and out are read and
+ * written in place by the kernels when they are page-locked memory mapped
+ * into the device's address space (cudaHostAlloc, or pinned memory under
+ * unified addressing), and staged by copies otherwise (pageable memory: the
+ * copies are then synchronous).  Otherwise they are device pointers.
+ * sketch, caches, idx, cnt, scores (optional) are device memory as above.
+ * workspace: >= sa_decode_step_workspace_bytes(...) bytes of device memory,
+ * zero-filled before first use exactly as for sa_decode (its head is
+ * sa_decode's workspace).
+ * On a stream other than the legacy default stream, an argument set that
+ * repeats (same pointers and sizes) is captured into a CUDA graph on its
+ * second call and replayed with one launch afterwards (at most 32 graphs,
+ * least recently used evicted); buffer contents may change between calls.
  */
 size_t sa_decode_step_workspace_bytes(int B, int T, int Hq, int Hkv, int d, int dtype, int kmax);
 sa_status_t sa_decode_step(const void* q, const void* k_new, const void* v_new, int dtype,
