@@ -158,6 +158,33 @@ def test_invalid_arguments_rejected_on_host(sa):
     st = L.sa_select_topk(sa.SA_SELECT_MASS, None, sa.SA_BF16, None, 16, 1, 262144, 1, 1, 128, 262144, 262144, 1, 128,
                           1, 8, 0, 1, 1.0, 16, 16, 2050, None)
     assert st == sa.SA_ERR_UNSUPPORTED
+    # per-query prefill: L past the grid limit, fp32, a short workspace, G > 16 for the token prefill
+    st = L.sa_token_mass_prefill(16, 16, sa.SA_BF16, 1, 70000, 8, 2, 128, 0.1, 16, 16, 1 << 40, None)
+    assert st == sa.SA_ERR_INVALID_ARG
+    st = L.sa_token_mass_prefill(16, 16, sa.SA_F32, 1, 64, 8, 2, 128, 0.1, 16, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_UNSUPPORTED
+    st = L.sa_token_mass_prefill(16, 16, sa.SA_BF16, 1, 64, 8, 2, 128, 0.1, 16, 16, 64, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"workspace" in L.sa_last_error()
+    st = L.sa_prefill_tokens(16, 16, 16, sa.SA_BF16, 16, 16, 8, 1, 64, 64, 2, 128, 0.1, 16, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_UNSUPPORTED  # G = 32 > 16
+    st = L.sa_prefill_tokens(16, 16, 16, sa.SA_BF16, 16, 16, 8, 1, 64, 8, 2, 128, 0.1, 16, 16, 64, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"workspace" in L.sa_last_error()
+    st = L.sa_prefill_tokens(16, 16, 16, sa.SA_BF16, 16, 16, 8, 1 << 20, 1 << 20, 8, 2, 128, 0.1, 16, 16, 1 << 30,
+                             None)
+    assert st == sa.SA_ERR_INVALID_ARG  # B*L*Hkv past 2^24
+    # workspace queries of the token paths grow with their inputs and reject bad shapes
+    assert sa.sa_token_mass_prefill_workspace_bytes(1, 4096, 32, 8) > sa.sa_token_mass_prefill_workspace_bytes(1, 2048,
+                                                                                                               32, 8)
+    assert sa.sa_token_mass_prefill_workspace_bytes(1, 4096, 32, 7) == 0
+    assert sa.sa_prefill_tokens_workspace_bytes(1, 4096, 32, 8, 128, 258) > 0
+    assert sa.sa_token_mass_workspace_bytes(1, 4, 32, 8, 262144) >= 8 * 16 * 262144 * 4
+    # the decode step rejects null buffers and a short workspace before any launch
+    st = L.sa_decode_step(None, 16, 16, sa.SA_BF16, 16, 16, 16, 8, 1, 32, 8, 128, 32768, 32768, 64, 32, 0.08, 16, 16,
+                          34, None, 16, 0, 16, 1 << 30, None)
+    assert st == sa.SA_ERR_INVALID_ARG
+    st = L.sa_decode_step(16, 16, 16, sa.SA_BF16, 16, 16, 16, 8, 1, 32, 8, 128, 32768, 32768, 64, 32, 0.08, 16, 16,
+                          34, None, 16, 0, 16, 64, None)
+    assert st == sa.SA_ERR_INVALID_ARG and b"workspace" in L.sa_last_error()
     # the bounded-wait self-test rejects a limit outside [1 ms, 1 s] before any launch
     assert L.sa_selftest_wait_timeout(5, None) == sa.SA_ERR_INVALID_ARG
     assert L.sa_selftest_wait_timeout(5_000_000_000, None) == sa.SA_ERR_INVALID_ARG
