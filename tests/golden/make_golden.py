@@ -38,9 +38,32 @@ def c1_decode_lines():
     return lines
 
 
+def c1_token_decode_lines():
+    """Head-collapsed token-level support on the small decode workload at 512 tokens
+    ("How Much Dense Attention is Necessary?" Sec. 2.1-2.2): the mass of the selected
+    tokens, the selection (top-32 + tokens 0 and 511) and the outputs over it."""
+    wl = synth.WORKLOADS["c1"].replace(L=512, k=32)
+    x = synth.make_inputs(wl)
+    P = oracle.token_mass_decode(x.q, x.k, wl.Hkv, wl.L, wl.scale)
+    idx, cnt = oracle.token_select(P, wl.k)
+    sel = idx[0, : cnt[0]]
+    rows = [(0, 0, h) for h in range(wl.Hq)]
+    out, lse = oracle.token_attend(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, idx, cnt, rows)
+    lines = ["# c1 token decode: B=1 T=1 Hq=4 Hkv=1 d=64 L=512, top-32 tokens + 0 + 511, fp32, seed %d" % wl.seed,
+             "selected " + " ".join(str(j) for j in sel),
+             "mass " + " ".join("%.17g" % P[0, j] for j in sel),
+             "masssum %.17g" % P[0].sum()]
+    for h in range(wl.Hq):
+        lines.append("lse %d %.17g" % (h, lse[h]))
+        lines.append("out %d " % h + " ".join("%.17g" % v for v in out[h]))
+    return lines
+
+
 def main():
     with open(os.path.join(HERE, "c1_decode.txt"), "w") as f:
         f.write("\n".join(c1_decode_lines()) + "\n")
+    with open(os.path.join(HERE, "c1_token_decode.txt"), "w") as f:
+        f.write("\n".join(c1_token_decode_lines()) + "\n")
 
 
 if __name__ == "__main__":
