@@ -199,7 +199,10 @@ def whole_job_value(step_bytes_per_rank, world, ms_per_step):
     return step_bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
 
 
-def bench_decode(args, wl, rank, world):
+def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=None):
+    """One decode workload as whole steps (append + select + decode), CUDA graphs over `rotate`
+    resident input sets; per-kernel times, the decode kernel's roofline, the end-to-end leg through
+    the C ABI with pinned host buffers, and (rank 0) the CPU oracle on a bounded sample."""
     import numpy as np
     import torch
 
@@ -210,7 +213,9 @@ def bench_decode(args, wl, rank, world):
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
     x = synth.make_inputs(wl.replace(seed=wl.seed + 100 * rank))
-    R = args.rotate
+    R = rotate or args.rotate
+    steps = steps or args.steps
+    cpu_seconds = args.cpu_seconds if cpu_seconds is None else cpu_seconds
     bf = wl.dtype == "bf16"
 
     def up(a):
@@ -275,7 +280,7 @@ def bench_decode(args, wl, rank, world):
 
     # the step as CUDA graphs: R consecutive steps over the R input sets
     g_full = capture([lambda s=s: step(s) for s in sets])
-    K = args.steps
+    K = steps
     rem = K % R
     g_rem = capture([lambda s=s: step(s) for s in sets[:rem]]) if rem else None
     with torch.cuda.stream(stream):
@@ -401,12 +406,12 @@ def bench_decode(args, wl, rank, world):
         "gpu_launches": K * (3 if bf and wl.G * wl.T <= 16 else 4),
         "clocks": clocks,
     }
-    if rank == 0 and args.cpu_baseline:
-        gbs, cores, sample = cpu_oracle_decode(wl, x, args.cpu_seconds)
+    if rank == 0 and args.cpu_baseline and cpu_seconds > 0:
+        gbs, cores, sample = cpu_oracle_decode(wl, x, cpu_seconds)
         res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                "sample": sample}
-    traffic = os.path.join(ROOT, "profiles", "decode_c2_traffic.txt")
-    if os.path.exists(traffic) and wl.name == "c2" and bf and wl.G * wl.T <= 16:
+    traffic = os.path.join(ROOT, "profiles", "decode_%s_traffic.txt" % wl.name)
+    if os.path.exists(traffic) and bf and wl.G * wl.T <= 16:
         try:
             t = {}
             for line in open(traffic):
@@ -418,6 +423,15 @@ def bench_decode(args, wl, rank, world):
         except Exception:
             pass
     return res
+
+
+def _leg_summary(r):
+    """A secondary decode workload's result, without the keys that only the headline line carries."""
+    keep = ("value", "unit", "ms_per_step", "steps", "dtype", "config", "pct_hbm_peak", "roofline", "e2e",
+            "kernels_us", "gpu_launches", "clocks", "cpu_baseline")
+    out = {k: r[k] for k in keep if k in r}
+    out["metric"] = r["metric"]
+    return out
 
 
 def _events_ms(fn, reps, stream):
@@ -799,6 +813,8 @@ def main():
     ap.add_argument("--rotate", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-decode-legs", dest="decode_legs", action="store_false",
+                    help="skip the c3 / c1 decode legs after the headline workload")
     ap.add_argument("--prefill-steps", type=int, default=5,
                     help="steps of each prefill leg (c5 sketch-selected, c4 oracle-mass); 0 skips them")
     ap.add_argument("--prefill-only", action="store_true", help="run only the prefill legs (profiling)")
@@ -849,6 +865,16 @@ def main():
             res = {"prefill": [bench_prefill(pf_wl(n), max(1, args.prefill_steps), peaks, src) for n in ("c5", "c4")]}
         else:
             res = bench_decode(args, wl, rank, world)
+            if args.decode_legs and res is not None:
+                # the other decode workloads, same step definition: c3 (256K context, 4 query tokens)
+                # and c1 (fp32, 4K context; 128 rotated sets so that no step finds its blocks in L2)
+                res["decode_legs"] = []
+                for name, rot in (("c3", 8), ("c1", 128)):
+                    if name == wl.name:
+                        continue
+                    leg = bench_decode(args, workload(name), rank, world, steps=min(args.steps, 4000), rotate=rot,
+                                       cpu_seconds=min(args.cpu_seconds, 8.0))
+                    res["decode_legs"].append(_leg_summary(leg))
             if args.prefill_steps > 0 and res is not None:
                 peaks, src = load_peaks()
                 res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src) for n in ("c5", "c4")]

@@ -210,6 +210,32 @@ sa_status_t sa_decode(const void* q, const void* k_cache, const void* v_cache, i
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * a2 + a3 + a4, decode, in one launch: the sketch scoring and top-k selection
+ * of sa_select_topk (SKETCH mode, decode) followed by the attention of
+ * sa_decode over the blocks just selected ("How Much Dense Attention is
+ * Necessary?" Sec. 2.1-2.2: score, keep the top-k, recompute exact attention on
+ * them; "Faster Than Flash" Sec. 1-3: one pass that scans the block summaries
+ * and then reads only the selected blocks).  One cluster of CTAs per
+ * (batch, kv-head) group: the CTAs score slices of the group's sketch, CTA 0
+ * of the cluster selects, each CTA attends over a share of the selected blocks,
+ * and the partials merge exactly through distributed shared memory.
+ *
+ * Arguments and layouts are those of sa_select_topk (q [B, T, Hq, d], sketch
+ * [B, Hkv, ceil(L_stride/block), d] fp32, idx [B, Hkv, kmax] and cnt [B, Hkv]
+ * written, scores [B, Hkv, ceil(L/block)] written when not NULL) and of
+ * sa_decode (k/v caches [B, Hkv, L_stride, d], out [B, T, Hq, d]); the
+ * selection and the output equal those of the two separate calls.  No
+ * workspace.  Requires dtype SA_BF16, d in {64, 128}, block == 64,
+ * G*T <= 16, T <= block, at most 16384 blocks; returns SA_ERR_UNSUPPORTED
+ * otherwise (use the two separate calls).  Invalid arguments return
+ * SA_ERR_INVALID_ARG before any launch.
+ */
+sa_status_t sa_select_decode(const void* q, int dtype, const float* sketch, const void* k_cache,
+                             const void* v_cache, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
+                             int block, int k, float scale, int32_t* idx, int32_t* cnt, int kmax,
+                             float* scores, void* out, void* stream);
+
+/*
  * sa_decode without a workspace argument, for callers that cannot allocate
  * device memory: code embedded in a host runtime that owns the whole device
  * memory pool and gives its plugins no allocation hook, or a latency-critical
@@ -225,7 +251,10 @@ sa_status_t sa_decode(const void* q, const void* k_cache, const void* v_cache, i
  *
  * The first call made with a given device current looks up the array's device
  * address on that device (cudaGetSymbolAddress); make that first call before
- * any stream capture.  Each call clears the arrival counters at the head of
+ * any stream capture.  The address is cached with the device's CUDA context;
+ * a call made in a new context of the device (after cudaDeviceReset) looks it
+ * up again, so that first call in the new context also belongs before any
+ * capture.  Each call clears the arrival counters at the head of
  * the array on `stream`, then runs the same kernels as sa_decode.  All calls
  * share the one array: calls that overlap on the device (on different streams,
  * or from several host threads without ordering) race on it and give wrong

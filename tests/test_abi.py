@@ -185,6 +185,25 @@ def test_invalid_arguments_rejected_on_host(sa):
     st = L.sa_decode_step(16, 16, 16, sa.SA_BF16, 16, 16, 16, 8, 1, 32, 8, 128, 32768, 32768, 64, 32, 0.08, 16, 16,
                           34, None, 16, 0, 16, 64, None)
     assert st == sa.SA_ERR_INVALID_ARG and b"workspace" in L.sa_last_error()
+    # fused selection + decode: shapes outside the cluster kernel, a short kmax, null caches
+    sd = [16, sa.SA_BF16, 16, 16, 16, 8, 1, 32, 8, 128, 32768, 32768, 64, 32, 0.088, 16, 16, 34, None, 16, None]
+    bad = list(sd)
+    bad[1] = sa.SA_F32
+    assert L.sa_select_decode(*bad) == sa.SA_ERR_UNSUPPORTED
+    bad = list(sd)
+    bad[6] = 8  # T = 8: G*T = 32
+    bad[17] = 34
+    assert L.sa_select_decode(*bad) == sa.SA_ERR_UNSUPPORTED and b"G*T" in L.sa_last_error()
+    bad = list(sd)
+    bad[12] = 128  # block 128
+    bad[17] = 34
+    assert L.sa_select_decode(*bad) == sa.SA_ERR_UNSUPPORTED
+    bad = list(sd)
+    bad[17] = 33  # kmax below the selection's 34
+    assert L.sa_select_decode(*bad) == sa.SA_ERR_INVALID_ARG and b"kmax" in L.sa_last_error()
+    bad = list(sd)
+    bad[3] = None  # no key cache
+    assert L.sa_select_decode(*bad) == sa.SA_ERR_INVALID_ARG and b"null" in L.sa_last_error()
     # the bounded-wait self-test rejects a limit outside [1 ms, 1 s] before any launch
     assert L.sa_selftest_wait_timeout(5, None) == sa.SA_ERR_INVALID_ARG
     assert L.sa_selftest_wait_timeout(5_000_000_000, None) == sa.SA_ERR_INVALID_ARG

@@ -112,3 +112,37 @@ def test_decode_topdelta_matches_oracle(sa, name):
         if delta >= 1e6:  # no threshold: the top-k selection
             t_idx, t_cnt, _, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax, sketch=sketch)
             assert np.array_equal(o_idx, t_idx) and np.array_equal(o_cnt, t_cnt)
+
+
+@pytest.mark.parametrize("n", [258, 259, 300, 512, 514, 1000, 4096, 16384])
+def test_select_small_budgets_patterns(sa, n):
+    """Budgets far below the candidate count (the decode regime), on score patterns that
+    stress a sampled threshold: exact ties everywhere, all equal, sorted ascending and
+    descending, a few large outliers, and random; bit-exact against the oracle."""
+    rng = np.random.default_rng(1000 + n)
+    pats = [
+        rng.integers(-4, 5, size=n).astype(np.float32) * 0.25,   # heavy ties
+        np.ones(n, dtype=np.float32),                             # all equal
+        np.arange(n, dtype=np.float32),                           # ascending: the top is at the end
+        -np.arange(n, dtype=np.float32),                          # descending: the top is at the start
+        np.where(rng.random(n) < 0.01, 10.0, rng.standard_normal(n)).astype(np.float32),  # needles
+        rng.standard_normal(n).astype(np.float32),
+    ]
+    s = np.stack(pats)
+    groups = s.shape[0]
+    for k in (1, 7, 32, 80, 128, 200):
+        kmax = sa.sa_select_kmax(n, 1, 0, False, k)
+        scores = torch.from_numpy(np.ascontiguousarray(s.reshape(1, groups, 1, n))).cuda()
+        idx = torch.full((1, groups, 1, kmax), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((1, groups, 1), -7, dtype=torch.int32, device="cuda")
+        sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, scores, groups, n, n, 1, 0, False, k, 0, 1, 1.0,
+                          idx, cnt, d=128, dtype=sa.SA_BF16, B=1, Tq=1, Hq=groups)
+        torch.cuda.synchronize()
+        assert sa.sa_device_status(clear=True) == 0
+        o_idx, o_cnt = oracle.select(s.astype(np.float64), n, n - 1, k, kmax)
+        g_idx = idx.cpu().numpy().reshape(groups, kmax)
+        g_cnt = cnt.cpu().numpy().reshape(groups)
+        for g in range(groups):
+            assert g_cnt[g] == o_cnt[g] and np.array_equal(g_idx[g], o_idx[g]), (
+                "n=%d k=%d pattern %d: gpu %s (cnt %d), oracle %s (cnt %d)" % (
+                    n, k, g, g_idx[g][:12].tolist(), g_cnt[g], o_idx[g][:12].tolist(), o_cnt[g]))

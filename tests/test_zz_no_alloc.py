@@ -61,11 +61,13 @@ def test_noalloc_rejects_oversized_problem(sa):
     """A problem needing more scratch than the fixed array is refused on the host."""
     B, T, Hq, Hkv, d, kmax = 64, 1, 32, 8, 128, 512
     assert sa.sa_decode_workspace_bytes(B, T, Hq, Hkv, d, kmax) > (8 << 20)
-    q = torch.zeros((B, T, Hq, d), dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros((B, Hkv, 64 * 512, d), dtype=torch.bfloat16, device="cuda")
-    idx = torch.zeros((B, Hkv, 1, kmax), dtype=torch.int32, device="cuda")
-    cnt = torch.zeros((B, Hkv, 1), dtype=torch.int32, device="cuda")
-    out = torch.empty_like(q)
+    # the shapes the binding passes are the oversized problem's; the memory behind them is a few
+    # bytes (broadcast views), since the call is refused before it reads any of it
+    q = torch.zeros((1, 1, 1, d), dtype=torch.bfloat16, device="cuda").expand(B, T, Hq, d)
+    kc = torch.zeros((1, 1, 1, d), dtype=torch.bfloat16, device="cuda").expand(B, Hkv, 64 * 512, d)
+    idx = torch.zeros((1, 1, 1, 1), dtype=torch.int32, device="cuda").expand(B, Hkv, 1, kmax)
+    cnt = torch.zeros((1, 1, 1), dtype=torch.int32, device="cuda").expand(B, Hkv, 1)
+    out = torch.zeros((1, 1, 1, d), dtype=torch.bfloat16, device="cuda").expand(B, T, Hq, d)
     with pytest.raises(sa.SparseAttnError) as e:
         sa.sa_decode_noalloc(q, kc, kc, idx, cnt, 64 * 512, 64, 0.088, out)
     assert e.value.status == sa.SA_ERR_INVALID_ARG and "scratch" in str(e.value)

@@ -54,6 +54,8 @@ SIGNATURES = {
     "sa_budget_sublinear": ([_i, _i, _i, _i, _f], _i),
     "sa_decode_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "sa_decode": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "sa_select_decode": ([_vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _i, _vp, _vp,
+                          _vp], _i),
     "sa_decode_noalloc": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "sa_prefill": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp], _i),
     "sa_oracle_mass_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
@@ -176,6 +178,18 @@ def sa_decode(q, k_cache, v_cache, idx, cnt, L, block, scale, out, workspace, st
     _check(lib.sa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(q), _ptr(idx), _ptr(cnt), kmax, B, T, Hq, Hkv,
                          d, L, Ls, block, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
                          _stream(stream)))
+
+
+def sa_select_decode(q, sketch, k_cache, v_cache, L, block, k, scale, idx, cnt, out, scores=None, stream=None):
+    """Sketch selection + sparse decode in one launch.  q, out: [B, T, Hq, d] bf16; sketch
+    [B, Hkv, nb_cap, d] float32; caches [B, Hkv, L_stride, d]; idx [B, Hkv, 1, kmax] and cnt [B, Hkv, 1]
+    int32 (written); scores [B, Hkv, 1, nb] float32 or None (written)."""
+    B, T, Hq, d = q.shape
+    Hkv, Ls = k_cache.shape[1], k_cache.shape[2]
+    kmax = idx.shape[-1]
+    _check(lib.sa_select_decode(_ptr(q), _dtype(q), _ptr(sketch), _ptr(k_cache), _ptr(v_cache), B, T, Hq, Hkv, d, L,
+                                Ls, block, k, float(scale), _ptr(idx), _ptr(cnt), kmax, _ptr(scores), _ptr(out),
+                                _stream(stream)))
 
 
 def sa_decode_noalloc(q, k_cache, v_cache, idx, cnt, L, block, scale, out, stream=None):

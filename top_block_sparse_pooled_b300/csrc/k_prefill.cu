@@ -12,13 +12,13 @@
 // has up to i + 1 causal blocks) and dealt round-robin to a persistent grid of
 // one CTA per SM.
 //
-// Roles (384 threads):
+// Roles (320 threads, kPfThreads):
 //   warp 0    TMA producer: the unit's Q tiles (3-D map: d, head, row), then
 //             the K and V tiles of each selected block into 2-stage rings.
 //   warp 1    TMEM allocator and MMA issuer (one thread):
 //               S_t = Q_t K^T  (M=128, N=128 keys, K=d; both K-major in smem)
 //               O_t += P_t V   (A = P_t from TMEM, B = V MN-major in smem)
-//   warps 4-7, 8-11  softmax warpgroup t = 0, 1: thread r owns query row r of
+//   warps 2-5, 6-9   softmax warpgroup t = 0, 1: thread r owns query row r of
 //             M tile t (= TMEM lane r).  It reads its S row from TMEM, masks
 //             (causal on the diagonal block, keys past L), keeps the running
 //             max m and sum l (base 2), writes P = exp2(S - m) as bf16 pairs

@@ -1,0 +1,556 @@
+// k_seldec.cu -- sparse decode by clusters of CTAs, one (batch, kv-head) group
+// per cluster, optionally with the block selection fused in front of it.
+//
+// "How Much Dense Attention is Necessary?" Sec. 2.1-2.2: score the blocks, keep
+// the top-k, recompute exact attention with the original q, k, v on the kept
+// blocks.  "Faster Than Flash" Sec. 1-3: the scan of the small block summaries
+// and the reads of the selected blocks run in one pass over memory.  "Pulsar
+// Attention" Phase 2: partial softmaxes over disjoint key sets merge exactly.
+//
+// Work split: cluster c handles groups c, c + clusters, ...; its CS CTAs split
+// each group's work.  Per group:
+//   S (with selection)  CTA rank r scores sketch rows [r*per, r*per + per) in
+//                       64-row chunks (tensor-core product of the fp32 sketch,
+//                       split into three bf16 parts, with the group's bf16 query
+//                       rows; float32-level scores) and stores them into CTA
+//                       rank 0's shared memory (distributed shared memory).
+//   K                   rank 0 selects the top-k blocks (forced sink and local
+//                       block, ties to the lower index) into its shared memory
+//                       and writes idx / cnt; every CTA then reads its share of
+//                       the list, the selected blocks at positions r, r + CS, ...
+//                       (without selection, the share is read from idx / cnt).
+//   A                   the CTA streams its blocks' K and V tiles and keeps an
+//                       online softmax per query row; its partial (max, sum,
+//                       unnormalised output rows) goes to its shared memory.
+//   merge               after a cluster barrier, each CTA combines a slice of
+//                       the output rows from all CS partials (exact rescaling)
+//                       and writes it; a last cluster barrier keeps every
+//                       partial alive until it has been read.
+//
+// Roles (288 threads): warps 0-7 consumers in two quads (quad q takes the ring
+// stages of sequence numbers v with v % 2 == q, so the two quads work on
+// alternate blocks; the four warps of a quad split a block's 64 keys, or a
+// sketch chunk's four 16-row M tiles); warp 8 is the producer: lane 0 issues
+// the TMA copies (sketch chunks, then K / V tiles) into a ring of an even
+// number of stages guarded by full / empty mbarriers.  The top-k runs on the
+// 256 consumer threads of rank 0.
+//
+// Waits are bounded (sa_ptx.cuh); after a give-up the roles run out their loops
+// without waiting, every thread still reaches every barrier, the producer
+// drains its copies, and the kernel returns with SA_ERR_TIMEOUT recorded.
+#pragma once
+
+#include "sa_ptx.cuh"
+
+namespace sa {
+
+constexpr int kSdQuads = 2;
+constexpr int kSdConsumers = 4 * kSdQuads;
+constexpr int kSdThreads = (kSdConsumers + 1) * 32;
+constexpr int kSdBk = 64;            // keys per block; sketch rows per chunk
+constexpr int kSdRmax = 16;          // query rows per group (G * T)
+
+// Shared-memory layout (runtime, from a 1024-aligned base).  A ring stage holds
+// one block's K and V tiles (64 rows of 2*D bytes each, 128-byte swizzle) or one
+// 64-row chunk of the fp32 sketch (4*D bytes per row, 128-byte swizzle): the
+// same number of bytes.
+struct SdLayout {
+  int nstages, D, nb, kmax, sel;
+  __host__ __device__ int stage_bytes() const { return 2 * kSdBk * D * 2; }
+  __host__ __device__ int q_off() const { return nstages * stage_bytes(); }
+  __host__ __device__ int all_off() const { return q_off() + kSdRmax * D * 2; }
+  __host__ __device__ int topk_off() const { return all_off() + (sel ? ((nb * 4 + 15) / 16) * 16 : 0); }
+  __host__ __device__ int sel_off() const {
+    return topk_off() + (sel ? static_cast<int>(((sizeof(TopkShared) + 15) / 16) * 16) : 0);
+  }
+  __host__ __device__ int list_off() const { return sel_off() + ((kmax * 4 + 4 + 15) / 16) * 16; }
+  __host__ __device__ int mlw_off() const { return list_off() + ((kmax * 4 + 15) / 16) * 16; }
+  __host__ __device__ int octa_off() const { return mlw_off() + kSdConsumers * kSdRmax * 8; }
+  __host__ __device__ int mlc_off() const { return octa_off() + kSdRmax * D * 4; }
+  __host__ __device__ int misc_off() const { return mlc_off() + kSdRmax * 8; }
+  __host__ __device__ int bar_off() const { return misc_off() + 16; }
+  __host__ __device__ int bytes() const { return bar_off() + (2 * nstages + 1) * 8 + 1024; }
+};
+
+struct SdParams {
+  const __nv_bfloat16* q;  // [B, T, Hq, D]
+  int32_t* idx;            // [groups, kmax]: written (with selection) or read
+  int32_t* cnt;            // [groups]
+  float* scores;           // optional [groups, nb] (with selection)
+  __nv_bfloat16* out;      // [B, T, Hq, D]
+  int kmax, k, T, Hq, Hkv, G, R, L, Ls, nb, nb_cap, groups;
+  int per;      // sketch rows per CTA (a multiple of 64)
+  float scale;  // score scale (the softmax scale)
+  float qscale;  // softmax scale * log2(e)
+  SdLayout lay;
+};
+
+__device__ __forceinline__ void bar_named(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// grid (CS, clusters), cluster (CS, 1, 1), kSdThreads threads, one CTA per SM.
+template <int D, bool kSel>
+__global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                const __grid_constant__ CUtensorMap vmap,
+                                                                const __grid_constant__ CUtensorMap skmap,
+                                                                const SdParams p) {
+  using C = DmCfg<D>;
+  constexpr int kBoxes = D * 4 / 128;  // 128-byte boxes per fp32 sketch row
+  constexpr uint32_t kStageBytes = 2 * kSdBk * D * 2;
+  extern __shared__ __align__(1024) uint8_t smem_sd[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_sd) + 1023) & ~uintptr_t(1023));
+  const SdLayout& lay = p.lay;
+  const int NS = lay.nstages;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t q_sh = sbase + lay.q_off();
+  const uint32_t all = sbase + lay.all_off();
+  const uint32_t topk_s = sbase + lay.topk_off();
+  const uint32_t sel_sh = sbase + lay.sel_off();  // rank 0: [kmax] selection, then its count
+  int32_t* sel_ptr = reinterpret_cast<int32_t*>(smem + lay.sel_off());
+  int32_t* list = reinterpret_cast<int32_t*>(smem + lay.list_off());  // this CTA's blocks (-1: skip)
+  float* mlw = reinterpret_cast<float*>(smem + lay.mlw_off());        // [warp][row] (max, sum)
+  float* octa = reinterpret_cast<float*>(smem + lay.octa_off());      // [R][D] this CTA's partial
+  float* mlc = reinterpret_cast<float*>(smem + lay.mlc_off());        // [R] (max, sum)
+  int* misc = reinterpret_cast<int*>(smem + lay.misc_off());          // [0]: entries in list
+  const uint32_t full0 = sbase + lay.bar_off();
+  const uint32_t empty0 = full0 + 8 * NS;
+  const uint32_t qbar = empty0 + 8 * NS;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int CS = gridDim.x;
+
+  cluster_arrive_relaxed();  // paired with the wait below: every CTA runs before any remote access
+  pdl_launch_dependents();
+  if (tid == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+    if (kSel) prefetch_tmap(&skmap);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 4);  // the four warps of the quad that owns the stage
+    }
+    mbar_init(qbar, 1);
+    fence_mbar_init();
+  }
+  pdl_wait();  // q, the sketch, the caches and idx / cnt may come from the previous kernel
+  __syncthreads();
+  cluster_wait();
+
+  const uint32_t all0 = map_cluster(all, 0);
+  const uint32_t sel0 = map_cluster(sel_sh, 0);
+  uint32_t vi = 0;   // ring sequence number (same count in every role)
+  int giter = 0;     // groups done by this CTA
+  bool ok = true;    // no wait has given up
+
+  for (int g = blockIdx.y; g < p.groups; g += gridDim.y, ++giter) {
+    const int b = g / p.Hkv, kvh = g % p.Hkv;
+    const int r0s = static_cast<int>(rank) * p.per;                 // this CTA's sketch rows
+    const int r1s = kSel ? min(p.nb, r0s + p.per) : 0;
+    const int nch = r1s > r0s ? (r1s - r0s + kSdBk - 1) / kSdBk : 0;  // sketch chunks
+    // ------------------------------------------------------------- phase S
+    if (kSel) {
+      if (warp == kSdConsumers) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(p.R * D * 2));
+          for (int t = 0; t < p.T; ++t)
+            bulk_g2s(q_sh + t * p.G * D * 2, p.q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + kvh * p.G) * D,
+                     p.G * D * 2, qbar);
+          for (int c = 0; c < nch; ++c) {
+            const uint32_t v = vi + c, st = v % NS;
+            if (v >= static_cast<uint32_t>(NS) && ok) ok = mbar_wait(empty0 + 8 * st, ((v / NS) - 1) & 1);
+            if (!ok) break;
+            const uint32_t full = full0 + 8 * st;
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(kBoxes * kSdBk * 128));
+#pragma unroll
+            for (int bx = 0; bx < kBoxes; ++bx)
+              tma_g2s_2d(sbase + st * kStageBytes + bx * kSdBk * 128, &skmap, bx * 32, g * p.nb_cap + r0s + c * kSdBk,
+                         full);
+          }
+        }
+        __syncwarp();
+      } else {
+        const int quad = warp >> 2, wq = warp & 3;
+        const int gq = lane >> 2, tq = lane & 3;
+        if (ok) ok = mbar_wait(qbar, giter & 1);
+        uint32_t bq[2][D / 16][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t qb = q_sh + 2u * ((nt * 8 + gq) * D + ks * 16 + 2 * tq);
+            bq[nt][ks][0] = lds_u32(qb);
+            bq[nt][ks][1] = lds_u32(qb + 16u);
+          }
+        for (int c = 0; c < nch; ++c) {
+          const uint32_t v = vi + c;
+          if (static_cast<int>(v & 1u) != quad) continue;
+          const uint32_t st = v % NS;
+          if (ok) ok = mbar_wait(full0 + 8 * st, (v / NS) & 1);
+          if (ok) {
+            const uint32_t tile = sbase + st * kStageBytes;
+            float acc[3][2][4];
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
+            const int rr0 = wq * 16 + gq, rr1 = rr0 + 8;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const int c0 = ks * 16 + 2 * tq;
+              const float2 x00 = lds_f32x2(tile + sel_tile_off<D>(rr0, c0));
+              const float2 x10 = lds_f32x2(tile + sel_tile_off<D>(rr1, c0));
+              const float2 x01 = lds_f32x2(tile + sel_tile_off<D>(rr0, c0 + 8));
+              const float2 x11 = lds_f32x2(tile + sel_tile_off<D>(rr1, c0 + 8));
+              uint32_t ah[4], am[4], al[4];
+              split3_bf16(x00.x, x00.y, ah[0], am[0], al[0]);
+              split3_bf16(x10.x, x10.y, ah[1], am[1], al[1]);
+              split3_bf16(x01.x, x01.y, ah[2], am[2], al[2]);
+              split3_bf16(x11.x, x11.y, ah[3], am[3], al[3]);
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                if (nt * 8 < p.R) {
+                  sel_mma_bf16(acc[0][nt], ah, bq[nt][ks][0], bq[nt][ks][1]);
+                  sel_mma_bf16(acc[1][nt], am, bq[nt][ks][0], bq[nt][ks][1]);
+                  sel_mma_bf16(acc[2][nt], al, bq[nt][ks][0], bq[nt][ks][1]);
+                }
+              }
+            }
+            float s0 = -INFINITY, s1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                if (nt * 8 + 2 * tq + j < p.R) {
+                  s0 = fmaxf(s0, p.scale * (acc[0][nt][j] + (acc[1][nt][j] + acc[2][nt][j])));
+                  s1 = fmaxf(s1, p.scale * (acc[0][nt][2 + j] + (acc[1][nt][2 + j] + acc[2][nt][2 + j])));
+                }
+            s0 = fmaxf(s0, __shfl_xor_sync(0xFFFFFFFFu, s0, 1));
+            s0 = fmaxf(s0, __shfl_xor_sync(0xFFFFFFFFu, s0, 2));
+            s1 = fmaxf(s1, __shfl_xor_sync(0xFFFFFFFFu, s1, 1));
+            s1 = fmaxf(s1, __shfl_xor_sync(0xFFFFFFFFu, s1, 2));
+            if (tq == 0) {
+              const int blk0 = r0s + c * kSdBk + rr0, blk1 = blk0 + 8;
+              if (blk0 < r1s) {
+                st_cluster_f32(all0 + 4u * static_cast<uint32_t>(blk0), s0);
+                if (p.scores) p.scores[static_cast<size_t>(g) * p.nb + blk0] = s0;
+              }
+              if (blk1 < r1s) {
+                st_cluster_f32(all0 + 4u * static_cast<uint32_t>(blk1), s1);
+                if (p.scores) p.scores[static_cast<size_t>(g) * p.nb + blk1] = s1;
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        }
+      }
+      vi += nch;
+      cluster_sync();  // every score of the group is in rank 0
+      // ----------------------------------------------------------- phase K
+      if (rank == 0 && warp < kSdConsumers) {
+        int32_t* cnt_sh = sel_ptr + p.kmax;
+        block_topk_fast<SyncFirst256>(all, p.nb, p.k, p.kmax, sel_ptr, cnt_sh, topk_s);
+        bar_named(1, kSdConsumers * 32);
+        for (int i = tid; i < p.kmax; i += kSdConsumers * 32) p.idx[static_cast<size_t>(g) * p.kmax + i] = sel_ptr[i];
+        if (tid == 0) p.cnt[g] = *cnt_sh;
+      }
+      cluster_sync();  // the selection is in rank 0's shared memory
+    }
+    // --------------------------------------------------- this CTA's block list
+    if (warp < kSdConsumers) {
+      int n;
+      if (kSel) {
+        n = ld_cluster_s32(sel0 + 4u * p.kmax);
+      } else {
+        n = p.cnt[g];
+      }
+      n = max(0, min(n, p.kmax));
+      const int mine = n > static_cast<int>(rank) ? (n - static_cast<int>(rank) + CS - 1) / CS : 0;
+      for (int i = tid; i < mine; i += kSdConsumers * 32) {
+        const int j = static_cast<int>(rank) + i * CS;
+        int blk = kSel ? ld_cluster_s32(sel0 + 4u * j) : p.idx[static_cast<size_t>(g) * p.kmax + j];
+        if (blk < 0 || blk * kSdBk >= p.L) blk = -1;
+        list[i] = blk;
+      }
+      if (tid == 0) misc[0] = mine;
+    }
+    bar_named(2, kSdThreads);  // list ready for every role
+    const int nlist = misc[0];
+    // ------------------------------------------------------------- phase A
+    if (warp == kSdConsumers) {
+      if (lane == 0) {
+        uint32_t v = vi;
+        for (int i = 0; i < nlist; ++i) {
+          const int blk = list[i];
+          if (blk < 0) continue;
+          const uint32_t st = v % NS;
+          if (v >= static_cast<uint32_t>(NS) && ok) ok = mbar_wait(empty0 + 8 * st, ((v / NS) - 1) & 1);
+          if (!ok) break;
+          const uint32_t full = full0 + 8 * st;
+          mbar_arrive_expect_tx(full, kStageBytes);
+          const uint32_t kt = sbase + st * kStageBytes;
+          const int row = g * p.Ls + blk * kSdBk;
+#pragma unroll
+          for (int bx = 0; bx < C::ROWB / 128; ++bx) {
+            tma_g2s_2d(kt + bx * kSdBk * 128, &kmap, bx * 64, row, full);
+            tma_g2s_2d(kt + C::TILEB + bx * kSdBk * 128, &vmap, bx * 64, row, full);
+          }
+          ++v;
+        }
+        // every copy issued has landed before the ring is reused or the CTA exits
+        for (uint32_t u = (v > vi + NS ? v - NS : vi); u < v; ++u) mbar_wait_drain(full0 + 8 * (u % NS), (u / NS) & 1);
+      }
+      __syncwarp();
+      bar_named(3, kSdThreads);  // the consumers' merge staging (in the ring) is done
+    } else {
+      const int quad = warp >> 2, wq = warp & 3;
+      const int gq = lane >> 2, tq = lane & 3;
+      const int kb = wq * 16;  // this warp's keys within a block
+      const int r0 = gq, r1 = gq + 8;
+      uint32_t qa[C::KSTEPS][4];
+      float o[C::NT][4];
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      int lim0 = -1, lim1 = -1;
+      {
+        const __nv_bfloat16* q0 = nullptr;
+        const __nv_bfloat16* q1 = nullptr;
+        if (r0 < p.R) {
+          q0 = p.q + ((static_cast<size_t>(b) * p.T + r0 / p.G) * p.Hq + kvh * p.G + r0 % p.G) * D;
+          lim0 = p.L - p.T + r0 / p.G;
+        }
+        if (r1 < p.R) {
+          q1 = p.q + ((static_cast<size_t>(b) * p.T + r1 / p.G) * p.Hq + kvh * p.G + r1 % p.G) * D;
+          lim1 = p.L - p.T + r1 / p.G;
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+          const int col = kk * 16 + 2 * tq;
+          qa[kk][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col) : 0u;
+          qa[kk][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col) : 0u;
+          qa[kk][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col + 8) : 0u;
+          qa[kk][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col + 8) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < C::NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+      }
+      uint32_t v = vi;
+      for (int i = 0; i < nlist; ++i) {
+        const int blk = list[i];
+        if (blk < 0) continue;
+        const uint32_t st = v % NS;
+        const bool mine_stage = static_cast<int>(v & 1u) == quad;
+        const uint32_t par = (v / NS) & 1;
+        ++v;
+        if (!mine_stage) continue;
+        if (ok) ok = mbar_wait(full0 + 8 * st, par);
+        if (ok) {
+          const uint32_t kt = sbase + st * kStageBytes;
+          const uint32_t vt = kt + C::TILEB;
+          float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int key = kb + (mi >> 1) * 8 + ri;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+              uint32_t b00, b01, b10, b11;
+              ldsm_x4(swz_chunk(kt, key, 2 * kk + (mi & 1)), b00, b01, b10, b11);
+              mma_bf16(s[0], qa[kk], b00, b01);
+              mma_bf16(s[1], qa[kk], b10, b11);
+            }
+          }
+          const int base = blk * kSdBk + kb + 2 * tq;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int key = base + nt * 8 + (x & 1);
+              const int lim = (x < 2) ? lim0 : lim1;
+              s[nt][x] = (key <= lim) ? s[nt][x] * p.qscale : -INFINITY;
+            }
+          float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+          float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+          const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+          const float c0 = exp2f(m0 - mu0), c1 = exp2f(m1 - mu1);
+          m0 = mn0;
+          m1 = mn1;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = exp2f(s[nt][0] - mu0);
+            s[nt][1] = exp2f(s[nt][1] - mu0);
+            s[nt][2] = exp2f(s[nt][2] - mu1);
+            s[nt][3] = exp2f(s[nt][3] - mu1);
+          }
+          l0 = l0 * c0 + (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
+          l1 = l1 * c1 + (s[0][2] + s[0][3]) + (s[1][2] + s[1][3]);
+          uint32_t pa[4];
+          pa[0] = pack_bf16(s[0][0], s[0][1]);
+          pa[1] = pack_bf16(s[0][2], s[0][3]);
+          pa[2] = pack_bf16(s[1][0], s[1][1]);
+          pa[3] = pack_bf16(s[1][2], s[1][3]);
+#pragma unroll
+          for (int j = 0; j < C::NT; ++j) {
+            o[j][0] *= c0;
+            o[j][1] *= c0;
+            o[j][2] *= c1;
+            o[j][3] *= c1;
+          }
+          {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int key = kb + (mi & 1) * 8 + ri;
+#pragma unroll
+            for (int jj = 0; jj < C::NT / 2; ++jj) {
+              uint32_t v0, v1, v2, v3;
+              ldsm_x4_t(swz_chunk(vt, key, 2 * jj + (mi >> 1)), v0, v1, v2, v3);
+              mma_bf16(o[2 * jj], pa, v0, v1);
+              mma_bf16(o[2 * jj + 1], pa, v2, v3);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      }
+      // ---- merge the eight warp states into this CTA's partial (fixed order)
+      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+      if (tq == 0) {
+        if (r0 < p.R) {
+          mlw[(warp * kSdRmax + r0) * 2] = m0;
+          mlw[(warp * kSdRmax + r0) * 2 + 1] = l0;
+        }
+        if (r1 < p.R) {
+          mlw[(warp * kSdRmax + r1) * 2] = m1;
+          mlw[(warp * kSdRmax + r1) * 2 + 1] = l1;
+        }
+      }
+      bar_named(1, kSdConsumers * 32);
+      float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kSdConsumers; ++w) {
+        if (r0 < p.R) M0 = fmaxf(M0, mlw[(w * kSdRmax + r0) * 2]);
+        if (r1 < p.R) M1 = fmaxf(M1, mlw[(w * kSdRmax + r1) * 2]);
+      }
+      {
+        const float c0 = exp2f(m0 - ((M0 == -INFINITY) ? 0.f : M0));
+        const float c1 = exp2f(m1 - ((M1 == -INFINITY) ? 0.f : M1));
+#pragma unroll
+        for (int j = 0; j < C::NT; ++j) {
+          o[j][0] *= c0;
+          o[j][1] *= c0;
+          o[j][2] *= c1;
+          o[j][3] *= c1;
+        }
+      }
+      // staging: [4][R][D] fp32 in the ring (every stage has been consumed; the
+      // producer issues nothing more until barrier 3)
+      float* stg = reinterpret_cast<float*>(smem) + static_cast<size_t>(wq) * kSdRmax * D;
+      if (quad == 1) {
+#pragma unroll
+        for (int j = 0; j < C::NT; ++j) {
+          const int col = j * 8 + 2 * tq;
+          if (r0 < p.R) *reinterpret_cast<float2*>(stg + r0 * D + col) = make_float2(o[j][0], o[j][1]);
+          if (r1 < p.R) *reinterpret_cast<float2*>(stg + r1 * D + col) = make_float2(o[j][2], o[j][3]);
+        }
+      }
+      bar_named(1, kSdConsumers * 32);
+      if (quad == 0) {
+#pragma unroll
+        for (int j = 0; j < C::NT; ++j) {
+          const int col = j * 8 + 2 * tq;
+          if (r0 < p.R) {
+            float2* a = reinterpret_cast<float2*>(stg + r0 * D + col);
+            const float2 x = *a;
+            *a = make_float2(o[j][0] + x.x, o[j][1] + x.y);
+          }
+          if (r1 < p.R) {
+            float2* a = reinterpret_cast<float2*>(stg + r1 * D + col);
+            const float2 x = *a;
+            *a = make_float2(o[j][2] + x.x, o[j][3] + x.y);
+          }
+        }
+      }
+      bar_named(1, kSdConsumers * 32);
+      const float* s0p = reinterpret_cast<const float*>(smem);
+      for (int e = tid; e < p.R * D / 4; e += kSdConsumers * 32) {
+        const float4 a = reinterpret_cast<const float4*>(s0p)[e];
+        const float4 bb = reinterpret_cast<const float4*>(s0p + kSdRmax * D)[e];
+        const float4 c = reinterpret_cast<const float4*>(s0p + 2 * kSdRmax * D)[e];
+        const float4 d = reinterpret_cast<const float4*>(s0p + 3 * kSdRmax * D)[e];
+        reinterpret_cast<float4*>(octa)[e] =
+            make_float4(((a.x + bb.x) + c.x) + d.x, ((a.y + bb.y) + c.y) + d.y, ((a.z + bb.z) + c.z) + d.z,
+                        ((a.w + bb.w) + c.w) + d.w);
+      }
+      if (tid < p.R) {
+        float M = -INFINITY;
+        for (int w = 0; w < kSdConsumers; ++w) M = fmaxf(M, mlw[(w * kSdRmax + tid) * 2]);
+        const float mu = (M == -INFINITY) ? 0.f : M;
+        float lsum = 0.f;
+        for (int w = 0; w < kSdConsumers; ++w)
+          lsum = fmaf(mlw[(w * kSdRmax + tid) * 2 + 1], exp2f(mlw[(w * kSdRmax + tid) * 2] - mu), lsum);
+        mlc[2 * tid] = M;
+        mlc[2 * tid + 1] = lsum;
+      }
+      fence_proxy_async_smem();  // staging writes (generic proxy) before later copies into the ring
+      bar_named(3, kSdThreads);
+    }
+    vi += 0;  // (sequence numbers advanced below, identically in every role)
+    {
+      int nv = 0;
+      for (int i = 0; i < nlist; ++i) nv += list[i] >= 0 ? 1 : 0;
+      vi += static_cast<uint32_t>(nv);
+    }
+    cluster_sync();  // every CTA's partial is complete
+    // ------------------------------------------------ merge across the cluster
+    if (warp < kSdConsumers) {
+      const uint32_t octa_a = sbase + lay.octa_off(), mlc_a = sbase + lay.mlc_off();
+      const int nq4 = p.R * D / 4;
+      for (int e = static_cast<int>(rank) * kSdConsumers * 32 + tid; e < nq4; e += CS * kSdConsumers * 32) {
+        const int r = (e * 4) / D, dd = (e * 4) % D;
+        float M = -INFINITY;
+        for (int k2 = 0; k2 < CS; ++k2) M = fmaxf(M, ld_cluster_f32(map_cluster(mlc_a + 8u * r, k2)));
+        const float mu = (M == -INFINITY) ? 0.f : M;
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k2 = 0; k2 < CS; ++k2) {
+          const float mk = ld_cluster_f32(map_cluster(mlc_a + 8u * r, k2));
+          const float lk = ld_cluster_f32(map_cluster(mlc_a + 8u * r + 4u, k2));
+          const float4 ok4 = ld_cluster_f32x4(map_cluster(octa_a + 16u * e, k2));
+          const float w = exp2f(mk - mu);
+          den = fmaf(lk, w, den);
+          num.x = fmaf(ok4.x, w, num.x);
+          num.y = fmaf(ok4.y, w, num.y);
+          num.z = fmaf(ok4.z, w, num.z);
+          num.w = fmaf(ok4.w, w, num.w);
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const int t = r / p.G, h = kvh * p.G + r % p.G;
+        uint2 pk;
+        pk.x = pack_bf16(num.x * inv, num.y * inv);
+        pk.y = pack_bf16(num.z * inv, num.w * inv);
+        *reinterpret_cast<uint2*>(p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * D + dd) = pk;
+      }
+    }
+    cluster_sync();  // every partial has been read: shared memory may be reused or released
+  }
+}
+
+}  // namespace sa

@@ -30,13 +30,27 @@ constexpr int kTopkMaxN = 16384;  // candidates per selection (blocks per sequen
 
 constexpr int kRankFinish = 64;  // rank the remaining keys once at most this many share the prefix
 
+constexpr int kFastCap = 256;  // sampled-threshold top-k: candidates ranked directly (one per thread)
+
+// 16-byte vector accesses: hist, live, fsamp, fkeys and fsel are 16-byte aligned
+// (the struct itself sits at a 16-byte aligned shared address).
 struct TopkShared {
-  uint32_t hist[4][256];     // one digit histogram per radix pass (8-bit digits, MSB first)
+  // radix path
+  alignas(16) uint32_t hist[4][256];  // one digit histogram per radix pass (8-bit digits, MSB first)
   uint32_t wdef[kSelWarps];  // per-warp count of selections decided without ties
   uint32_t weq[kSelWarps];   // per-warp count of candidates tied with the threshold key
-  uint32_t live[kRankFinish];  // rank finish: the keys still sharing the threshold's prefix
+  alignas(16) uint32_t live[kRankFinish];  // rank finish: the keys still sharing the threshold's prefix
   uint32_t nlive, fin_thr, fin_need;
+  // sampled-threshold path (block_topk_fast): 64-bit selection keys
+  alignas(16) unsigned long long fsamp[kFastCap];  // the evenly spread sample's keys
+  alignas(16) unsigned long long fkeys[kFastCap];  // gathered keys above the threshold
+  alignas(16) uint32_t fsel[kFastCap];             // slot r: block index of the rank-r gathered key
+  unsigned long long ftau;                         // the threshold key
 };
+static_assert(offsetof(TopkShared, hist) % 16 == 0 && offsetof(TopkShared, live) % 16 == 0 &&
+                  offsetof(TopkShared, fsamp) % 16 == 0 && offsetof(TopkShared, fkeys) % 16 == 0 &&
+                  offsetof(TopkShared, fsel) % 16 == 0,
+              "vector-accessed members must be 16-byte aligned");
 
 // Shared-memory accesses by 32-bit shared-window address (explicit state space,
 // so that no access falls back to generic addressing).
@@ -75,6 +89,16 @@ __device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
+// Barrier policies for the top-k functions: the whole CTA, or the first
+// kSelThreads threads of a larger CTA (named barrier 1; the other warps of that
+// CTA must not use barrier 1 meanwhile).
+struct SyncCta {
+  static __device__ __forceinline__ void sync() { __syncthreads(); }
+};
+struct SyncFirst256 {
+  static __device__ __forceinline__ void sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+};
+
 // Select from scores score(0..n-1): the forced
 // blocks are the first and the last (0 and n-1, one block when n == 1); the
 // candidates are 1..n-2; keep min(budget, n-2) of them with the highest scores,
@@ -94,7 +118,7 @@ __device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
 // ties, and after one barrier writes its selections at their ascending
 // positions; ties at the threshold are admitted in index order until the budget
 // is met.
-template <typename LoadF>
+template <typename Sync = SyncCta, typename LoadF>
 __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
                                                 int32_t* __restrict__ cnt_out, uint32_t S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -114,7 +138,7 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
     for (int i = tid; i < 4 * 256 / 4; i += kSelThreads)
       asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(hist + 16u * i), "r"(0u) : "memory");
     if (tid == 0) sts_u32(nlive, 0u);
-    __syncthreads();
+    Sync::sync();
     uint32_t prefix = 0u, mask = 0u, remaining = static_cast<uint32_t>(take);
     for (int p = 0; p < 4; ++p) {
       const int shift = 24 - 8 * p;
@@ -123,7 +147,7 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
         const uint32_t key = float_key(score(b));
         if ((key & mask) == prefix) red_add_shared(hp + 4u * ((key >> shift) & 255u), 1u);
       }
-      __syncthreads();
+      Sync::sync();
       // lane l holds digits 255-8l .. 248-8l (descending); the chosen digit is the
       // one where the count of keys above it stays below `remaining` and the count
       // including it reaches it (exactly one (lane, e) qualifies)
@@ -170,7 +194,7 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
           slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
           if (in) sts_u32(live + 4u * (slot0 + __popc(bal & ((1u << lane) - 1u))), key);
         }
-        __syncthreads();
+        Sync::sync();
         // ... and the key with count-above < remaining <= count-above-or-equal is the threshold
         if (tid < static_cast<int>(ceq)) {
           const uint32_t kt = lds_u32(live + 4u * tid);
@@ -195,7 +219,7 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
             sts_u32(fin_need, remaining - above);
           }
         }
-        __syncthreads();
+        Sync::sync();
         prefix = lds_u32(fin_thr);
         remaining = lds_u32(fin_need);
         break;
@@ -234,7 +258,7 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
     sts_u32(wdef + 4u * warp, ndef);
     sts_u32(weq + 4u * warp, neq);
   }
-  __syncthreads();
+  Sync::sync();
   uint32_t def_before = 0u, eq_before = 0u, def_all = 0u, eq_all = 0u;
 #pragma unroll
   for (int w = 0; w < kSelWarps; ++w) {
@@ -263,6 +287,183 @@ __device__ __forceinline__ void block_topk_impl(LoadF score, int n, int budget, 
   }
   for (int i = static_cast<int>(total) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
   if (tid == 0) *cnt_out = static_cast<int32_t>(total);
+}
+
+__device__ __forceinline__ unsigned long long lds_u64(uint32_t a) {
+  unsigned long long v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void lds_u64x2(uint32_t a, unsigned long long& x, unsigned long long& y) {
+  asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "r"(a) : "memory");
+}
+__device__ __forceinline__ void sts_u64(uint32_t a, unsigned long long v) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+// Selection key of candidate b: the order-preserving score key in the high
+// word, the complement of the index in the low word.  Keys are distinct, and a
+// larger key is a higher score or, at equal scores, a lower index: exactly the
+// selection order, so the top-k keys are the selection with ties resolved.
+__device__ __forceinline__ unsigned long long sel_key64(float s, int b) {
+  return (static_cast<unsigned long long>(float_key(s)) << 32) | static_cast<unsigned long long>(~static_cast<uint32_t>(b));
+}
+
+// The same selection as block_topk_impl, faster for budgets far below the
+// candidate count (decode: tens of blocks out of hundreds or thousands).
+// A sample of kFastCap candidates spread evenly over the index range gives a
+// threshold key tau (its rs-th largest sample key, rs chosen so that about
+// 1.5 * take + 2 * ncand / kFastCap candidates lie above tau); the candidates
+// above tau are gathered, and when there are between take and kFastCap of them
+// they hold the top-take keys, found by each gathered key counting the keys
+// above it (one thread per key, no ties since keys are distinct).  The key of
+// rank r < take drops its block index into slot r; each of those take threads
+// then counts the slots holding a lower index, which is its ascending output
+// position after block 0.  When too few or too many keys lie above tau, or the
+// budget is not far below the candidate count, the radix select runs instead;
+// with at most kFastCap candidates every one is gathered directly.  Shared
+// memory is read in batches of several independent loads before their uses.
+// All kSelThreads threads call; barriers are uniform.
+template <typename Sync = SyncCta, typename LoadF>
+__device__ __forceinline__ void block_topk_fast_impl(LoadF score, int n, int budget, int kmax,
+                                                     int32_t* __restrict__ idx_out, int32_t* __restrict__ cnt_out,
+                                                     uint32_t S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ncand = n > 2 ? n - 2 : 0;  // candidates 1 .. n-2
+  const int take = budget <= 0 ? 0 : (budget < ncand ? budget : ncand);
+  constexpr int m = kFastCap;
+  int rs = 0;  // sample rank of tau (0: no sample, every candidate is gathered)
+  if (ncand > m) {
+    rs = (3 * take * m) / (2 * ncand) + 2;
+    if (rs > m) rs = m;
+  }
+  // expected gathered count rs * ncand / m must leave room below the cap
+  const bool fast = take > 0 && take < ncand && static_cast<long long>(rs) * ncand <= 200LL * m;
+  if (!fast) {
+    block_topk_impl<Sync>(score, n, budget, kmax, idx_out, cnt_out, S);
+    return;
+  }
+  static_assert(kSelThreads == kFastCap, "one thread per sample / gathered key");
+  const uint32_t samp = S + static_cast<uint32_t>(offsetof(TopkShared, fsamp));
+  const uint32_t keys = S + static_cast<uint32_t>(offsetof(TopkShared, fkeys));
+  const uint32_t fsel = S + static_cast<uint32_t>(offsetof(TopkShared, fsel));
+  const uint32_t wcnt = S + static_cast<uint32_t>(offsetof(TopkShared, wdef));  // per-warp gather counts
+  const uint32_t tau_a = S + static_cast<uint32_t>(offsetof(TopkShared, ftau));
+  // count the keys above `mine` among cnt16 * 16 keys at shared address arr (16-byte aligned)
+  auto count_above = [](uint32_t arr, int cnt16, unsigned long long mine) -> uint32_t {
+    uint32_t above = 0u;
+    for (int j = 0; j < cnt16; ++j) {
+      unsigned long long x[16];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) lds_u64x2(arr + 128u * j + 16u * v, x[2 * v], x[2 * v + 1]);
+#pragma unroll
+      for (int v = 0; v < 16; ++v) above += x[v] > mine ? 1u : 0u;
+    }
+    return above;
+  };
+  if (rs > 0) {
+    const int b = 1 + static_cast<int>((static_cast<long long>(tid) * ncand) / m);
+    const unsigned long long mine = sel_key64(score(b), b);
+    sts_u64(samp + 8u * tid, mine);
+    Sync::sync();
+    if (count_above(samp, m / 16, mine) == static_cast<uint32_t>(rs - 1)) sts_u64(tau_a, mine);  // one thread
+  } else if (tid == 0) {
+    sts_u64(tau_a, 0ull);  // below every candidate key: gather them all
+  }
+  Sync::sync();
+  const unsigned long long tau = lds_u64(tau_a);
+  // gather: each thread counts its candidates above tau (b = 1 + tid + 256 i), a warp scan gives
+  // its slots, one more barrier gives the warp offsets; the keys are then written in place
+  constexpr int kBatch = 8;
+  uint32_t mine_n = 0u;
+  for (int b0 = 1 + tid; b0 < n - 1; b0 += kBatch * kSelThreads) {
+    float v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int b = b0 + j * kSelThreads;
+      v[j] = b < n - 1 ? score(b) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int b = b0 + j * kSelThreads;
+      mine_n += (b < n - 1 && sel_key64(v[j], b) > tau) ? 1u : 0u;
+    }
+  }
+  uint32_t incl = mine_n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sts_u32(wcnt + 4u * warp, incl);
+  Sync::sync();
+  uint32_t c = 0u, wbase = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    const uint32_t x = lds_u32(wcnt + 4u * w);
+    wbase += w < warp ? x : 0u;
+    c += x;
+  }
+  if (c < static_cast<uint32_t>(take) || c > static_cast<uint32_t>(kFastCap)) {  // uniform
+    Sync::sync();
+    block_topk_impl<Sync>(score, n, budget, kmax, idx_out, cnt_out, S);
+    return;
+  }
+  uint32_t at = wbase + incl - mine_n;
+  if (mine_n > 0u) {
+    for (int b0 = 1 + tid; b0 < n - 1; b0 += kBatch * kSelThreads) {
+      float v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int b = b0 + j * kSelThreads;
+        v[j] = b < n - 1 ? score(b) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int b = b0 + j * kSelThreads;
+        if (b < n - 1) {
+          const unsigned long long key = sel_key64(v[j], b);
+          if (key > tau) sts_u64(keys + 8u * (at++), key);
+        }
+      }
+    }
+  }
+  // pad the gathered keys to a multiple of 16 with zeros (below every key) for the batched count
+  const int c16 = (static_cast<int>(c) + 15) / 16;
+  if (tid >= static_cast<int>(c) && tid < 16 * c16) sts_u64(keys + 8u * tid, 0ull);
+  Sync::sync();
+  if (tid < static_cast<int>(c)) {
+    const unsigned long long mine = lds_u64(keys + 8u * tid);
+    const uint32_t r = count_above(keys, c16, mine);
+    if (r < static_cast<uint32_t>(take)) sts_u32(fsel + 4u * r, ~static_cast<uint32_t>(mine));
+  }
+  Sync::sync();
+  if (tid < take) {
+    const uint32_t my_idx = lds_u32(fsel + 4u * tid);
+    uint32_t before = 0u;
+    int j = 0;
+    for (; j + 4 <= take; j += 4) {
+      const uint4 x = lds_u32x4(fsel + 4u * j);
+      before += (x.x < my_idx ? 1u : 0u) + (x.y < my_idx ? 1u : 0u) + (x.z < my_idx ? 1u : 0u) +
+                (x.w < my_idx ? 1u : 0u);
+    }
+    for (; j < take; ++j) before += lds_u32(fsel + 4u * j) < my_idx ? 1u : 0u;
+    if (1 + static_cast<int>(before) < kmax) idx_out[1 + before] = static_cast<int32_t>(my_idx);
+  }
+  if (tid == 0) {
+    idx_out[0] = 0;
+    if (take + 1 < kmax) idx_out[take + 1] = n - 1;
+    *cnt_out = take + 2;
+  }
+  for (int i = take + 2 + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
+}
+
+// scores at shared address sc
+template <typename Sync = SyncCta>
+__device__ __forceinline__ void block_topk_fast(uint32_t sc, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
+                                                int32_t* __restrict__ cnt_out, uint32_t S) {
+  block_topk_fast_impl<Sync>([&](int b) { return lds_f32(sc + 4u * static_cast<uint32_t>(b)); }, n, budget, kmax, idx_out,
+                       cnt_out, S);
 }
 
 // scores at shared address sc
@@ -562,7 +763,7 @@ __global__ void __launch_bounds__(kSelThreads) select_decode_kernel(
     }
     budget = min(c, k);
   }
-  block_topk(all, nb, budget, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, topk_s);
+  block_topk_fast(all, nb, budget, kmax, idx + static_cast<size_t>(g) * kmax, cnt + g, topk_s);
 }
 
 // --------------------------------------------------------------------------
@@ -599,7 +800,7 @@ __global__ void __launch_bounds__(kSelThreads) select_given_kernel(const float* 
     }
   }
   __syncthreads();
-  block_topk(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, topk_s);
+  block_topk_fast(sc, nvalid, budget, kmax, idx + u * kmax, cnt + u, topk_s);
 }
 
 // Selection from a given score array too large for shared memory (one-token

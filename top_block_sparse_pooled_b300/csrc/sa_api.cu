@@ -40,6 +40,7 @@
 #include "k_sketch.cu"
 #include "k_tokmass.cu"
 #include "k_selftest.cu"
+#include "k_seldec.cu"
 
 namespace {
 
@@ -104,6 +105,28 @@ sa_status_t dev_info(DevInfo* out) {
   *out = cache[dev];
   if (out->cc_major != 10 || out->cc_minor != 3)
     return fail(SA_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", out->cc_major, out->cc_minor);
+  return SA_OK;
+}
+
+// An int derived once per device (occupancy, cluster limits) for one kernel
+// instantiation: each call site keeps its own function-local PerDevice.
+struct PerDevice {
+  std::mutex mu;
+  int v[64] = {};
+};
+
+template <typename F>
+sa_status_t per_device(PerDevice& c, F compute, int* out) {
+  int dev = 0;
+  SA_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(SA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(c.mu);
+  if (c.v[dev] == 0) {
+    int x = 0;
+    SA_TRY(compute(&x));
+    c.v[dev] = std::max(1, x);
+  }
+  *out = c.v[dev];
   return SA_OK;
 }
 
@@ -275,14 +298,16 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
   const int nb_cap = cdiv(a.Ls, a.block);
   auto kern = sa::select_decode_kernel<TE, D, RMAX>;
   constexpr bool kBf16 = std::is_same<TE, __nv_bfloat16>::value;
-  static int max_cs = 0;  // per instantiation
-  if (max_cs == 0) {
+  static PerDevice max_cs_cache;  // per instantiation and device
+  int max_cs = 0;
+  SA_TRY(per_device(max_cs_cache, [&](int* v) -> sa_status_t {
     sa::SelDecodeLayout big{sa::sel_tile_bytes(sa::kSelTileRows, D), sa::sel_q_bytes(D, RMAX, kBf16),
                             sa::kTopkMaxN};
     SA_TRY(set_smem(kern, big.bytes()));
     cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    max_cs = std::max(1, std::min(16, max_cluster_size(reinterpret_cast<const void*>(kern), big.bytes(), groups, st)));
-  }
+    *v = std::min(16, max_cluster_size(reinterpret_cast<const void*>(kern), big.bytes(), groups, st));
+    return SA_OK;
+  }, &max_cs));
   // about one CTA per SM in total, at most 1024 blocks per CTA
   int cs = std::min(max_cs, std::max(1, cdiv(di.sms, groups)));
   cs = std::max(cs, cdiv(nb, 1024));
@@ -340,13 +365,15 @@ sa_status_t run_select(const SelectArgs& a, cudaStream_t st) {
       // a cluster of CTAs holds the scores in shared memory, 16384 per CTA
       auto ck = sa::select_given_cluster_kernel;
       const int head = static_cast<int>(((sizeof(sa::SelClusterShared) + 15) / 16) * 16);
-      static int max_cs_cl = 0;
-      if (max_cs_cl == 0) {
+      static PerDevice max_cs_cl_cache;
+      int max_cs_cl = 0;
+      SA_TRY(per_device(max_cs_cl_cache, [&](int* v) -> sa_status_t {
         SA_TRY(set_smem(ck, head + sa::kSelClusterPer * 4));
         cudaFuncSetAttribute(reinterpret_cast<const void*>(ck), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        max_cs_cl = std::max(1, std::min(16, max_cluster_size(reinterpret_cast<const void*>(ck),
-                                                               head + sa::kSelClusterPer * 4, groups, st)));
-      }
+        *v = std::min(16, max_cluster_size(reinterpret_cast<const void*>(ck), head + sa::kSelClusterPer * 4, groups,
+                                           st));
+        return SA_OK;
+      }, &max_cs_cl));
       const int cs = cdiv(nb, sa::kSelClusterPer);
       if (cs <= max_cs_cl) {
         const int per = cdiv(nb, cs);
@@ -511,16 +538,172 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
   return launch_pdl(kern, dim3(nctas), dim3(sa::kDmThreads), smem, st, km, vm, p);
 }
 
+// --------------------------------------------------- cluster decode (seldec)
+// One cluster of CS CTAs per (batch, kv-head) group; with `sel`, the sketch
+// scoring and the top-k run in the same kernel, in front of the attention.
+struct SdArgs {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  const float* sketch;  // with selection
+  int32_t* idx;         // written with selection, read without
+  int32_t* cnt;
+  float* scores;  // optional, with selection
+  void* out;
+  int B, T, Hq, Hkv, d, L, Ls, k, kmax;
+  float scale;
+  bool sel;
+};
+
+constexpr int kSdMinSmem = 120 * 1024;  // keeps the kernel at one CTA per SM
+
+// Co-resident clusters of cs CTAs for one seldec instantiation on the current
+// device (cudaOccupancyMaxActiveClusters; 0 when cs is not launchable).
+template <int D, bool kSel>
+sa_status_t sd_max_clusters(int cs, int* out) {
+  auto kern = sa::seldec_kernel<D, kSel>;
+  static std::mutex mu;
+  static int cache[64][17] = {};  // per instantiation: device x cluster size, value + 1
+  int dev = 0;
+  SA_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64 || cs < 1 || cs > 16) return fail(SA_ERR_UNSUPPORTED, "device %d / cluster size %d", dev, cs);
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev][cs] == 0) {
+    SA_TRY(set_smem(kern, 227 * 1024));
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 64);
+    cfg.blockDim = dim3(sa::kSdThreads);
+    cfg.dynamicSmemBytes = kSdMinSmem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cache[dev][cs] = n + 1;
+  }
+  *out = cache[dev][cs] - 1;
+  return SA_OK;
+}
+
+// Cluster size and cluster count: the fewest 32 KB loads per CTA (sketch chunks
+// and K/V blocks, times the rounds when the groups outnumber the clusters that
+// fit at once); ties go to the smaller cluster.
+template <int D, bool kSel>
+sa_status_t sd_shape(int groups, int nb, int kmax, int* cs_out, int* ncl_out) {
+  constexpr bool sel = kSel;
+  long long best = -1;
+  for (int cs = 1; cs <= 16; ++cs) {
+    int fit = 0;
+    SA_TRY((sd_max_clusters<D, kSel>(cs, &fit)));
+    if (fit < 1) continue;
+    const int ncl = std::min(groups, fit);
+    const long long rounds = (groups + ncl - 1) / ncl;
+    const long long work = rounds * ((sel ? cdiv(cdiv(nb, cs), sa::kSdBk) : 0) + cdiv(kmax, cs));
+    if (best < 0 || work < best) {
+      best = work;
+      *cs_out = cs;
+      *ncl_out = ncl;
+    }
+  }
+  if (best < 0) return fail(SA_ERR_UNSUPPORTED, "no launchable cluster shape for the decode kernel");
+  return SA_OK;
+}
+
+template <int D, bool kSel>
+sa_status_t launch_seldec(const SdArgs& a, cudaStream_t st) {
+  auto kern = sa::seldec_kernel<D, kSel>;
+  const int groups = a.B * a.Hkv;
+  const int nb = cdiv(a.L, sa::kSdBk);
+  const int nb_cap = cdiv(a.Ls, sa::kSdBk);
+  int cs = 1, ncl = 1;
+  SA_TRY((sd_shape<D, kSel>(groups, nb, a.kmax, &cs, &ncl)));
+  const int per = cdiv(cdiv(nb, cs), sa::kSdBk) * sa::kSdBk;  // sketch rows per CTA, whole chunks
+  sa::SdLayout lay{4, D, nb, a.kmax, kSel ? 1 : 0};
+  if (lay.bytes() > 227 * 1024) lay.nstages = 2;
+  SA_SUP(lay.bytes() <= 227 * 1024, "decode over %d blocks needs %d bytes of shared memory", nb, lay.bytes());
+  const int smem = std::max(lay.bytes(), kSdMinSmem);
+  SA_TRY(set_smem(kern, smem));
+  SA_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  sa::SdParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.idx = a.idx;
+  p.cnt = a.cnt;
+  p.scores = a.scores;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.kmax = a.kmax;
+  p.k = a.k;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.R = p.G * a.T;
+  p.L = a.L;
+  p.Ls = a.Ls;
+  p.nb = nb;
+  p.nb_cap = nb_cap;
+  p.groups = groups;
+  p.per = per;
+  p.scale = a.scale;
+  p.qscale = a.scale * 1.4426950408889634f;
+  p.lay = lay;
+  CUtensorMap km, vm, skm;
+  const uint64_t rows = static_cast<uint64_t>(groups) * a.Ls;
+  SA_TRY(make_map_2d(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kc, D, rows, D * 2, 64, sa::kSdBk,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  SA_TRY(make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.vc, D, rows, D * 2, 64, sa::kSdBk,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+  if (kSel)
+    SA_TRY(make_map_2d(&skm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.sketch, D, static_cast<uint64_t>(groups) * nb_cap,
+                       D * 4, 32, sa::kSdBk, CU_TENSOR_MAP_SWIZZLE_128B));
+  else
+    skm = km;  // unused
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, ncl);
+  cfg.blockDim = dim3(sa::kSdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  SA_CUDA(cudaLaunchKernelEx(&cfg, kern, km, vm, skm, p));
+  return SA_OK;
+}
+
+sa_status_t run_seldec(const SdArgs& a, cudaStream_t st) {
+  if (a.sel) return a.d == 128 ? launch_seldec<128, true>(a, st) : launch_seldec<64, true>(a, st);
+  return a.d == 128 ? launch_seldec<128, false>(a, st) : launch_seldec<64, false>(a, st);
+}
+
+// The cluster decode applies to bf16, block 64, G * T <= 16.
+bool seldec_fits(int dtype, int block, int G, int T) {
+  return dtype == SA_BF16 && block == sa::kSdBk && G * T <= sa::kSdRmax;
+}
+
 template <typename TE, int D, int RMAX>
 sa_status_t launch_decode(const DecodeArgs& a, const DevInfo& di, cudaStream_t st) {
   using C = sa::DecodeCfg<TE, D, RMAX>;
   auto kern = sa::decode_split_kernel<TE, D, RMAX>;
   SA_TRY(set_smem(kern, C::kBytes));
-  static int occ = 0;  // per instantiation
-  if (occ == 0) {
-    SA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, sa::kDecThreads, C::kBytes));
-    occ = std::max(occ, 1);
-  }
+  static PerDevice occ_cache;  // per instantiation and device
+  int occ = 0;
+  SA_TRY(per_device(occ_cache, [&](int* v) -> sa_status_t {
+    SA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, sa::kDecThreads, C::kBytes));
+    return SA_OK;
+  }, &occ));
   const int groups = a.B * a.Hkv;
   const int target = di.sms * occ;
   int nsplit = std::max(1, std::min(a.kmax, target / std::max(groups, 1)));
@@ -560,6 +743,13 @@ sa_status_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   DevInfo di;
   SA_TRY(dev_info(&di));
   if (a.tok) return a.d == 128 ? launch_decode_mma<128, true>(a, di, st) : launch_decode_mma<64, true>(a, di, st);
+  // few groups: one cluster per group, merged through distributed shared memory;
+  // many groups: equal contiguous ranges of (group, block) units over all SMs
+  if (seldec_fits(a.dtype, a.block, a.Hq / a.Hkv, a.T) && 2 * a.B * a.Hkv <= di.sms) {
+    const SdArgs sd{a.q, a.kc, a.vc, nullptr, const_cast<int32_t*>(a.idx), const_cast<int32_t*>(a.cnt), nullptr,
+                    a.out, a.B, a.T, a.Hq, a.Hkv, a.d, a.L, a.Ls, 0, a.kmax, a.scale, false};
+    return run_seldec(sd, st);
+  }
   if (a.dtype == SA_BF16 && (a.Hq / a.Hkv) * a.T <= 16)
     return a.d == 128 ? launch_decode_mma<128, false>(a, di, st) : launch_decode_mma<64, false>(a, di, st);
   if (a.dtype == SA_F32)
@@ -963,6 +1153,28 @@ sa_status_t sa_decode(const void* q, const void* k_cache, const void* v_cache, i
   return run_decode(a, as_stream(stream));
 }
 
+sa_status_t sa_select_decode(const void* q, int dtype, const float* sketch, const void* k_cache, const void* v_cache,
+                             int B, int T, int Hq, int Hkv, int d, int L, int L_stride, int block, int k, float scale,
+                             int32_t* idx, int32_t* cnt, int kmax, float* scores, void* out, void* stream) {
+  t_err.clear();
+  SelectArgs sel{SA_SELECT_SKETCH, q, dtype, sketch, scores, B, T, Hq, Hkv, d, L, L_stride, block, 0, 0, k,
+                 0, 1, scale, idx, cnt, kmax};
+  SA_TRY(validate_select(sel));
+  SA_SUP(seldec_fits(dtype, block, Hq / Hkv, T),
+         "fused selection + decode supports bf16, block == %d and G*T <= %d (got dtype %d, block %d, G*T %d)",
+         sa::kSdBk, sa::kSdRmax, dtype, block, (Hq / Hkv) * T);
+  SA_ARG(k_cache && v_cache && out, "null pointer argument");
+  SA_ARG(aligned16(k_cache) && aligned16(v_cache) && aligned16(out), "k/v caches and out must be 16-byte aligned");
+  SA_ARG(T <= block && T <= L, "T (%d) must be <= block and <= L", T);
+  SA_ARG(static_cast<long long>(B) * Hkv * L_stride < (1LL << 31), "B*Hkv*L_stride too large");
+  SA_ARG(scale > 0.f && scale < 1e30f, "scale must be positive and finite");
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  const SdArgs a{q, k_cache, v_cache, sketch, idx, cnt, scores, out, B, T, Hq, Hkv, d, L, L_stride, k, kmax, scale,
+                 true};
+  return run_seldec(a, as_stream(stream));
+}
+
 sa_status_t sa_decode_tokens(const void* q, const void* k_cache, const void* v_cache, int dtype, const int32_t* idx,
                              const int32_t* cnt, int kmax, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
                              float scale, void* out, void* workspace, size_t ws_bytes, void* stream) {
@@ -1150,10 +1362,16 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
   void* sp = static_cast<void*>(st);
   SA_TRY(sa_append_kv(knd, vnd, a.dtype, a.B, a.Hkv, a.T, a.d, a.k_cache, a.v_cache, a.L_stride, a.L - a.T, a.block,
                       a.sketch, sp));
-  SA_TRY(sa_select_topk(SA_SELECT_SKETCH, qd, a.dtype, a.sketch, a.scores, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
-                        a.L_stride, a.block, 0, 0, a.k, 0, 1, a.scale, a.idx, a.cnt, a.kmax, sp));
-  SA_TRY(sa_decode(qd, a.k_cache, a.v_cache, a.dtype, a.idx, a.cnt, a.kmax, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
-                   a.L_stride, a.block, a.scale, outd, w, dec, sp));
+  if (seldec_fits(a.dtype, a.block, a.Hq / a.Hkv, a.T)) {
+    // selection and attention in one launch (one cluster per group)
+    SA_TRY(sa_select_decode(qd, a.dtype, a.sketch, a.k_cache, a.v_cache, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
+                            a.L_stride, a.block, a.k, a.scale, a.idx, a.cnt, a.kmax, a.scores, outd, sp));
+  } else {
+    SA_TRY(sa_select_topk(SA_SELECT_SKETCH, qd, a.dtype, a.sketch, a.scores, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
+                          a.L_stride, a.block, 0, 0, a.k, 0, 1, a.scale, a.idx, a.cnt, a.kmax, sp));
+    SA_TRY(sa_decode(qd, a.k_cache, a.v_cache, a.dtype, a.idx, a.cnt, a.kmax, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
+                     a.L_stride, a.block, a.scale, outd, w, dec, sp));
+  }
   if (a.host_io && !out_mapped) SA_CUDA(cudaMemcpyAsync(a.out, outd, qb, cudaMemcpyDeviceToHost, st));
   return SA_OK;
 }

@@ -4,8 +4,8 @@
 // unit after the decode launch helpers it reuses.
 //
 // The scratch is one file-scope __device__ array of a fixed size.  Its device
-// address is looked up once per device, with that device current, through
-// cudaGetSymbolAddress (the name of the array in host code is only a host-side
+// address is looked up once per device (and context), with that device current,
+// through cudaGetSymbolAddress (the name of the array in host code is only a host-side
 // stand-in and must never be handed to a kernel).  Every call shares the
 // array; the arrival counters at its head are cleared on the caller's stream
 // before each launch, and the rest is fully rewritten by the kernels.
@@ -20,21 +20,47 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-// Device address of g_noalloc_scratch on the current device (looked up on the
-// first call made with that device current, then cached).
+// Device address of g_noalloc_scratch on the current device.  It is looked up
+// with cudaGetSymbolAddress on the first call made with that device current and
+// cached for the device's current CUDA context; a call made in another context
+// of the same device (after cudaDeviceReset, or a primary-context teardown and
+// re-creation) looks it up again, because the array then lives in the new
+// context's copy of the module.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+sa_status_t current_context(CUcontext* out) {
+  static std::once_flag once;
+  static CtxGetCurrentFn f = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  if (!f) return fail(SA_ERR_CUDA, "cuCtxGetCurrent unavailable");
+  if (f(out) != CUDA_SUCCESS) return fail(SA_ERR_CUDA, "cuCtxGetCurrent failed");
+  return SA_OK;
+}
+
 sa_status_t noalloc_scratch(void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static CUcontext ctx[64] = {};
   int dev = 0;
   SA_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return fail(SA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  CUcontext cur = nullptr;  // null until the runtime has made the device's context current
+  SA_TRY(current_context(&cur));
   std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || cur == nullptr || ctx[dev] != cur) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr)
       return fail(SA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch) on device %d: %s", dev, cudaGetErrorString(e));
+    SA_TRY(current_context(&cur));  // the lookup made the context current
     addr[dev] = p;
+    ctx[dev] = cur;
   }
   *out = addr[dev];
   return SA_OK;
