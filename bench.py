@@ -326,9 +326,18 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
         sa.sa_select_topdelta(s["q"], s["sk"], None, wl.Hkv, wl.L, wl.L, wl.Bk, 0.3, wl.k, wl.scale, s["idx"],
                               s["cnt"])
 
+    def fused(s):  # selection and attention in one launch (the step's kernel for these shapes)
+        sa.sa_select_decode(s["q"], s["sk"], s["kc"], s["vc"], wl.L, wl.Bk, wl.k, wl.scale, s["idx"], s["cnt"],
+                            s["out"])
+
+    fused_ok = bf and wl.G * wl.T <= 16 and wl.Bk == 64
     reps = max(10, min(500, K // (4 * R)))
     kern_us = {}
-    for name, fn in (("append", app), ("select", sel), ("decode", dec), ("select_topdelta", seld)):
+    legs = [("append", app), ("select", sel), ("decode", dec)]
+    if fused_ok:
+        legs.append(("select_decode", fused))
+    legs.append(("select_topdelta", seld))
+    for name, fn in legs:
         g = capture([lambda s=s, fn=fn: fn(s) for s in sets * 4])
         kern_us[name] = round(graph_us(g, 4 * R, reps), 3)
     torch.cuda.synchronize()
@@ -339,6 +348,15 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
     torch.cuda.synchronize()
     dec_ms = kern_us["decode"] * 1e-3
     dec_gbs = kv_b / (dec_ms * 1e-3) / 1e9
+    # the step's dominant kernel: the fused selection + attention (sketch scan + selected K/V), or,
+    # for shapes without it, the attention kernel
+    if fused_ok:
+        top_ms, top_bytes = kern_us["select_decode"] * 1e-3, kv_b + sk_b
+        top_name = "sa_select_decode (seldec_kernel: sketch scoring, top-k and sparse attention in one launch)"
+    else:
+        top_ms, top_bytes = dec_ms, kv_b
+        top_name = "sa_decode (decode_split_kernel + decode_combine_kernel)"
+    top_gbs = top_bytes / (top_ms * 1e-3) / 1e9
 
     # ---- end to end through the C ABI with pinned host buffers
     hq = sets[0]["q"].cpu().pin_memory()
@@ -379,23 +397,32 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
         "config": {
             "workload": "%s decode: B=%d T=%d Hq=%d Hkv=%d d=%d L=%d block=%d top-k=%d + sink + local" % (
                 wl.name, wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, wl.L, wl.Bk, wl.k),
-            "step": "append+sketch refresh, score+top-k select, split-KV sparse decode (CUDA graphs of %d steps)" % R,
+            "step": ("append+sketch refresh, then score+top-k select and sparse decode in one launch" if fused_ok else
+                     "append+sketch refresh, score+top-k select, split-KV sparse decode") + (
+                " (CUDA graphs of %d steps)" % R),
             "bytes_per_step": {"selected_kv": kv_b, "sketch_scan": sk_b, "append": ap_b},
             "l2": "%d resident input sets rotated (%.1f GB of K/V); no step reuses L2 from the previous" % (
                 R, R * x.k.nbytes * 2 / 1e9),
         },
         "pct_hbm_peak": round(100 * value / peaks["hbm_gbs"], 2),
         "roofline": {
-            "kernel": "sa_decode (decode_mma_kernel, one launch)" if bf and wl.G * wl.T <= 16 else
-                      "sa_decode (decode_split_kernel + decode_combine_kernel)",
+            "kernel": top_name,
             "bound": "hbm",
-            "achieved": round(dec_gbs, 2),
+            "achieved": round(top_gbs, 2),
             "peak": peaks["hbm_gbs"],
             "peak_source": peak_src,
             "unit": "GB/s",
-            "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
+            "frac": round(top_gbs / peaks["hbm_gbs"], 4),
             "traffic": None,
-            "avg_launch_us": round(dec_ms * 1e3, 3),
+            "avg_launch_us": round(top_ms * 1e3, 3),
+            "algorithmic_bytes_per_launch": top_bytes,
+        },
+        "decode_roofline": {
+            "kernel": "sa_decode alone (selected K/V given): " + (
+                "seldec_kernel, one cluster per group" if fused_ok and 2 * wl.B * wl.Hkv <= 148 else
+                "decode_mma_kernel" if fused_ok else "decode_split_kernel + decode_combine_kernel"),
+            "bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peaks["hbm_gbs"], "peak_source": peak_src,
+            "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "avg_launch_us": round(dec_ms * 1e3, 3),
             "algorithmic_bytes_per_launch": kv_b,
         },
         "e2e": {"value": round(step_bytes / t_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -403,7 +430,7 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
         "kernels_us": kern_us,
         "topdelta": {"delta": 0.3, "cap": wl.k, "mean_blocks_kept_per_group": round(topdelta_blocks, 2),
                      "select_us": kern_us["select_topdelta"]},
-        "gpu_launches": K * (3 if bf and wl.G * wl.T <= 16 else 4),
+        "gpu_launches": K * (2 if fused_ok else 4),
         "clocks": clocks,
     }
     if rank == 0 and args.cpu_baseline and cpu_seconds > 0:
@@ -427,8 +454,8 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
 
 def _leg_summary(r):
     """A secondary decode workload's result, without the keys that only the headline line carries."""
-    keep = ("value", "unit", "ms_per_step", "steps", "dtype", "config", "pct_hbm_peak", "roofline", "e2e",
-            "kernels_us", "gpu_launches", "clocks", "cpu_baseline")
+    keep = ("value", "unit", "ms_per_step", "steps", "dtype", "config", "pct_hbm_peak", "roofline", "decode_roofline",
+            "e2e", "kernels_us", "gpu_launches", "clocks", "cpu_baseline")
     out = {k: r[k] for k in keep if k in r}
     out["metric"] = r["metric"]
     return out
@@ -451,7 +478,66 @@ def _events_ms(fn, reps, stream):
     return ts[len(ts) // 2]
 
 
-def bench_prefill(wl, steps, peaks, peak_src):
+def cpu_oracle_prefill(wl, x, budget_s, executed_flop):
+    """The CPU oracle's prefill step on a seeded sample of (group, tile) units, extrapolated to the
+    whole workload: each part of the step is scaled by the share of its work the sample holds
+    (sketch-mode scores by causal blocks x rows, dense mass by causal pairs, sparse attention by
+    selected tiles; the fp64 sketch of the keys is timed in full).  Returns the executed sparse-
+    attention TFLOP of the full GPU step divided by the extrapolated CPU step time."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(4242)
+    groups = wl.B * wl.Hkv
+    all_c = np.array([oracle.causal_blocks(i, wl.Qt, wl.Bk, wl.L) for i in range(wl.nq)], dtype=np.float64)
+    budget_i = np.array([oracle.prefill_budget(i, wl.k, wl.frac_num, wl.frac_den, wl.Qt, wl.Bk, wl.L)
+                         for i in range(wl.nq)], dtype=np.float64)
+    sel_i = np.minimum(all_c, budget_i + 2)  # selected blocks per tile (forced included)
+    t_sketch = 0.0
+    sketch = None
+    if wl.mode != "mass":
+        t0 = time.perf_counter()
+        sketch = oracle.block_means(x.k, wl.L, wl.Bk)
+        t_sketch = time.perf_counter() - t0
+    n = 4
+    t_score = t_sel = t_att = 0.0
+    while True:
+        units = [(int(rng.integers(groups)), int(rng.integers(wl.nq))) for _ in range(n)]
+        t0 = time.perf_counter()
+        if wl.mode == "mass":
+            sc = oracle.mass(x.q, x.k, wl.Hkv, wl.L, 0, wl.Qt, wl.Bk, wl.scale, units)
+        else:
+            sc = oracle.prefill_scores(x.q, sketch, wl.Hkv, wl.Qt, wl.Bk, wl.scale, units)
+        t1 = time.perf_counter()
+        idx, cnt, _, _ = oracle.prefill_select(x.q, x.k, wl, units, scores=sc)
+        t2 = time.perf_counter()
+        rows = np.array([(g // wl.Hkv, t, (g % wl.Hkv) * wl.G + h) for g, i in units
+                         for t in range(i * wl.Qt, min((i + 1) * wl.Qt, wl.L)) for h in range(wl.G)], dtype=np.int64)
+        full_idx = -np.ones((groups * wl.nq, idx.shape[1]), dtype=np.int32)  # the sampled units' selections
+        full_cnt = np.zeros((groups * wl.nq,), dtype=np.int32)
+        for u, (g, i) in enumerate(units):
+            full_idx[g * wl.nq + i] = idx[u]
+            full_cnt[g * wl.nq + i] = cnt[u]
+        oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, 0, wl.Bk, wl.scale, rows, full_idx, full_cnt, nsel=wl.nq,
+                      rows_per_sel=wl.Qt)
+        t3 = time.perf_counter()
+        t_score, t_sel, t_att = t1 - t0, t2 - t1, t3 - t2
+        if t3 - t0 > budget_s / 4 or n >= 4096:
+            break
+        n *= 2
+    ii = np.array([i for _, i in units])
+    share_c = all_c[ii].sum() / (groups * all_c.sum())          # causal blocks (scores, mass)
+    share_s = sel_i[ii].sum() / (groups * sel_i.sum())          # selected tiles (attention)
+    step_s = t_sketch + (t_score + t_sel) / share_c + t_att / share_s
+    sample = "%d random (group, tile) units of %d; %s; scaled to the whole step by causal blocks and " \
+             "selected tiles (extrapolated)" % (len(units), groups * wl.nq,
+                                                "dense fp64 mass" if wl.mode == "mass" else
+                                                "fp64 sketch of all keys timed in full")
+    return {"value": round(executed_flop / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle", "sample": sample, "extrapolated": True, "step_s": round(step_s, 3)}
+
+
+def bench_prefill(wl, steps, peaks, peak_src, cpu_seconds=0.0):
     """One prefill step = (sketch build + sketch select | oracle mass + mass select) + sparse prefill,
     on the full workload.  Returns a dict with per-kernel times and tensor-core rooflines."""
     import numpy as np
@@ -467,7 +553,6 @@ def bench_prefill(wl, steps, peaks, peak_src):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
     q, k, v = up(x.q), up(x.k), up(x.v)
-    del x
     kmax = sa.sa_select_kmax(wl.L, wl.Bk, wl.Qt, True, wl.k, wl.frac_num, wl.frac_den)
     idx = torch.empty((wl.B, wl.Hkv, wl.nq, kmax), dtype=torch.int32, device=dev)
     cnt = torch.empty((wl.B, wl.Hkv, wl.nq), dtype=torch.int32, device=dev)
@@ -547,6 +632,9 @@ def bench_prefill(wl, steps, peaks, peak_src):
                                 "algorithmic_flop_per_launch": mass_flops}
     del q, k, v, out
     torch.cuda.empty_cache()
+    if cpu_seconds > 0:
+        res["cpu_baseline"] = cpu_oracle_prefill(wl, x, cpu_seconds, executed)
+    del x
     return res
 
 
@@ -748,9 +836,10 @@ def bench_prefill_tokens(reps, peaks, peak_src):
 
 
 def _kernel_hash():
+    """Hash of the sources of the step's dominant kernel (stored DRAM traffic is used while it matches)."""
     import hashlib
     h = hashlib.sha256()
-    for fn in ("k_decode_mma.cu", "sa_ptx.cuh"):
+    for fn in ("k_seldec.cu", "k_select.cu", "k_decode_mma.cu", "sa_ptx.cuh"):
         with open(os.path.join(ROOT, "top_block_sparse_pooled_b300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -877,7 +966,8 @@ def main():
                     res["decode_legs"].append(_leg_summary(leg))
             if args.prefill_steps > 0 and res is not None:
                 peaks, src = load_peaks()
-                res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src) for n in ("c5", "c4")]
+                cs = min(args.cpu_seconds, 10.0) if (args.cpu_baseline and rank == 0) else 0.0
+                res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src, cs) for n in ("c5", "c4")]
                 res["gpu_launches"] += 4 * args.prefill_steps * 2
             if args.tokens_reps > 0 and res is not None:
                 peaks, src = load_peaks()

@@ -116,9 +116,10 @@ def test_decode_topdelta_matches_oracle(sa, name):
 
 @pytest.mark.parametrize("n", [258, 259, 300, 512, 514, 1000, 4096, 16384])
 def test_select_small_budgets_patterns(sa, n):
-    """Budgets far below the candidate count (the decode regime), on score patterns that
-    stress a sampled threshold: exact ties everywhere, all equal, sorted ascending and
-    descending, a few large outliers, and random; bit-exact against the oracle."""
+    """Budgets from one to a third of the candidates, on score patterns that stress a
+    value-histogram threshold search: exact ties everywhere, all equal, sorted ascending and
+    descending, a few large outliers, random, and values spread over 60 octaves (most of
+    them in one bin, so the search refines over several rounds); bit-exact against the oracle."""
     rng = np.random.default_rng(1000 + n)
     pats = [
         rng.integers(-4, 5, size=n).astype(np.float32) * 0.25,   # heavy ties
@@ -127,10 +128,11 @@ def test_select_small_budgets_patterns(sa, n):
         -np.arange(n, dtype=np.float32),                          # descending: the top is at the start
         np.where(rng.random(n) < 0.01, 10.0, rng.standard_normal(n)).astype(np.float32),  # needles
         rng.standard_normal(n).astype(np.float32),
+        (2.0 ** rng.integers(0, 60, size=n)).astype(np.float32),  # values over 60 octaves: several rounds
     ]
     s = np.stack(pats)
     groups = s.shape[0]
-    for k in (1, 7, 32, 80, 128, 200):
+    for k in (1, 7, 32, 80, 128, 200, n // 3):
         kmax = sa.sa_select_kmax(n, 1, 0, False, k)
         scores = torch.from_numpy(np.ascontiguousarray(s.reshape(1, groups, 1, n))).cuda()
         idx = torch.full((1, groups, 1, kmax), -7, dtype=torch.int32, device="cuda")

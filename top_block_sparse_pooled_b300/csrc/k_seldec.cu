@@ -22,10 +22,11 @@
 //   A                   the CTA streams its blocks' K and V tiles and keeps an
 //                       online softmax per query row; its partial (max, sum,
 //                       unnormalised output rows) goes to its shared memory.
-//   merge               after a cluster barrier, each CTA combines a slice of
-//                       the output rows from all CS partials (exact rescaling)
-//                       and writes it; a last cluster barrier keeps every
-//                       partial alive until it has been read.
+//   merge               output row r is merged by CTA r % CS: every CTA pushes
+//                       its partial rows into their receivers' shared memory
+//                       and arrives on the receivers' mbarriers; a receiver
+//                       combines the CS partials (exact rescaling) and writes
+//                       the row.
 //
 // Roles (288 threads): warps 0-7 consumers in two quads (quad q takes the ring
 // stages of sequence numbers v with v % 2 == q, so the two quads work on
@@ -49,6 +50,7 @@ constexpr int kSdConsumers = 4 * kSdQuads;
 constexpr int kSdThreads = (kSdConsumers + 1) * 32;
 constexpr int kSdBk = 64;            // keys per block; sketch rows per chunk
 constexpr int kSdRmax = 16;          // query rows per group (G * T)
+constexpr int kSdRecvRows = 32;      // >= CS * ceil(R / CS) for CS <= 16, R <= 16
 
 // Shared-memory layout (runtime, from a 1024-aligned base).  A ring stage holds
 // one block's K and V tiles (64 rows of 2*D bytes each, 128-byte swizzle) or one
@@ -68,8 +70,11 @@ struct SdLayout {
   __host__ __device__ int octa_off() const { return mlw_off() + kSdConsumers * kSdRmax * 8; }
   __host__ __device__ int mlc_off() const { return octa_off() + kSdRmax * D * 4; }
   __host__ __device__ int misc_off() const { return mlc_off() + kSdRmax * 8; }
-  __host__ __device__ int bar_off() const { return misc_off() + 16; }
-  __host__ __device__ int bytes() const { return bar_off() + (2 * nstages + 1) * 8 + 1024; }
+  // partial rows pushed here by every CTA of the cluster: slot (sender, row) of D floats, then
+  // the row's (max, sum) and two pad words
+  __host__ __device__ int recv_off() const { return misc_off() + 16; }
+  __host__ __device__ int bar_off() const { return recv_off() + kSdRecvRows * (D + 4) * 4; }
+  __host__ __device__ int bytes() const { return bar_off() + (2 * nstages + 2) * 8 + 1024; }
 };
 
 struct SdParams {
@@ -92,6 +97,19 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t a) {
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
                : "memory");
   return v;
+}
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t a, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t a, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
+// earlier writes (and those ordered before them) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("fence.acq_rel.cluster;\n\tmbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 __device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
   int v;
@@ -126,6 +144,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
   const uint32_t full0 = sbase + lay.bar_off();
   const uint32_t empty0 = full0 + 8 * NS;
   const uint32_t qbar = empty0 + 8 * NS;
+  const uint32_t recvbar = qbar + 8;  // CS arrivals per group: every CTA has pushed its rows
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -142,6 +161,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
       mbar_init(empty0 + 8 * s, 4);  // the four warps of the quad that owns the stage
     }
     mbar_init(qbar, 1);
+    mbar_init(recvbar, CS);
     fence_mbar_init();
   }
   pdl_wait();  // q, the sketch, the caches and idx / cnt may come from the previous kernel
@@ -155,6 +175,9 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
   bool ok = true;    // no wait has given up
 
   for (int g = blockIdx.y; g < p.groups; g += gridDim.y, ++giter) {
+    // a later group's partials may be pushed only once every CTA has merged the previous group's
+    // (with selection, the barriers of the selection phase order this)
+    if (!kSel && giter > 0) cluster_sync();
     const int b = g / p.Hkv, kvh = g % p.Hkv;
     const int r0s = static_cast<int>(rank) * p.per;                 // this CTA's sketch rows
     const int r1s = kSel ? min(p.nb, r0s + p.per) : 0;
@@ -518,38 +541,58 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
       for (int i = 0; i < nlist; ++i) nv += list[i] >= 0 ? 1 : 0;
       vi += static_cast<uint32_t>(nv);
     }
-    cluster_sync();  // every CTA's partial is complete
     // ------------------------------------------------ merge across the cluster
+    // Row r of the output is merged by CTA r % CS: every CTA pushes its partial rows into their
+    // receivers' shared memory and arrives on the receivers' mbarriers; a receiver waits for all
+    // CS pushes and combines them (exact rescaling).  Nothing reads this CTA's shared memory
+    // from outside after this point, so a CTA that receives nothing may leave at once.
     if (warp < kSdConsumers) {
-      const uint32_t octa_a = sbase + lay.octa_off(), mlc_a = sbase + lay.mlc_off();
-      const int nq4 = p.R * D / 4;
-      for (int e = static_cast<int>(rank) * kSdConsumers * 32 + tid; e < nq4; e += CS * kSdConsumers * 32) {
-        const int r = (e * 4) / D, dd = (e * 4) % D;
-        float M = -INFINITY;
-        for (int k2 = 0; k2 < CS; ++k2) M = fmaxf(M, ld_cluster_f32(map_cluster(mlc_a + 8u * r, k2)));
-        const float mu = (M == -INFINITY) ? 0.f : M;
-        float den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k2 = 0; k2 < CS; ++k2) {
-          const float mk = ld_cluster_f32(map_cluster(mlc_a + 8u * r, k2));
-          const float lk = ld_cluster_f32(map_cluster(mlc_a + 8u * r + 4u, k2));
-          const float4 ok4 = ld_cluster_f32x4(map_cluster(octa_a + 16u * e, k2));
-          const float w = exp2f(mk - mu);
-          den = fmaf(lk, w, den);
-          num.x = fmaf(ok4.x, w, num.x);
-          num.y = fmaf(ok4.y, w, num.y);
-          num.z = fmaf(ok4.z, w, num.z);
-          num.w = fmaf(ok4.w, w, num.w);
+      const int rpr = (p.R + CS - 1) / CS;  // rows per receiver
+      const uint32_t recv_a = sbase + lay.recv_off();
+      for (int e = tid; e < p.R * (D / 4); e += kSdConsumers * 32) {
+        const int r = e / (D / 4), c4 = e % (D / 4);
+        const uint32_t slot = static_cast<uint32_t>(static_cast<int>(rank) * rpr + r / CS);
+        st_cluster_f32x4(map_cluster(recv_a + (slot * (D + 4) + c4 * 4) * 4u, r % CS),
+                         reinterpret_cast<const float4*>(octa)[e]);
+      }
+      if (tid < p.R) {
+        const uint32_t slot = static_cast<uint32_t>(static_cast<int>(rank) * rpr + tid / CS);
+        st_cluster_f32x2(map_cluster(recv_a + (slot * (D + 4) + D) * 4u, tid % CS), mlc[2 * tid], mlc[2 * tid + 1]);
+      }
+      bar_named(1, kSdConsumers * 32);  // every push of this CTA is issued before the arrivals
+      const int nrecv = min(CS, p.R);
+      if (tid < nrecv) mbar_arrive_remote(map_cluster(recvbar, tid));
+      if (static_cast<int>(rank) < nrecv) {
+        if (ok) ok = mbar_wait(recvbar, giter & 1);
+        const int mine = (p.R - static_cast<int>(rank) + CS - 1) / CS;  // rows rank, rank + CS, ...
+        const float* rv = reinterpret_cast<const float*>(smem + lay.recv_off());
+        for (int e = tid; e < mine * (D / 4); e += kSdConsumers * 32) {
+          const int j = e / (D / 4), dd = (e % (D / 4)) * 4;
+          const int r = static_cast<int>(rank) + j * CS;
+          float M = -INFINITY;
+          for (int k2 = 0; k2 < CS; ++k2) M = fmaxf(M, rv[(k2 * rpr + j) * (D + 4) + D]);
+          const float mu = (M == -INFINITY) ? 0.f : M;
+          float den = 0.f;
+          float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k2 = 0; k2 < CS; ++k2) {
+            const float* row = rv + (k2 * rpr + j) * (D + 4);
+            const float w = exp2f(row[D] - mu);
+            const float4 ok4 = *reinterpret_cast<const float4*>(row + dd);
+            den = fmaf(row[D + 1], w, den);
+            num.x = fmaf(ok4.x, w, num.x);
+            num.y = fmaf(ok4.y, w, num.y);
+            num.z = fmaf(ok4.z, w, num.z);
+            num.w = fmaf(ok4.w, w, num.w);
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          const int t = r / p.G, h = kvh * p.G + r % p.G;
+          uint2 pk;
+          pk.x = pack_bf16(num.x * inv, num.y * inv);
+          pk.y = pack_bf16(num.z * inv, num.w * inv);
+          *reinterpret_cast<uint2*>(p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * D + dd) = pk;
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const int t = r / p.G, h = kvh * p.G + r % p.G;
-        uint2 pk;
-        pk.x = pack_bf16(num.x * inv, num.y * inv);
-        pk.y = pack_bf16(num.z * inv, num.w * inv);
-        *reinterpret_cast<uint2*>(p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * D + dd) = pk;
       }
     }
-    cluster_sync();  // every partial has been read: shared memory may be reused or released
   }
 }
 

@@ -291,6 +291,47 @@ int max_cluster_size(const void* fn, int smem, int groups, cudaStream_t st) {
   return size;
 }
 
+// Co-resident clusters of cs CTAs of `threads` threads and `smem` bytes of a kernel on the
+// current device (cached per device, kernel, cluster size and shared-memory size).
+sa_status_t active_clusters(const void* kern, int cs, int threads, int smem, int* out) {
+  struct Key {
+    int dev;
+    const void* kern;
+    int cs, threads, smem;
+  };
+  static std::mutex mu;
+  static std::vector<std::pair<Key, int>> cache;
+  int dev = 0;
+  SA_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& e : cache)
+    if (e.first.dev == dev && e.first.kern == kern && e.first.cs == cs && e.first.threads == threads &&
+        e.first.smem == smem) {
+      *out = e.second;
+      return SA_OK;
+    }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, 64);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (cache.size() > 256) cache.clear();
+  cache.push_back({Key{dev, kern, cs, threads, smem}, n});
+  *out = n;
+  return SA_OK;
+}
+
 template <typename TE, int D, int RMAX>
 sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStream_t st) {
   const int groups = a.B * a.Hkv;
@@ -315,10 +356,24 @@ sa_status_t launch_select_decode(const SelectArgs& a, const DevInfo& di, cudaStr
          max_cs);
   cs = std::min(cs, nb);
   // whole 64-row chunks per CTA (only the group's last CTA stages a partial one)
-  const int per = cdiv(cdiv(nb, cs), sa::kSelChunkRows) * sa::kSelChunkRows;
+  int per = cdiv(cdiv(nb, cs), sa::kSelChunkRows) * sa::kSelChunkRows;
   cs = cdiv(nb, per);
-  const int tile_rows = std::min(sa::kSelTileRows, per);
-  const sa::SelDecodeLayout lay{sa::sel_tile_bytes(tile_rows, D), sa::sel_q_bytes(D, RMAX, kBf16), nb};
+  int tile_rows = std::min(sa::kSelTileRows, per);
+  sa::SelDecodeLayout lay{sa::sel_tile_bytes(tile_rows, D), sa::sel_q_bytes(D, RMAX, kBf16), nb};
+  // smaller clusters while the groups' clusters would not all be resident at once (a second
+  // wave of clusters doubles the time); never below the 1024-blocks-per-CTA limit
+  const int cs_min = cdiv(nb, 1024);
+  while (cs > cs_min) {
+    int fit = 0;
+    SA_TRY(set_smem(kern, lay.bytes()));
+    SA_TRY(active_clusters(reinterpret_cast<const void*>(kern), cs, sa::kSelThreads, lay.bytes(), &fit));
+    if (fit >= groups || fit == 0) break;
+    const int next = std::max(cs_min, cs - 1);
+    per = cdiv(cdiv(nb, next), sa::kSelChunkRows) * sa::kSelChunkRows;
+    cs = cdiv(nb, per);
+    tile_rows = std::min(sa::kSelTileRows, per);
+    lay = sa::SelDecodeLayout{sa::sel_tile_bytes(tile_rows, D), sa::sel_q_bytes(D, RMAX, kBf16), nb};
+  }
   const int smem = lay.bytes();
   SA_TRY(set_smem(kern, smem));
   CUtensorMap map;
