@@ -17,18 +17,22 @@
 // carry its 24-bit significand, and the three products are accumulated in the
 // fp32 TMEM accumulator.  This gives float32-level scores from kind::f16 MMAs.
 //
-// Work unit: (group, query tile i), i descending, round-robin over a
-// persistent grid of one CTA per SM.  Per unit, the causal blocks are taken in
-// M tiles of 128; per M tile the group's heads are taken in chunks of two
-// (N = 128 query rows each, 256 TMEM columns per chunk, two chunk buffers).
+// Work unit: (group g, chunk c of 128 query tiles, M tile m <= c of 128 key
+// blocks), dealt round-robin over a persistent grid of one CTA per SM.  The
+// unit splits its M tile of the sketch once and keeps the three parts in
+// shared memory while the query rows of every tile of the chunk stream past:
+// per tile, the group's heads are taken in pairs (N = 128 query rows each, 256
+// TMEM columns per pair, two pair buffers).  Tile i needs the blocks 0..i, so
+// chunk c needs M tiles 0..c; the diagonal unit (m == c) also masks the blocks
+// past each tile and writes -inf for the M tiles past the chunk.
 // Roles (384 threads):
 //   warp 0        TMA producer: one head's 128 query rows per ring slot
 //                 (3-D map: d, head, row), in the order the MMA consumes them.
 //   warp 1        TMEM allocator and MMA issuer.
-//   warps 4-11    convert the M tile's fp32 sketch rows into the three bf16
+//   warps 4-11    convert the unit's fp32 sketch rows into the three bf16
 //                 parts (128-byte-swizzled K-major tiles in shared memory);
 //                 warps 4-7 also read the accumulators (thread = block lane),
-//                 take the max over the chunk's columns and write the scores.
+//                 take the max over the tile's rows and heads and write the scores.
 #pragma once
 
 #include "sa_tc.cuh"
@@ -54,8 +58,32 @@ struct ScParams {
   const float* sketch;  // [groups, nb_cap, 128]
   float* scores;        // [groups, nq, nb]
   int L, Hq, Hkv, G, groups, nq, nb, nb_cap, units;
+  int nc;  // chunks of 128 tiles
   float scale;
 };
+
+constexpr int kScChunk = 128;  // query tiles per unit (= key blocks per M tile)
+
+struct ScUnit {
+  int g, c, m, i0, i1;  // group, chunk, M tile, tiles [i0, i1)
+};
+
+// Unit u -> (group, chunk, M tile): groups vary fastest, then the (c, m) pairs
+// m <= c in the order (0,0), (1,0), (1,1), (2,0), ...
+__device__ __forceinline__ ScUnit sc_unit(const ScParams& p, int u) {
+  ScUnit w;
+  w.g = u % p.groups;
+  int r = u / p.groups, c = 0;
+  while (r > c) {
+    r -= c + 1;
+    ++c;
+  }
+  w.c = c;
+  w.m = r;
+  w.i0 = c * kScChunk;
+  w.i1 = min(p.nq, w.i0 + kScChunk);
+  return w;
+}
 
 __device__ __forceinline__ uint32_t bf16_bits(float x) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
@@ -102,10 +130,9 @@ __global__ void __launch_bounds__(kScThreads, 1) score_prefill_kernel(const __gr
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-        const int i = p.nq - 1 - u / p.groups, g = u % p.groups;
-        const int b = g / p.Hkv, kvh = g % p.Hkv;
-        const int mtiles = i / 128 + 1;  // causal blocks 0..i
-        for (int m = 0; m < mtiles; ++m)
+        const ScUnit w = sc_unit(p, u);
+        const int b = w.g / p.Hkv, kvh = w.g % p.Hkv;
+        for (int i = w.i0; i < w.i1; ++i)
           for (int h = 0; h < p.G; ++h, ++it) {
             const int s = it % kScQSlots;
             if (it >= kScQSlots && ok) ok = mbar_wait(bar(ScSmem::Q_EMPTY + s), ((it / kScQSlots) - 1) & 1);
@@ -124,12 +151,11 @@ __global__ void __launch_bounds__(kScThreads, 1) score_prefill_kernel(const __gr
       constexpr uint32_t kId = tc::idesc_bf16(128, 128, false, false);
       uint32_t it = 0, mt = 0, dc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-        const int i = p.nq - 1 - u / p.groups;
-        const int mtiles = i / 128 + 1;
-        for (int m = 0; m < mtiles; ++m, ++mt) {
-          if (ok) ok = mbar_wait(bar(ScSmem::A_FULL), mt & 1);
-          tc::fence_after_sync();
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++mt) {
+        const ScUnit w = sc_unit(p, u);
+        if (ok) ok = mbar_wait(bar(ScSmem::A_FULL), mt & 1);
+        tc::fence_after_sync();
+        for (int i = w.i0; i < w.i1; ++i) {
           for (int c = 0; c < nchunks; ++c, ++dc) {
             const uint32_t db = dc & 1;
             if (dc >= 2 && ok) ok = mbar_wait(bar(ScSmem::D_FREE + db), ((dc >> 1) - 1) & 1);
@@ -153,8 +179,8 @@ __global__ void __launch_bounds__(kScThreads, 1) score_prefill_kernel(const __gr
             }
             tc::mma_commit(bar(ScSmem::D_FULL + db));
           }
-          tc::mma_commit(bar(ScSmem::A_EMPTY));
         }
+        tc::mma_commit(bar(ScSmem::A_EMPTY));
       }
       // drain: every MMA issued has completed before TMEM is freed
       tc::mma_commit(bar(ScSmem::DONE));
@@ -169,69 +195,67 @@ __global__ void __launch_bounds__(kScThreads, 1) score_prefill_kernel(const __gr
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     uint32_t mt = 0, dc = 0;
     bool ok = true;
-    // this thread's 16 four-float pieces of an M tile's sketch rows (blocks past i read as zero);
-    // the next M tile's pieces are loaded while the tensor core works on the current one
+    // this thread's 16 four-float pieces of the unit's sketch rows (blocks past the sequence read
+    // as zero); the next unit's pieces are loaded while the tensor core works on the current one
     float4 cur[16];
-    auto load_tile = [&](int uu, int mm) {
-      const int ii = p.nq - 1 - uu / p.groups, gg = uu % p.groups;
+    auto load_tile = [&](int uu) {
+      const ScUnit w = sc_unit(p, uu);
 #pragma unroll
       for (int it = 0; it < 16; ++it) {
         const int item = ct + it * 256;
         const int r = item >> 5, c4 = item & 31;
-        const int blk = mm * 128 + r;
-        cur[it] = (blk <= ii && blk < p.nb)
-                      ? __ldg(reinterpret_cast<const float4*>(p.sketch + (static_cast<size_t>(gg) * p.nb_cap + blk) * 128) + c4)
+        const int blk = w.m * 128 + r;
+        cur[it] = (blk < p.nb)
+                      ? __ldg(reinterpret_cast<const float4*>(p.sketch + (static_cast<size_t>(w.g) * p.nb_cap + blk) * 128) + c4)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     };
-    if (blockIdx.x < p.units) load_tile(blockIdx.x, 0);
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-      const int i = p.nq - 1 - u / p.groups, g = u % p.groups;
-      const int mtiles = i / 128 + 1;
-      const int rows_valid = min(128, p.L - i * 128);  // query rows of the tile (last tile may be short)
-      float* srow = p.scores + (static_cast<size_t>(g) * p.nq + i) * p.nb;
-      for (int m = 0; m < mtiles; ++m, ++mt) {
-        // ---- convert sketch rows 128m .. 128m+127 into the three bf16 parts
-        if (mt > 0 && ok) ok = mbar_wait(bar(ScSmem::A_EMPTY), (mt - 1) & 1);
+    if (blockIdx.x < p.units) load_tile(blockIdx.x);
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++mt) {
+      const ScUnit w = sc_unit(p, u);
+      // ---- convert the unit's sketch rows into the three bf16 parts
+      if (mt > 0 && ok) ok = mbar_wait(bar(ScSmem::A_EMPTY), (mt - 1) & 1);
 #pragma unroll
-        for (int it = 0; it < 16; ++it) {
-          const int item = ct + it * 256;
-          const int r = item >> 5, c4 = item & 31;  // row, 4-float chunk
-          const float4 x = cur[it];
-          const float xs[4] = {x.x, x.y, x.z, x.w};
-          uint32_t part[3][2];
+      for (int it = 0; it < 16; ++it) {
+        const int item = ct + it * 256;
+        const int r = item >> 5, c4 = item & 31;  // row, 4-float chunk
+        const float4 x = cur[it];
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+        uint32_t part[3][2];
 #pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            uint32_t hv[2], mv[2], lv[2];
+        for (int e2 = 0; e2 < 2; ++e2) {
+          uint32_t hv[2], mv[2], lv[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float v = xs[2 * e2 + e];
-              const float h = __bfloat162float(__float2bfloat16_rn(v));
-              const float r1 = v - h;
-              const float mdl = __bfloat162float(__float2bfloat16_rn(r1));
-              const float r2 = r1 - mdl;
-              hv[e] = bf16_bits(h);
-              mv[e] = bf16_bits(mdl);
-              lv[e] = bf16_bits(r2);
-            }
-            part[0][e2] = hv[0] | (hv[1] << 16);
-            part[1][e2] = mv[0] | (mv[1] << 16);
-            part[2][e2] = lv[0] | (lv[1] << 16);
+          for (int e = 0; e < 2; ++e) {
+            const float v = xs[2 * e2 + e];
+            const float h = __bfloat162float(__float2bfloat16_rn(v));
+            const float r1 = v - h;
+            const float mdl = __bfloat162float(__float2bfloat16_rn(r1));
+            const float r2 = r1 - mdl;
+            hv[e] = bf16_bits(h);
+            mv[e] = bf16_bits(mdl);
+            lv[e] = bf16_bits(r2);
           }
-          const int dcol = c4 * 4;                     // first d column of this chunk
-          const int box = dcol >> 6, e64 = dcol & 63;  // 64-column box, column inside it
-          const int ch = e64 >> 3;                     // 16-byte chunk in the 128-byte row
-          const uint32_t off = box * kScBox + r * 128 + (((ch ^ (r & 7)) << 4) | ((e64 & 7) * 2));
-#pragma unroll
-          for (int pp = 0; pp < 3; ++pp)
-            *reinterpret_cast<uint2*>(smem + ScSmem::kA + pp * kScTile + off) = make_uint2(part[pp][0], part[pp][1]);
+          part[0][e2] = hv[0] | (hv[1] << 16);
+          part[1][e2] = mv[0] | (mv[1] << 16);
+          part[2][e2] = lv[0] | (lv[1] << 16);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(ScSmem::A_FULL));
-        if (m + 1 < mtiles) load_tile(u, m + 1);
-        else if (u + static_cast<int>(gridDim.x) < p.units) load_tile(u + gridDim.x, 0);
-        if (!epi) continue;
-        // ---- epilogue: max over the chunk columns of this block lane
+        const int dcol = c4 * 4;                     // first d column of this chunk
+        const int box = dcol >> 6, e64 = dcol & 63;  // 64-column box, column inside it
+        const int ch = e64 >> 3;                     // 16-byte chunk in the 128-byte row
+        const uint32_t off = box * kScBox + r * 128 + (((ch ^ (r & 7)) << 4) | ((e64 & 7) * 2));
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp)
+          *reinterpret_cast<uint2*>(smem + ScSmem::kA + pp * kScTile + off) = make_uint2(part[pp][0], part[pp][1]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(ScSmem::A_FULL));
+      if (u + static_cast<int>(gridDim.x) < p.units) load_tile(u + gridDim.x);
+      if (!epi) continue;
+      // ---- epilogue, per tile: max over the tile's rows and heads of this block lane
+      const int blk = w.m * 128 + lrow;
+      for (int i = w.i0; i < w.i1; ++i) {
+        const int rows_valid = min(128, p.L - i * 128);  // query rows of the tile (last tile may be short)
         float mx = -INFINITY;
         for (int c = 0; c < nchunks; ++c, ++dc) {
           const uint32_t db = dc & 1;
@@ -256,12 +280,11 @@ __global__ void __launch_bounds__(kScThreads, 1) score_prefill_kernel(const __gr
           tc::fence_before_sync();
           mbar_arrive(bar(ScSmem::D_FREE + db));
         }
-        const int blk = m * 128 + lrow;
-        if (blk <= i && blk < p.nb) srow[blk] = mx * p.scale;
+        float* srow = p.scores + (static_cast<size_t>(w.g) * p.nq + i) * p.nb;
+        if (blk < p.nb) srow[blk] = blk <= i ? mx * p.scale : -INFINITY;
+        if (w.m == w.c)  // the diagonal unit: the M tiles past the chunk are not causal for any of its tiles
+          for (int bb = (w.m + 1) * 128 + lrow; bb < p.nb; bb += 128) srow[bb] = -INFINITY;
       }
-      // non-causal entries of the row
-      if (epi)
-        for (int blk = i + 1 + lrow; blk < p.nb; blk += 128) srow[blk] = -INFINITY;
     }
   }
   tc::fence_before_sync();

@@ -481,7 +481,9 @@ sa_status_t run_select(const SelectArgs& a, cudaStream_t st) {
   p.nq = nq;
   p.nb = nb;
   p.nb_cap = cdiv(a.Ls, a.block);
-  const long long units = static_cast<long long>(groups) * nq;
+  p.nc = cdiv(nq, sa::kScChunk);
+  // units: (group, chunk c, M tile m <= c)
+  const long long units = static_cast<long long>(groups) * p.nc * (p.nc + 1) / 2;
   SA_ARG(units < (1LL << 31), "too many tiles");
   p.units = static_cast<int>(units);
   p.scale = a.scale;
