@@ -331,6 +331,8 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
                             s["out"])
 
     fused_ok = bf and wl.G * wl.T <= 16 and wl.Bk == 64
+    # the step's append runs inside the same launch when the new rows lie in the local block
+    fused_append = fused_ok and (wl.L - wl.T) // wl.Bk == (wl.L - 1) // wl.Bk
     reps = max(10, min(500, K // (4 * R)))
     kern_us = {}
     legs = [("append", app), ("select", sel), ("decode", dec)]
@@ -350,7 +352,11 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
     dec_gbs = kv_b / (dec_ms * 1e-3) / 1e9
     # the step's dominant kernel: the fused selection + attention (sketch scan + selected K/V), or,
     # for shapes without it, the attention kernel
-    if fused_ok:
+    if fused_append:  # the step is one launch: its time is the step time of the timed region
+        top_ms, top_bytes = ms_per_step, step_bytes
+        top_name = ("sa_decode_step (seldec_kernel: cache append, sketch scoring, top-k and sparse attention in "
+                    "one launch)")
+    elif fused_ok:
         top_ms, top_bytes = kern_us["select_decode"] * 1e-3, kv_b + sk_b
         top_name = "sa_select_decode (seldec_kernel: sketch scoring, top-k and sparse attention in one launch)"
     else:
@@ -397,7 +403,8 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
         "config": {
             "workload": "%s decode: B=%d T=%d Hq=%d Hkv=%d d=%d L=%d block=%d top-k=%d + sink + local" % (
                 wl.name, wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, wl.L, wl.Bk, wl.k),
-            "step": ("append+sketch refresh, then score+top-k select and sparse decode in one launch" if fused_ok else
+            "step": ("append+sketch refresh, score+top-k select and sparse decode in one launch" if fused_append else
+                     "append+sketch refresh, then score+top-k select and sparse decode in one launch" if fused_ok else
                      "append+sketch refresh, score+top-k select, split-KV sparse decode") + (
                 " (CUDA graphs of %d steps)" % R),
             "bytes_per_step": {"selected_kv": kv_b, "sketch_scan": sk_b, "append": ap_b},
@@ -430,7 +437,7 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
         "kernels_us": kern_us,
         "topdelta": {"delta": 0.3, "cap": wl.k, "mean_blocks_kept_per_group": round(topdelta_blocks, 2),
                      "select_us": kern_us["select_topdelta"]},
-        "gpu_launches": K * (2 if fused_ok else 4),
+        "gpu_launches": K * (1 if fused_append else 2 if fused_ok else 4),
         "clocks": clocks,
     }
     if rank == 0 and args.cpu_baseline and cpu_seconds > 0:

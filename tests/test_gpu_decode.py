@@ -217,6 +217,46 @@ def test_decode_step_matches_oracle(sa, host_io):
     assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s)
     ref, _ = oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, pos, wl.Bk, wl.scale, _all_rows(wl), o_idx, o_cnt)
     assert_close(host(out).reshape(ref.shape), ref, what="decode step")
+    _check_appended_state(wl, x, kc, vc, sk)
+
+
+def _check_appended_state(wl, x, kc, vc, sk):
+    """After a step: the caches hold the new rows bit for bit and the sketch equals the oracle's."""
+    assert torch.equal(kc.view(torch.int16), dev(x.k).view(torch.int16)), "key cache after the step"
+    assert torch.equal(vc.view(torch.int16), dev(x.v).view(torch.int16)), "value cache after the step"
+    ref = oracle.block_means(x.k, wl.L, wl.Bk)
+    assert_close(host(sk)[:, :, : wl.nb].reshape(ref.shape), ref, atol=1e-6, rtol=1e-5, what="sketch after the step")
+
+
+@pytest.mark.parametrize("T,L", [(4, 8192), (3, 8193), (2, 65)])
+def test_decode_step_multi_token(sa, T, L):
+    """T new rows per step: within one block (the append runs inside the selection + decode launch)
+    and across a block boundary (a launch of its own), with the cache and sketch checked after."""
+    wl = DECODE_CASES["c2"].replace(B=2, L=L, T=T, k=8, needles=2, seed=700 + T)
+    x = synth.make_inputs(wl)
+    pos = wl.L - wl.T
+    kc, vc = dev(x.k).clone(), dev(x.v).clone()
+    kc[:, :, pos:] = 0
+    vc[:, :, pos:] = 0
+    sk = _sketch_buf(wl)
+    sa.sa_build_sketch(kc, pos, wl.Bk, sk)
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
+    idx = torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sa.sa_decode_step_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, sa.SA_BF16, kmax),
+                     dtype=torch.uint8, device="cuda")
+    q = dev(x.q)
+    k_new = dev(x.k)[:, :, pos:].permute(0, 2, 1, 3).contiguous()
+    v_new = dev(x.v)[:, :, pos:].permute(0, 2, 1, 3).contiguous()
+    out = torch.empty_like(q)
+    sa.sa_decode_step(q, k_new, v_new, kc, vc, sk, wl.L, wl.Bk, wl.k, wl.scale, idx, cnt, out, ws)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    o_idx, o_cnt, o_s, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax)
+    assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s)
+    ref, _ = oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, pos, wl.Bk, wl.scale, _all_rows(wl), o_idx, o_cnt)
+    assert_close(host(out).reshape(ref.shape), ref, what="decode step T=%d" % T)
+    _check_appended_state(wl, x, kc, vc, sk)
 
 
 def test_decode_step_graph_replay_reads_new_inputs(sa):

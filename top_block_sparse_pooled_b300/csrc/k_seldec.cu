@@ -85,6 +85,17 @@ struct SdParams {
   __nv_bfloat16* out;      // [B, T, Hq, D]
   int kmax, k, T, Hq, Hkv, G, R, L, Ls, nb, nb_cap, groups;
   int per;      // sketch rows per CTA (a multiple of 64)
+  // Cache append fused in (the decode step; with selection only, when the T new rows [pos, L)
+  // lie in the local block nb - 1 and no scores are returned): k_new / v_new [B, T, Hkv, D]; one
+  // CTA writes the rows into the caches and the block's new sketch row while rank 0 selects.
+  // The local block is kept whatever its score, so the selection does not depend on them; the
+  // CTA that attends over the block takes the new rows from k_new / v_new into its staged tile.
+  const __nv_bfloat16* k_new;  // nullptr: no append
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* kc;  // the caches [groups, Ls, D] (written rows)
+  __nv_bfloat16* vc;
+  float* sketch;      // [groups, nb_cap, D] (the rewritten row)
+  int pos;
   float scale;  // score scale (the softmax scale)
   float qscale;  // softmax scale * log2(e)
   SdLayout lay;
@@ -115,6 +126,56 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
   int v;
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
   return v;
+}
+
+// The cache append of one group, by the 256 consumer threads of the group's CTA rank 0: the T
+// new rows of K and V into the caches, then the local block's sketch row (mean of its rows
+// 64*lb .. L-1, the rows before pos read from the cache and the new ones from k_new; the same
+// thread mapping and summation order as the append kernel's block_mean_rows).  red: 128 * 8
+// floats of shared scratch.
+template <int D>
+__device__ __forceinline__ void append_rows(const SdParams& p, int g, int b, int kvh, float* red) {
+  const int tid = threadIdx.x;
+  constexpr int CPR = D / 8;               // 16-byte chunks per row
+  for (int i = tid; i < p.T * CPR; i += kSdConsumers * 32) {
+    const int t = i / CPR, c = i % CPR;
+    const size_t src = ((static_cast<size_t>(b) * p.T + t) * p.Hkv + kvh) * D + c * 8;
+    const size_t dst = (static_cast<size_t>(g) * p.Ls + p.pos + t) * D + c * 8;
+    *reinterpret_cast<uint4*>(p.kc + dst) = *reinterpret_cast<const uint4*>(p.k_new + src);
+    *reinterpret_cast<uint4*>(p.vc + dst) = *reinterpret_cast<const uint4*>(p.v_new + src);
+  }
+  constexpr int kThr = 128;               // the append kernel's thread count
+  constexpr int RSTEP = kThr / CPR;       // rows in flight per iteration
+  const int lb = p.pos / kSdBk, j0 = lb * kSdBk, nrows = p.L - j0;
+  if (tid < kThr) {
+    const int c = tid % CPR, r0 = tid / CPR;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int r = r0; r < nrows; r += RSTEP) {
+      const int j = j0 + r;
+      const __nv_bfloat16* src = j < p.pos
+                                     ? p.kc + (static_cast<size_t>(g) * p.Ls + j) * D + c * 8
+                                     : p.k_new + ((static_cast<size_t>(b) * p.T + (j - p.pos)) * p.Hkv + kvh) * D + c * 8;
+      const uint4 x = *reinterpret_cast<const uint4*>(src);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[2 * e] += __uint_as_float(w[e] << 16);
+        acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[r0 * D + c * 8 + e] = acc[e];
+  }
+  bar_named(1, kSdConsumers * 32);
+  const float inv = 1.0f / static_cast<float>(nrows);
+  for (int col = tid; col < D; col += kSdConsumers * 32) {
+    float sum = 0.f;
+    for (int rr = 0; rr < RSTEP; ++rr) sum += red[rr * D + col];
+    p.sketch[(static_cast<size_t>(g) * p.nb_cap + lb) * D + col] = sum * inv;
+  }
+  bar_named(1, kSdConsumers * 32);  // red is free again
 }
 
 // grid (CS, clusters), cluster (CS, 1, 1), kSdThreads threads, one CTA per SM.
@@ -289,6 +350,11 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
         for (int i = tid; i < p.kmax; i += kSdConsumers * 32) p.idx[static_cast<size_t>(g) * p.kmax + i] = sel_ptr[i];
         if (tid == 0) p.cnt[g] = *cnt_sh;
       }
+      // the fused cache append: no score the top-k reads depends on it, and the attention takes
+      // the new rows from the inputs, so it runs here, off the critical path, in rank 1 (rank 0
+      // after its top-k when the cluster has one CTA)
+      if (p.k_new && warp < kSdConsumers && static_cast<int>(rank) == (CS > 1 ? 1 : 0))
+        append_rows<D>(p, g, b, kvh, octa);
       cluster_sync();  // the selection is in rank 0's shared memory
     }
     // --------------------------------------------------- this CTA's block list
@@ -381,6 +447,22 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
         if (ok) {
           const uint32_t kt = sbase + st * kStageBytes;
           const uint32_t vt = kt + C::TILEB;
+          if (kSel && p.k_new && blk * kSdBk + kSdBk > p.pos) {
+            // the block holding the appended rows: this warp's rows among them come from the inputs
+            // (the tile was copied from the cache before or while rank 0 wrote them)
+            const int r0 = max(kb, p.pos - blk * kSdBk), r1 = min(kb + 16, p.L - blk * kSdBk);
+            for (int e = lane; e < (r1 > r0 ? r1 - r0 : 0) * (D / 8); e += 32) {
+              const int r = r0 + e / (D / 8), ch = e % (D / 8);
+              const size_t src = ((static_cast<size_t>(b) * p.T + (blk * kSdBk + r - p.pos)) * p.Hkv + kvh) * D + ch * 8;
+              const uint4 kx = *reinterpret_cast<const uint4*>(p.k_new + src);
+              const uint4 vx = *reinterpret_cast<const uint4*>(p.v_new + src);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz_chunk(kt, r, ch)), "r"(kx.x), "r"(kx.y),
+                           "r"(kx.z), "r"(kx.w) : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz_chunk(vt, r, ch)), "r"(vx.x), "r"(vx.y),
+                           "r"(vx.z), "r"(vx.w) : "memory");
+            }
+            __syncwarp();
+          }
           float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
           {
             const int mi = lane >> 3, ri = lane & 7;

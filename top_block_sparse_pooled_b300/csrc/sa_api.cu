@@ -610,6 +610,11 @@ struct SdArgs {
   int B, T, Hq, Hkv, d, L, Ls, k, kmax;
   float scale;
   bool sel;
+  // the decode step's cache append, fused (see SdParams::k_new)
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  float* sketch_w = nullptr;
+  int pos = 0;
 };
 
 constexpr int kSdMinSmem = 120 * 1024;  // keeps the kernel at one CTA per SM
@@ -708,6 +713,12 @@ sa_status_t launch_seldec(const SdArgs& a, cudaStream_t st) {
   p.nb_cap = nb_cap;
   p.groups = groups;
   p.per = per;
+  p.k_new = kSel ? static_cast<const __nv_bfloat16*>(a.k_new) : nullptr;
+  p.v_new = kSel ? static_cast<const __nv_bfloat16*>(a.v_new) : nullptr;
+  p.kc = static_cast<__nv_bfloat16*>(const_cast<void*>(a.kc));
+  p.vc = static_cast<__nv_bfloat16*>(const_cast<void*>(a.vc));
+  p.sketch = a.sketch_w;
+  p.pos = a.pos;
   p.scale = a.scale;
   p.qscale = a.scale * 1.4426950408889634f;
   p.lay = lay;
@@ -1172,6 +1183,46 @@ int sa_select_kmax(int L, int block, int qtile, int prefill, int k, int frac_num
   return select_kmax(L, block, qtile, prefill, k, frac_num, frac_den);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The fused selection + decode, optionally with the decode step's cache append in front (k_new
+// and v_new [B, T, Hkv, d], written at rows L - T .. L - 1; the caller checks that the rows lie in
+// the local block and that no scores are returned, and the sketch is then writable).
+sa_status_t select_decode_impl(const void* q, int dtype, const float* sketch, const void* k_cache,
+                               const void* v_cache, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
+                               int block, int k, float scale, int32_t* idx, int32_t* cnt, int kmax, float* scores,
+                               void* out, const void* k_new, const void* v_new, cudaStream_t st) {
+  SelectArgs sel{SA_SELECT_SKETCH, q, dtype, sketch, scores, B, T, Hq, Hkv, d, L, L_stride, block, 0, 0, k,
+                 0, 1, scale, idx, cnt, kmax};
+  SA_TRY(validate_select(sel));
+  SA_SUP(seldec_fits(dtype, block, Hq / Hkv, T),
+         "fused selection + decode supports bf16, block == %d and G*T <= %d (got dtype %d, block %d, G*T %d)",
+         sa::kSdBk, sa::kSdRmax, dtype, block, (Hq / Hkv) * T);
+  SA_ARG(k_cache && v_cache && out, "null pointer argument");
+  SA_ARG(aligned16(k_cache) && aligned16(v_cache) && aligned16(out), "k/v caches and out must be 16-byte aligned");
+  SA_ARG(T <= block && T <= L, "T (%d) must be <= block and <= L", T);
+  SA_ARG(static_cast<long long>(B) * Hkv * L_stride < (1LL << 31), "B*Hkv*L_stride too large");
+  SA_ARG(scale > 0.f && scale < 1e30f, "scale must be positive and finite");
+  if (k_new) {
+    SA_ARG(v_new && aligned16(k_new) && aligned16(v_new), "k_new and v_new must be 16-byte aligned");
+    SA_ARG((L - T) / block == (L - 1) / block && scores == nullptr, "fused append needs one local block, no scores");
+  }
+  DevInfo di;
+  SA_TRY(dev_info(&di));
+  SdArgs a{q, k_cache, v_cache, sketch, idx, cnt, scores, out, B, T, Hq, Hkv, d, L, L_stride, k, kmax, scale, true};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.sketch_w = const_cast<float*>(sketch);
+  a.pos = L - T;
+  return run_seldec(a, st);
+}
+
+}  // namespace
+
+extern "C" {
+
 sa_status_t sa_select_topk(int mode, const void* q, int dtype, const float* sketch, float* scores, int B, int Tq,
                            int Hq, int Hkv, int d, int L, int L_stride, int block, int qtile, int prefill, int k,
                            int frac_num, int frac_den, float scale, int32_t* idx, int32_t* cnt, int kmax,
@@ -1214,22 +1265,8 @@ sa_status_t sa_select_decode(const void* q, int dtype, const float* sketch, cons
                              int B, int T, int Hq, int Hkv, int d, int L, int L_stride, int block, int k, float scale,
                              int32_t* idx, int32_t* cnt, int kmax, float* scores, void* out, void* stream) {
   t_err.clear();
-  SelectArgs sel{SA_SELECT_SKETCH, q, dtype, sketch, scores, B, T, Hq, Hkv, d, L, L_stride, block, 0, 0, k,
-                 0, 1, scale, idx, cnt, kmax};
-  SA_TRY(validate_select(sel));
-  SA_SUP(seldec_fits(dtype, block, Hq / Hkv, T),
-         "fused selection + decode supports bf16, block == %d and G*T <= %d (got dtype %d, block %d, G*T %d)",
-         sa::kSdBk, sa::kSdRmax, dtype, block, (Hq / Hkv) * T);
-  SA_ARG(k_cache && v_cache && out, "null pointer argument");
-  SA_ARG(aligned16(k_cache) && aligned16(v_cache) && aligned16(out), "k/v caches and out must be 16-byte aligned");
-  SA_ARG(T <= block && T <= L, "T (%d) must be <= block and <= L", T);
-  SA_ARG(static_cast<long long>(B) * Hkv * L_stride < (1LL << 31), "B*Hkv*L_stride too large");
-  SA_ARG(scale > 0.f && scale < 1e30f, "scale must be positive and finite");
-  DevInfo di;
-  SA_TRY(dev_info(&di));
-  const SdArgs a{q, k_cache, v_cache, sketch, idx, cnt, scores, out, B, T, Hq, Hkv, d, L, L_stride, k, kmax, scale,
-                 true};
-  return run_seldec(a, as_stream(stream));
+  return select_decode_impl(q, dtype, sketch, k_cache, v_cache, B, T, Hq, Hkv, d, L, L_stride, block, k, scale, idx,
+                            cnt, kmax, scores, out, nullptr, nullptr, as_stream(stream));
 }
 
 sa_status_t sa_decode_tokens(const void* q, const void* k_cache, const void* v_cache, int dtype, const int32_t* idx,
@@ -1417,13 +1454,24 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
     outd = out_mapped ? out_map : out_dev;
   }
   void* sp = static_cast<void*>(st);
-  SA_TRY(sa_append_kv(knd, vnd, a.dtype, a.B, a.Hkv, a.T, a.d, a.k_cache, a.v_cache, a.L_stride, a.L - a.T, a.block,
-                      a.sketch, sp));
-  if (seldec_fits(a.dtype, a.block, a.Hq / a.Hkv, a.T)) {
+  const bool fused = seldec_fits(a.dtype, a.block, a.Hq / a.Hkv, a.T);
+  // the append runs inside the fused launch when its rows lie in the local block (kept whatever
+  // its score) and no scores are returned; otherwise it is a launch of its own
+  const bool fused_append = fused && a.L >= a.T && a.T >= 1 && (a.L - a.T) / a.block == (a.L - 1) / a.block &&
+                            a.scores == nullptr;
+  if (fused_append) {
+    SA_ARG(a.k_cache && a.v_cache && a.sketch, "null pointer argument");
+    SA_TRY(select_decode_impl(qd, a.dtype, a.sketch, a.k_cache, a.v_cache, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
+                              a.L_stride, a.block, a.k, a.scale, a.idx, a.cnt, a.kmax, a.scores, outd, knd, vnd, st));
+  } else if (fused) {
+    SA_TRY(sa_append_kv(knd, vnd, a.dtype, a.B, a.Hkv, a.T, a.d, a.k_cache, a.v_cache, a.L_stride, a.L - a.T,
+                        a.block, a.sketch, sp));
     // selection and attention in one launch (one cluster per group)
     SA_TRY(sa_select_decode(qd, a.dtype, a.sketch, a.k_cache, a.v_cache, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
                             a.L_stride, a.block, a.k, a.scale, a.idx, a.cnt, a.kmax, a.scores, outd, sp));
   } else {
+    SA_TRY(sa_append_kv(knd, vnd, a.dtype, a.B, a.Hkv, a.T, a.d, a.k_cache, a.v_cache, a.L_stride, a.L - a.T,
+                        a.block, a.sketch, sp));
     SA_TRY(sa_select_topk(SA_SELECT_SKETCH, qd, a.dtype, a.sketch, a.scores, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
                           a.L_stride, a.block, 0, 0, a.k, 0, 1, a.scale, a.idx, a.cnt, a.kmax, sp));
     SA_TRY(sa_decode(qd, a.k_cache, a.v_cache, a.dtype, a.idx, a.cnt, a.kmax, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
