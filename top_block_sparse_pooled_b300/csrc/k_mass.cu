@@ -27,9 +27,26 @@
 // TMEM: S_t[buf] at columns (2t + buf) * 128.
 #pragma once
 
+#include "sa_f32x2.cuh"
 #include "sa_tc.cuh"
 
 namespace sa {
+
+// sum over e of 2^(s[e] * qscale - sub), keys taken in pairs
+__device__ __forceinline__ float ms_exp2_sum(const float (&s)[128], float qscale, float sub) {
+  const uint64_t qs2 = f2_pack(qscale, qscale), ns2 = f2_pack(-sub, -sub);
+  uint64_t a2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+  for (int e = 0; e < 128; e += 2) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), qs2, ns2), x0, x1);
+    a2[(e >> 1) & 1] = f2_add(a2[(e >> 1) & 1], f2_pack(ex2_approx(x0), ex2_approx(x1)));
+  }
+  float c0, c1, c2, c3;
+  f2_unpack(a2[0], c0, c1);
+  f2_unpack(a2[1], c2, c3);
+  return (c0 + c1) + (c2 + c3);
+}
 
 constexpr int kMsStages = 3;
 constexpr int kMsThreads = 384;
@@ -210,27 +227,20 @@ __global__ void __launch_bounds__(kMsThreads, 1) mass_kernel(const __grid_consta
             float rs = 0.f;
             if (pass == 0) {
               // online log-sum-exp (base 2): block max first, then one exp per key
-              float m8[8];
+              float m4[4];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+              for (int e = 0; e < 4; ++e) m4[e] = -INFINITY;
 #pragma unroll
-              for (int e = 0; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[e]);
-              float bm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+              for (int e = 0; e < 128; e += 2) m4[(e >> 1) & 3] = f2_max3(m4[(e >> 1) & 3], s[e], s[e + 1]);
+              float bm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
               bm = (bm == -INFINITY) ? -INFINITY : bm * p.qscale;
               const float mn = fmaxf(m, bm);
               if (mn != -INFINITY) {
-                float c4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int e = 0; e < 128; ++e) c4[e & 3] += ex2_approx(fmaf(s[e], p.qscale, -mn));
-                l = l * ex2_approx(m - mn) + ((c4[0] + c4[1]) + (c4[2] + c4[3]));
+                l = l * ex2_approx(m - mn) + ms_exp2_sum(s, p.qscale, mn);
                 m = mn;
               }
             } else {
-              float c4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-              for (int e = 0; e < 128; ++e) c4[e & 3] += ex2_approx(fmaf(s[e], p.qscale, -lse2));
-              rs = (c4[0] + c4[1]) + (c4[2] + c4[3]);
+              rs = ms_exp2_sum(s, p.qscale, lse2);
             }
             if (pass == 1) {
 #pragma unroll

@@ -33,6 +33,7 @@
 // MMA issuer drain what they issued, and TMEM is freed before exit.
 #pragma once
 
+#include "sa_f32x2.cuh"
 #include "sa_tc.cuh"
 
 namespace sa {
@@ -276,7 +277,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         ++s_waits;
         tc::fence_after_sync();
         // the whole S row in registers (one TMEM round trip), then the row max
-        // over the visible keys (raw dot products; qscale > 0), eight chains
+        // over the visible keys (raw dot products; qscale > 0), four chains of
+        // three-input max
         const int kbase = blk * kPfKeys;
         const bool full = kbase + kPfKeys - 1 <= qpos && kbase + kPfKeys <= p.L;
         const int lim = full ? kPfKeys - 1 : min(qpos, p.L - 1) - kbase;  // last visible key column
@@ -290,12 +292,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         }
         float mx;
         {
-          float m8[8];
+          float m4[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) m8[e] = sr[e];
+          for (int e = 0; e < 4; ++e) m4[e] = fmaxf(sr[2 * e], sr[2 * e + 1]);
 #pragma unroll
-          for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], sr[e]);
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int e = 8; e < 128; e += 2) m4[(e >> 1) & 3] = f2_max3(m4[(e >> 1) & 3], sr[e], sr[e + 1]);
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
         mx = (mx == -INFINITY) ? -INFINITY : mx * p.qscale;
         // lazy rescale: the running max moves only when it grows by more than
@@ -306,19 +308,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // P = exp2(S * qscale - m) as bf16 pairs into columns 0-63 of S_t (the S
         // values are all in registers already; masked keys are -inf, giving 0)
         const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t qs2 = f2_pack(p.qscale, p.qscale), nm2 = f2_pack(-mu, -mu);
+        uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a0 = ex2_approx(fmaf(sr[32 * c + 2 * e], p.qscale, -mu));
-            const float a1 = ex2_approx(fmaf(sr[32 * c + 2 * e + 1], p.qscale, -mu));
-            ls4[e & 3] += a0 + a1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sr[32 * c + 2 * e], sr[32 * c + 2 * e + 1]), qs2, nm2), x0, x1);
+            const float a0 = ex2_approx(x0), a1 = ex2_approx(x1);
+            ls2[e & 1] = f2_add(ls2[e & 1], f2_pack(a0, a1));
             pk[e] = pack_bf16x2(a0, a1);
           }
           tc::tmem_st16(s_addr + 16 * c, pk);
         }
+        float ls4[4];
+        f2_unpack(ls2[0], ls4[0], ls4[1]);
+        f2_unpack(ls2[1], ls4[2], ls4[3]);
         if (jj > 0) {  // PV_t of the previous block has completed: O_t is stable
           if (ok) ok = mbar_wait(bar(PfSmem::O_BAR + t), o_waits & 1);
           ok = __all_sync(0xFFFFFFFFu, ok);
