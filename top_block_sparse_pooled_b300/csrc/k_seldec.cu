@@ -20,13 +20,15 @@
 //                       the list, the selected blocks at positions r, r + CS, ...
 //                       (without selection, the share is read from idx / cnt).
 //   A                   the CTA streams its blocks' K and V tiles and keeps an
-//                       online softmax per query row; its partial (max, sum,
-//                       unnormalised output rows) goes to its shared memory.
-//   merge               output row r is merged by CTA r % CS: every CTA pushes
-//                       its partial rows into their receivers' shared memory
-//                       and arrives on the receivers' mbarriers; a receiver
-//                       combines the CS partials (exact rescaling) and writes
-//                       the row.
+//                       online softmax per query row and warp; each warp then
+//                       parks its unscaled state (max, sum, output rows) in
+//                       its own slot over the ring.
+//   merge               output row r is merged by CTA r % CS: every CTA
+//                       combines its eight warp slots per row (exact
+//                       rescaling) while pushing the row into its receiver's
+//                       shared memory, then arrives on the receivers'
+//                       mbarriers; a receiver combines the CS partials the
+//                       same way and writes the row.
 //
 // Roles (288 threads): warps 0-7 consumers in two quads (quad q takes the ring
 // stages of sequence numbers v with v % 2 == q, so the two quads work on
@@ -58,8 +60,17 @@ constexpr int kSdRecvRows = 32;      // >= CS * ceil(R / CS) for CS <= 16, R <= 
 // same number of bytes.
 struct SdLayout {
   int nstages, D, nb, kmax, sel;
+  // After the attention, each consumer warp parks its partial rows (kSdRmax rows of D floats,
+  // padded to a row stride of D + 8 words so that the warp's fragment stores hit distinct banks)
+  // over the ring, which is at least that large.
+  __host__ __device__ static constexpr int slot_stride(int d) { return d + 8; }
   __host__ __device__ int stage_bytes() const { return 2 * kSdBk * D * 2; }
-  __host__ __device__ int q_off() const { return nstages * stage_bytes(); }
+  __host__ __device__ int ring_bytes() const {
+    const int slots = kSdConsumers * kSdRmax * slot_stride(D) * 4;
+    const int ring = nstages * stage_bytes();
+    return ring > slots ? ring : ((slots + 1023) / 1024) * 1024;
+  }
+  __host__ __device__ int q_off() const { return ring_bytes(); }
   __host__ __device__ int all_off() const { return q_off() + kSdRmax * D * 2; }
   __host__ __device__ int topk_off() const { return all_off() + (sel ? ((nb * 4 + 15) / 16) * 16 : 0); }
   __host__ __device__ int sel_off() const {
@@ -67,9 +78,8 @@ struct SdLayout {
   }
   __host__ __device__ int list_off() const { return sel_off() + ((kmax * 4 + 4 + 15) / 16) * 16; }
   __host__ __device__ int mlw_off() const { return list_off() + ((kmax * 4 + 15) / 16) * 16; }
-  __host__ __device__ int octa_off() const { return mlw_off() + kSdConsumers * kSdRmax * 8; }
-  __host__ __device__ int mlc_off() const { return octa_off() + kSdRmax * D * 4; }
-  __host__ __device__ int misc_off() const { return mlc_off() + kSdRmax * 8; }
+  __host__ __device__ int red_off() const { return mlw_off() + kSdConsumers * kSdRmax * 8; }
+  __host__ __device__ int misc_off() const { return red_off() + 128 * 8 * 4; }
   // partial rows pushed here by every CTA of the cluster: slot (sender, row) of D floats, then
   // the row's (max, sum) and two pad words
   __host__ __device__ int recv_off() const { return misc_off() + 16; }
@@ -199,8 +209,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
   int32_t* sel_ptr = reinterpret_cast<int32_t*>(smem + lay.sel_off());
   int32_t* list = reinterpret_cast<int32_t*>(smem + lay.list_off());  // this CTA's blocks (-1: skip)
   float* mlw = reinterpret_cast<float*>(smem + lay.mlw_off());        // [warp][row] (max, sum)
-  float* octa = reinterpret_cast<float*>(smem + lay.octa_off());      // [R][D] this CTA's partial
-  float* mlc = reinterpret_cast<float*>(smem + lay.mlc_off());        // [R] (max, sum)
+  float* red = reinterpret_cast<float*>(smem + lay.red_off());        // the append's sketch scratch
   int* misc = reinterpret_cast<int*>(smem + lay.misc_off());          // [0]: entries in list
   const uint32_t full0 = sbase + lay.bar_off();
   const uint32_t empty0 = full0 + 8 * NS;
@@ -354,7 +363,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
       // the new rows from the inputs, so it runs here, off the critical path, in rank 1 (rank 0
       // after its top-k when the cluster has one CTA)
       if (p.k_new && warp < kSdConsumers && static_cast<int>(rank) == (CS > 1 ? 1 : 0))
-        append_rows<D>(p, g, b, kvh, octa);
+        append_rows<D>(p, g, b, kvh, red);
       cluster_sync();  // the selection is in rank 0's shared memory
     }
     // --------------------------------------------------- this CTA's block list
@@ -402,7 +411,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
         for (uint32_t u = (v > vi + NS ? v - NS : vi); u < v; ++u) mbar_wait_drain(full0 + 8 * (u % NS), (u / NS) & 1);
       }
       __syncwarp();
-      bar_named(3, kSdThreads);  // the consumers' merge staging (in the ring) is done
+      bar_named(3, kSdThreads);  // the consumers' slots (over the ring) are read
     } else {
       const int quad = warp >> 2, wq = warp & 3;
       const int gq = lane >> 2, tq = lane & 3;
@@ -532,11 +541,20 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
       }
-      // ---- merge the eight warp states into this CTA's partial (fixed order)
+      // ---- park this warp's unscaled state (o, and the row's max and sum) in its own slot;
+      // the slots overlay the ring, which every warp has finished reading after this barrier
       l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
       l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
       l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
       l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+      bar_named(1, kSdConsumers * 32);
+      float* slot = reinterpret_cast<float*>(smem) + static_cast<size_t>(warp) * kSdRmax * SdLayout::slot_stride(D);
+#pragma unroll
+      for (int j = 0; j < C::NT; ++j) {
+        const int col = j * 8 + 2 * tq;
+        if (r0 < p.R) *reinterpret_cast<float2*>(slot + r0 * SdLayout::slot_stride(D) + col) = make_float2(o[j][0], o[j][1]);
+        if (r1 < p.R) *reinterpret_cast<float2*>(slot + r1 * SdLayout::slot_stride(D) + col) = make_float2(o[j][2], o[j][3]);
+      }
       if (tq == 0) {
         if (r0 < p.R) {
           mlw[(warp * kSdRmax + r0) * 2] = m0;
@@ -548,74 +566,6 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
         }
       }
       bar_named(1, kSdConsumers * 32);
-      float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kSdConsumers; ++w) {
-        if (r0 < p.R) M0 = fmaxf(M0, mlw[(w * kSdRmax + r0) * 2]);
-        if (r1 < p.R) M1 = fmaxf(M1, mlw[(w * kSdRmax + r1) * 2]);
-      }
-      {
-        const float c0 = exp2f(m0 - ((M0 == -INFINITY) ? 0.f : M0));
-        const float c1 = exp2f(m1 - ((M1 == -INFINITY) ? 0.f : M1));
-#pragma unroll
-        for (int j = 0; j < C::NT; ++j) {
-          o[j][0] *= c0;
-          o[j][1] *= c0;
-          o[j][2] *= c1;
-          o[j][3] *= c1;
-        }
-      }
-      // staging: [4][R][D] fp32 in the ring (every stage has been consumed; the
-      // producer issues nothing more until barrier 3)
-      float* stg = reinterpret_cast<float*>(smem) + static_cast<size_t>(wq) * kSdRmax * D;
-      if (quad == 1) {
-#pragma unroll
-        for (int j = 0; j < C::NT; ++j) {
-          const int col = j * 8 + 2 * tq;
-          if (r0 < p.R) *reinterpret_cast<float2*>(stg + r0 * D + col) = make_float2(o[j][0], o[j][1]);
-          if (r1 < p.R) *reinterpret_cast<float2*>(stg + r1 * D + col) = make_float2(o[j][2], o[j][3]);
-        }
-      }
-      bar_named(1, kSdConsumers * 32);
-      if (quad == 0) {
-#pragma unroll
-        for (int j = 0; j < C::NT; ++j) {
-          const int col = j * 8 + 2 * tq;
-          if (r0 < p.R) {
-            float2* a = reinterpret_cast<float2*>(stg + r0 * D + col);
-            const float2 x = *a;
-            *a = make_float2(o[j][0] + x.x, o[j][1] + x.y);
-          }
-          if (r1 < p.R) {
-            float2* a = reinterpret_cast<float2*>(stg + r1 * D + col);
-            const float2 x = *a;
-            *a = make_float2(o[j][2] + x.x, o[j][3] + x.y);
-          }
-        }
-      }
-      bar_named(1, kSdConsumers * 32);
-      const float* s0p = reinterpret_cast<const float*>(smem);
-      for (int e = tid; e < p.R * D / 4; e += kSdConsumers * 32) {
-        const float4 a = reinterpret_cast<const float4*>(s0p)[e];
-        const float4 bb = reinterpret_cast<const float4*>(s0p + kSdRmax * D)[e];
-        const float4 c = reinterpret_cast<const float4*>(s0p + 2 * kSdRmax * D)[e];
-        const float4 d = reinterpret_cast<const float4*>(s0p + 3 * kSdRmax * D)[e];
-        reinterpret_cast<float4*>(octa)[e] =
-            make_float4(((a.x + bb.x) + c.x) + d.x, ((a.y + bb.y) + c.y) + d.y, ((a.z + bb.z) + c.z) + d.z,
-                        ((a.w + bb.w) + c.w) + d.w);
-      }
-      if (tid < p.R) {
-        float M = -INFINITY;
-        for (int w = 0; w < kSdConsumers; ++w) M = fmaxf(M, mlw[(w * kSdRmax + tid) * 2]);
-        const float mu = (M == -INFINITY) ? 0.f : M;
-        float lsum = 0.f;
-        for (int w = 0; w < kSdConsumers; ++w)
-          lsum = fmaf(mlw[(w * kSdRmax + tid) * 2 + 1], exp2f(mlw[(w * kSdRmax + tid) * 2] - mu), lsum);
-        mlc[2 * tid] = M;
-        mlc[2 * tid + 1] = lsum;
-      }
-      fence_proxy_async_smem();  // staging writes (generic proxy) before later copies into the ring
-      bar_named(3, kSdThreads);
     }
     vi += 0;  // (sequence numbers advanced below, identically in every role)
     {
@@ -631,16 +581,38 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
     if (warp < kSdConsumers) {
       const int rpr = (p.R + CS - 1) / CS;  // rows per receiver
       const uint32_t recv_a = sbase + lay.recv_off();
+      const float* slots = reinterpret_cast<const float*>(smem);
+      constexpr int SS = SdLayout::slot_stride(D);
+      // this CTA's partial row r = the eight warp states rescaled to their common max (fixed
+      // order), pushed into slot (rank, r / CS) of receiver r % CS
       for (int e = tid; e < p.R * (D / 4); e += kSdConsumers * 32) {
         const int r = e / (D / 4), c4 = e % (D / 4);
-        const uint32_t slot = static_cast<uint32_t>(static_cast<int>(rank) * rpr + r / CS);
-        st_cluster_f32x4(map_cluster(recv_a + (slot * (D + 4) + c4 * 4) * 4u, r % CS),
-                         reinterpret_cast<const float4*>(octa)[e]);
+        float mw[kSdConsumers];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kSdConsumers; ++w) {
+          mw[w] = mlw[(w * kSdRmax + r) * 2];
+          M = fmaxf(M, mw[w]);
+        }
+        const float mu = (M == -INFINITY) ? 0.f : M;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSdConsumers; ++w) {
+          const float wt = exp2f(mw[w] - mu);
+          const float4 x = *reinterpret_cast<const float4*>(slots + (w * kSdRmax + r) * SS + c4 * 4);
+          acc.x = fmaf(x.x, wt, acc.x);
+          acc.y = fmaf(x.y, wt, acc.y);
+          acc.z = fmaf(x.z, wt, acc.z);
+          acc.w = fmaf(x.w, wt, acc.w);
+          lsum = fmaf(mlw[(w * kSdRmax + r) * 2 + 1], wt, lsum);
+        }
+        const uint32_t rs = static_cast<uint32_t>(static_cast<int>(rank) * rpr + r / CS);
+        st_cluster_f32x4(map_cluster(recv_a + (rs * (D + 4) + c4 * 4) * 4u, r % CS), acc);
+        if (c4 == 0) st_cluster_f32x2(map_cluster(recv_a + (rs * (D + 4) + D) * 4u, r % CS), M, lsum);
       }
-      if (tid < p.R) {
-        const uint32_t slot = static_cast<uint32_t>(static_cast<int>(rank) * rpr + tid / CS);
-        st_cluster_f32x2(map_cluster(recv_a + (slot * (D + 4) + D) * 4u, tid % CS), mlc[2 * tid], mlc[2 * tid + 1]);
-      }
+      fence_proxy_async_smem();  // slot writes (generic proxy) before later copies into the ring
+      bar_named(3, kSdThreads);  // the slots are read: the producer may refill the ring
       bar_named(1, kSdConsumers * 32);  // every push of this CTA is issued before the arrivals
       const int nrecv = min(CS, p.R);
       if (tid < nrecv) mbar_arrive_remote(map_cluster(recvbar, tid));
