@@ -10,7 +10,8 @@
 // each softmax taken over the row's whole causal range (dense, not sparse).
 //
 // Work unit: (group, query tile i), tiles in descending order (tile i has i+1
-// causal blocks), round-robin over a persistent grid of one CTA per SM.  A
+// causal blocks), dealt in alternating directions (snake_unit) over a
+// persistent grid of one CTA per SM.  A
 // unit walks the group's heads two at a time (two 128-row M tiles sharing each
 // K tile) and makes two passes over its causal blocks:
 //   pass 1: row log-sum-exp (online max and sum, base 2);
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kMsThreads, 1) mass_kernel(const __grid_consta
     if (lane == 0) {
       uint32_t kit = 0, qn = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd)) {
         const int i = p.nq - 1 - u / per_i, g = u % per_i;
         const int b = g / p.Hkv, kvh = g % p.Hkv;
         const int nc = (min((i + 1) * kPfRows, p.L) - 1) / kPfKeys + 1;  // causal blocks
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kMsThreads, 1) mass_kernel(const __grid_consta
       uint32_t kit = 0, qn = 0;
       uint32_t sit[2] = {0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd)) {
         const int i = p.nq - 1 - u / per_i;
         const int nc = (min((i + 1) * kPfRows, p.L) - 1) / kPfKeys + 1;
         for (int pair = 0; pair < p.npairs; ++pair, ++qn) {
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kMsThreads, 1) mass_kernel(const __grid_consta
     uint32_t sit = 0;
     bool ok = true;
     float* my_acc = acc + (t * 4 + wq) * p.nb;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd)) {
       const int i = p.nq - 1 - u / per_i, g = u % per_i;
       const int qpos = i * kPfRows + r;
       const bool live = qpos < p.L;

@@ -9,8 +9,9 @@
 // Work unit: (group g = (b, kv-head), query tile i, head pair).  The two heads
 // of a pair share every K/V tile the CTA loads (GQA), each head being one
 // 128-row M tile.  Units are ordered longest first (tile i descending: tile i
-// has up to i + 1 causal blocks) and dealt round-robin to a persistent grid of
-// one CTA per SM.
+// has up to i + 1 causal blocks) and dealt to a persistent grid of one CTA per
+// SM in alternating directions (snake_unit), which evens out the CTAs'
+// totals.
 //
 // Roles (320 threads, kPfThreads):
 //   warp 0    TMA producer: the unit's Q tiles (3-D map: d, head, row), then
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       uint32_t it = 0;  // K/V ring iteration (valid blocks, across units)
       int nu = 0;       // units processed
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+      for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd), ++nu) {
         const PfUnit w = pf_unit(p, u);
         if (nu > 0 && ok) ok = mbar_wait(bar(PfSmem::Q_EMPTY), (nu - 1) & 1);
         mbar_arrive_expect_tx(bar(PfSmem::Q_FULL), w.nt * kPfTile);
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       uint32_t units_t[2] = {0, 0};    // earlier units in which M tile t was active
       bool pv_pending[2] = {false, false};
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+      for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd), ++nu) {
         const PfUnit w = pf_unit(p, u);
         if (ok) ok = mbar_wait(bar(PfSmem::Q_FULL), nu & 1);
         tc::fence_after_sync();
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const uint32_t o_addr = lane_base + 256 + t * 128;
     uint32_t s_waits = 0, o_waits = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd)) {
       const PfUnit w = pf_unit(p, u);
       if (t >= w.nt) continue;
       const int qpos = w.i * kPfRows + r;  // query position of this row

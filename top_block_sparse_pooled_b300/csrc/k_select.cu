@@ -592,6 +592,237 @@ __device__ __forceinline__ void block_topk_hist_impl(LoadF score, int n, int bud
   topk_output<Sync>(score, n, take, true, thr, need_eq, kmax, idx_out, cnt_out, S);
 }
 
+// Register-resident selection for n <= 16 * kSelThreads candidates: the same
+// selection as block_topk_impl (forced first and last index; the take highest
+// keys among 1 .. n-2, ties to the lower index; ascending output).  Warp w owns
+// the indices [32*M*w, 32*M*(w+1)); its lane l holds indices 32*M*w + 32*j + l,
+// j < M, in registers (conflict-free loads, every score read once).
+// Threshold: one value histogram (kHistBins linear bins over the candidates'
+// key range, a monotone map) locates the bin b* of the take-th largest key.
+// When all of b*'s keys are needed (the usual case: the bin holds one key), the
+// selection is every key with a bin >= b*; otherwise b*'s keys (at most
+// kHistCand) are gathered and ranked directly for the exact threshold key and
+// the number of its ties to admit (lowest indices first).  Output: per-row
+// ballots of the sure and the tied keys give each selected index its position
+// from the warp's prefix counts.  Five barriers in the usual case (range,
+// histogram, bin totals, bin choice, warp counts), seven with the bin ranked.
+// Returns false (nothing written, every thread returning together) when the
+// key range has no finite positive width or the threshold bin holds more than
+// kHistCand keys; the caller then synchronises and runs the general selection.
+template <int M, typename Sync, typename LoadF>
+__device__ __forceinline__ bool block_topk_reg(LoadF score, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
+                                               int32_t* __restrict__ cnt_out, uint32_t S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t hist = S + static_cast<uint32_t>(offsetof(TopkShared, hist));
+  const uint32_t cand = S + static_cast<uint32_t>(offsetof(TopkShared, cand));
+  const uint32_t wmax = S + static_cast<uint32_t>(offsetof(TopkShared, wmax));
+  const uint32_t wmin = S + static_cast<uint32_t>(offsetof(TopkShared, wmin));
+  const uint32_t wdef = S + static_cast<uint32_t>(offsetof(TopkShared, wdef));
+  const uint32_t weq = S + static_cast<uint32_t>(offsetof(TopkShared, weq));
+  const uint32_t bsel = S + static_cast<uint32_t>(offsetof(TopkShared, bsel));
+  const uint32_t fin_thr = S + static_cast<uint32_t>(offsetof(TopkShared, fin_thr));
+  const uint32_t fin_need = S + static_cast<uint32_t>(offsetof(TopkShared, fin_need));
+  const int last = n - 1;
+  const int ncand = n > 2 ? n - 2 : 0;
+  const int take = budget <= 0 ? 0 : (budget < ncand ? budget : ncand);
+  const bool by_key = take > 0 && take < ncand;
+  const int i0 = 32 * M * warp + lane;  // index of row j: i0 + 32 * j
+  const uint32_t lt = (1u << lane) - 1u;
+  float v[M];
+  uint32_t key[M];
+#pragma unroll
+  for (int j = 0; j < M; ++j) {
+    const int b = i0 + 32 * j;
+    v[j] = (b >= 1 && b < last) ? score(b) : 0.f;
+  }
+  // selection rule: by bin (every key whose bin is >= b*) when the threshold bin is taken
+  // whole, else by key (keys above thr, and the first need_eq keys equal to it)
+  int bstar = 0;
+  bool by_bin = false;
+  uint32_t thr = 0u, need_eq = 0u;
+  int bn[M];
+#pragma unroll
+  for (int j = 0; j < M; ++j) {
+    key[j] = float_key(v[j]);
+    bn[j] = 0;
+  }
+  if (by_key) {
+    uint32_t kmx = 0u, kmn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+      const int b = i0 + 32 * j;
+      if (b >= 1 && b < last) {
+        kmx = max(kmx, key[j]);
+        kmn = min(kmn, key[j]);
+      }
+    }
+    kmx = __reduce_max_sync(0xFFFFFFFFu, kmx);
+    kmn = __reduce_min_sync(0xFFFFFFFFu, kmn);
+    if (lane == 0) {
+      sts_u32(wmax + 4u * warp, kmx);
+      sts_u32(wmin + 4u * warp, kmn);
+    }
+    for (int i = tid; i < kHistBins / 4; i += kSelThreads)
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(hist + 16u * i), "r"(0u) : "memory");
+    if (tid == 0) sts_u32(bsel + 12u, 0u);
+    Sync::sync();  // 1: key range, cleared histogram
+    uint32_t klo = 0xFFFFFFFFu, khi = 0u;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) {
+      khi = max(khi, lds_u32(wmax + 4u * w));
+      klo = min(klo, lds_u32(wmin + 4u * w));
+    }
+    if (klo == khi) {  // every candidate has the threshold key
+      thr = klo;
+      need_eq = static_cast<uint32_t>(take);
+    } else {
+      const float smin = key_float(klo), smax = key_float(khi);
+      const float inv = static_cast<float>(kHistBins) / (smax - smin);
+      if (!(inv > 0.f && inv < 3.0e38f && smax - smin < 3.0e38f)) return false;  // uniform
+#pragma unroll
+      for (int j = 0; j < M; ++j) {
+        const int b = i0 + 32 * j;
+        // bin = floor((v - smin) * inv) clamped to the last bin: a monotone map of the score
+        // (the floor by a round-down add of 2^23, whose low mantissa bits are then the integer)
+        const float f = fminf((v[j] - smin) * inv, static_cast<float>(kHistBins - 1));
+        bn[j] = __float_as_int(__fadd_rd(f, 8388608.0f)) - 0x4B000000;
+        if (b >= 1 && b < last) red_add_shared(hist + 4u * static_cast<uint32_t>(bn[j]), 1u);
+      }
+      Sync::sync();  // 2: histogram
+      // thread t holds bins kHistBins-1-8t .. kHistBins-8-8t (descending)
+      uint32_t c[8];
+      {
+        const uint4 hi4 = lds_u32x4(hist + 4u * (kHistBins - 4 - 8 * tid));
+        const uint4 lo4 = lds_u32x4(hist + 4u * (kHistBins - 8 - 8 * tid));
+        c[0] = hi4.w; c[1] = hi4.z; c[2] = hi4.y; c[3] = hi4.x;
+        c[4] = lo4.w; c[5] = lo4.z; c[6] = lo4.y; c[7] = lo4.x;
+      }
+      const uint32_t sum = ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));
+      uint32_t inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) sts_u32(wdef + 4u * warp, inc);
+      Sync::sync();  // 3: warp totals of the bins
+      uint32_t run = inc - sum;
+#pragma unroll
+      for (int w = 0; w < kSelWarps; ++w) run += w < warp ? lds_u32(wdef + 4u * w) : 0u;
+      const uint32_t remaining = static_cast<uint32_t>(take);
+      if (run < remaining && remaining <= run + sum) {  // the threshold bin is one of this thread's
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (run < remaining && remaining <= run + c[e]) {
+            sts_u32(bsel, static_cast<uint32_t>(kHistBins - 1 - 8 * tid - e));
+            sts_u32(bsel + 4u, remaining - run);
+            sts_u32(bsel + 8u, c[e]);
+          }
+          run += c[e];
+        }
+      }
+      Sync::sync();  // 4: the bin
+      bstar = static_cast<int>(lds_u32(bsel));
+      const uint32_t rem = lds_u32(bsel + 4u), inside = lds_u32(bsel + 8u);
+      if (rem >= inside) {
+        by_bin = true;
+      } else {  // only some of the bin's keys: rank them
+        if (inside > static_cast<uint32_t>(kHistCand)) return false;  // uniform
+        uint32_t bal[M], tot = 0u;
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+          const int b = i0 + 32 * j;
+          bal[j] = __ballot_sync(0xFFFFFFFFu, b >= 1 && b < last && bn[j] == bstar);
+          tot += static_cast<uint32_t>(__popc(bal[j]));
+        }
+        // slots: one atomic per warp (the order of the gathered keys does not matter)
+        uint32_t base = 0u;
+        if (lane == 0 && tot > 0u)
+          asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(base) : "r"(bsel + 12u), "r"(tot) : "memory");
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+          if ((bal[j] >> lane) & 1u) sts_u32(cand + 4u * (base + static_cast<uint32_t>(__popc(bal[j] & lt))), key[j]);
+          base += static_cast<uint32_t>(__popc(bal[j]));
+        }
+        Sync::sync();  // 5: gathered
+        if (tid < static_cast<int>(inside)) {
+          const uint32_t kt = lds_u32(cand + 4u * tid);
+          uint32_t above = 0u, same = 0u;
+          for (uint32_t j0 = 0; j0 < inside; j0 += 4) {
+            const uint4 x = lds_u32x4(cand + 4u * j0);
+            const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const bool ok = j0 + q < inside;  // entries past the count are stale
+              above += (ok && xv[q] > kt) ? 1u : 0u;
+              same += (ok && xv[q] == kt) ? 1u : 0u;
+            }
+          }
+          if (above < rem && rem <= above + same) {  // every such thread writes the same pair
+            sts_u32(fin_thr, kt);
+            sts_u32(fin_need, rem - above);
+          }
+        }
+        Sync::sync();  // 6: threshold key
+        thr = lds_u32(fin_thr);
+        need_eq = lds_u32(fin_need);
+      }
+    }
+  }
+  // ---- output: ballots of the sure and the tied keys per row; warp counts; positions
+  uint32_t sb[M], tb[M], dw = 0u, ew = 0u;
+#pragma unroll
+  for (int j = 0; j < M; ++j) {
+    const int b = i0 + 32 * j;
+    bool sure = false, tie = false;
+    if (b < n) {
+      if (b == 0 || b == last) {
+        sure = true;
+      } else if (take > 0) {
+        if (!by_key) {
+          sure = true;
+        } else if (by_bin) {
+          sure = bn[j] >= bstar;
+        } else {
+          sure = key[j] > thr;
+          tie = key[j] == thr;
+        }
+      }
+    }
+    sb[j] = __ballot_sync(0xFFFFFFFFu, sure);
+    tb[j] = __ballot_sync(0xFFFFFFFFu, tie);
+    dw += static_cast<uint32_t>(__popc(sb[j]));
+    ew += static_cast<uint32_t>(__popc(tb[j]));
+  }
+  if (lane == 0) sts_u32(weq + 4u * warp, (dw << 16) | ew);
+  Sync::sync();  // warp counts
+  uint32_t dcum = 0u, ecum = 0u, dall = 0u, eall = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    const uint32_t x = lds_u32(weq + 4u * w);
+    dcum += w < warp ? x >> 16 : 0u;
+    ecum += w < warp ? x & 0xFFFFu : 0u;
+    dall += x >> 16;
+    eall += x & 0xFFFFu;
+  }
+  const uint32_t total = dall + min(eall, need_eq);
+#pragma unroll
+  for (int j = 0; j < M; ++j) {
+    // selected before this index: the sure ones, and the ties while the budget for them lasts
+    const uint32_t d_at = dcum + static_cast<uint32_t>(__popc(sb[j] & lt));
+    const uint32_t e_at = ecum + static_cast<uint32_t>(__popc(tb[j] & lt));
+    const bool sel = ((sb[j] >> lane) & 1u) || (((tb[j] >> lane) & 1u) && e_at < need_eq);
+    const uint32_t at = d_at + min(e_at, need_eq);
+    if (sel && at < static_cast<uint32_t>(kmax)) idx_out[at] = i0 + 32 * j;
+    dcum += static_cast<uint32_t>(__popc(sb[j]));
+    ecum += static_cast<uint32_t>(__popc(tb[j]));
+  }
+  for (int i = static_cast<int>(total) + tid; i < kmax; i += kSelThreads) idx_out[i] = -1;
+  if (tid == 0) *cnt_out = static_cast<int32_t>(total);
+  return true;
+}
+
 // scores at shared address sc
 // Either threshold search gives the same selection; the digit passes are faster up to about a
 // thousand candidates or for budgets of a sixteenth of them or more, the value histogram for
@@ -604,6 +835,19 @@ template <typename Sync = SyncCta>
 __device__ __forceinline__ void block_topk_fast(uint32_t sc, int n, int budget, int kmax, int32_t* __restrict__ idx_out,
                                                 int32_t* __restrict__ cnt_out, uint32_t S) {
   auto score = [&](int b) { return lds_f32(sc + 4u * static_cast<uint32_t>(b)); };
+  if (n <= 16 * kSelThreads) {
+    bool done;
+    if (n <= 2 * kSelThreads)
+      done = block_topk_reg<2, Sync>(score, n, budget, kmax, idx_out, cnt_out, S);
+    else if (n <= 4 * kSelThreads)
+      done = block_topk_reg<4, Sync>(score, n, budget, kmax, idx_out, cnt_out, S);
+    else if (n <= 8 * kSelThreads)
+      done = block_topk_reg<8, Sync>(score, n, budget, kmax, idx_out, cnt_out, S);
+    else
+      done = block_topk_reg<16, Sync>(score, n, budget, kmax, idx_out, cnt_out, S);
+    if (done) return;
+    Sync::sync();  // every thread has left the register selection
+  }
   if (n <= kHistMinN || 16LL * budget >= n)
     block_topk_impl<Sync>(score, n, budget, kmax, idx_out, cnt_out, S);
   else

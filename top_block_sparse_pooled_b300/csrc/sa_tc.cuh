@@ -8,6 +8,15 @@
 #include "sa_ptx.cuh"
 
 namespace sa {
+// Persistent kernels deal their work units, heaviest first, to the CTAs in alternating
+// directions: CTA c takes units c, 2G-1-c, 2G+c, 4G-1-c, ... (G CTAs).  With unit sizes
+// that fall with the unit index this evens out the per-CTA totals, where a plain round
+// robin gives CTA 0 the largest unit of every round.
+__device__ __forceinline__ int snake_unit(int r) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
 namespace tc {
 
 // ---------------------------------------------------------------- TMEM
