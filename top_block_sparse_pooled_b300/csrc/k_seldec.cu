@@ -83,8 +83,10 @@ struct SdLayout {
   // partial rows pushed here by every CTA of the cluster: slot (sender, row) of D floats, then
   // the row's (max, sum) and two pad words
   __host__ __device__ int recv_off() const { return misc_off() + 16; }
-  __host__ __device__ int bar_off() const { return recv_off() + kSdRecvRows * (D + 4) * 4; }
-  __host__ __device__ int bytes() const { return bar_off() + (2 * nstages + 2) * 8 + 1024; }
+  // with selection: the local block's cached rows, staged for the fused append's sketch row
+  __host__ __device__ int astage_off() const { return recv_off() + kSdRecvRows * (D + 4) * 4; }
+  __host__ __device__ int bar_off() const { return astage_off() + (sel ? kSdBk * D * 2 : 0); }
+  __host__ __device__ int bytes() const { return bar_off() + (2 * nstages + 3) * 8 + 1024; }
 };
 
 struct SdParams {
@@ -138,14 +140,18 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
   return v;
 }
 
-// The cache append of one group, by the 256 consumer threads of the group's CTA rank 0: the T
-// new rows of K and V into the caches, then the local block's sketch row (mean of its rows
-// 64*lb .. L-1, the rows before pos read from the cache and the new ones from k_new; the same
+// The cache append of one group, by the 256 consumer threads of the appending CTA: the T new
+// rows of K and V into the caches, then the local block's sketch row (mean of its rows
+// 64*lb .. L-1; the rows before pos come from `stage`, where the producer copied them from the
+// cache at the start of the group (abar completes that copy), the new ones from k_new; the same
 // thread mapping and summation order as the append kernel's block_mean_rows).  red: 128 * 8
 // floats of shared scratch.
 template <int D>
-__device__ __forceinline__ void append_rows(const SdParams& p, int g, int b, int kvh, float* red) {
+__device__ __forceinline__ bool append_rows(const SdParams& p, int g, int b, int kvh, float* red,
+                                            const uint8_t* stage, uint32_t abar, uint32_t parity) {
   const int tid = threadIdx.x;
+  bool ok = mbar_wait(abar, parity);
+  if (!ok) mbar_wait_drain(abar, parity);  // the copy has landed before the buffer is reused
   constexpr int CPR = D / 8;               // 16-byte chunks per row
   for (int i = tid; i < p.T * CPR; i += kSdConsumers * 32) {
     const int t = i / CPR, c = i % CPR;
@@ -164,10 +170,10 @@ __device__ __forceinline__ void append_rows(const SdParams& p, int g, int b, int
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     for (int r = r0; r < nrows; r += RSTEP) {
       const int j = j0 + r;
-      const __nv_bfloat16* src = j < p.pos
-                                     ? p.kc + (static_cast<size_t>(g) * p.Ls + j) * D + c * 8
-                                     : p.k_new + ((static_cast<size_t>(b) * p.T + (j - p.pos)) * p.Hkv + kvh) * D + c * 8;
-      const uint4 x = *reinterpret_cast<const uint4*>(src);
+      const uint4 x = j < p.pos
+                          ? *reinterpret_cast<const uint4*>(stage + (static_cast<size_t>(r) * D + c * 8) * 2)
+                          : *reinterpret_cast<const uint4*>(
+                                p.k_new + ((static_cast<size_t>(b) * p.T + (j - p.pos)) * p.Hkv + kvh) * D + c * 8);
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -185,7 +191,9 @@ __device__ __forceinline__ void append_rows(const SdParams& p, int g, int b, int
     for (int rr = 0; rr < RSTEP; ++rr) sum += red[rr * D + col];
     p.sketch[(static_cast<size_t>(g) * p.nb_cap + lb) * D + col] = sum * inv;
   }
-  bar_named(1, kSdConsumers * 32);  // red is free again
+  fence_proxy_async_smem();          // the stage's reads before a later copy into it
+  bar_named(1, kSdConsumers * 32);  // red and the stage are free again
+  return ok;
 }
 
 // grid (CS, clusters), cluster (CS, 1, 1), kSdThreads threads, one CTA per SM.
@@ -215,6 +223,8 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
   const uint32_t empty0 = full0 + 8 * NS;
   const uint32_t qbar = empty0 + 8 * NS;
   const uint32_t recvbar = qbar + 8;  // CS arrivals per group: every CTA has pushed its rows
+  const uint32_t abar = recvbar + 8;  // the fused append's staged rows
+  const uint8_t* astage = smem + lay.astage_off();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -232,6 +242,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
     }
     mbar_init(qbar, 1);
     mbar_init(recvbar, CS);
+    mbar_init(abar, 1);
     fence_mbar_init();
   }
   pdl_wait();  // q, the sketch, the caches and idx / cnt may come from the previous kernel
@@ -252,10 +263,19 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
     const int r0s = static_cast<int>(rank) * p.per;                 // this CTA's sketch rows
     const int r1s = kSel ? min(p.nb, r0s + p.per) : 0;
     const int nch = r1s > r0s ? (r1s - r0s + kSdBk - 1) / kSdBk : 0;  // sketch chunks
+    // the CTA that appends this group's new rows (while rank 0 selects)
+    const bool appender = kSel && p.k_new && static_cast<int>(rank) == (CS > 1 ? 1 : 0);
     // ------------------------------------------------------------- phase S
     if (kSel) {
       if (warp == kSdConsumers) {
         if (lane == 0) {
+          if (appender) {  // the local block's cached rows, for its new sketch row, land during scoring
+            const int j0 = (p.pos / kSdBk) * kSdBk;
+            const uint32_t nbytes = static_cast<uint32_t>((p.pos - j0) * D * 2);
+            mbar_arrive_expect_tx(abar, nbytes);
+            if (nbytes > 0)
+              bulk_g2s(smem_u32(astage), p.kc + (static_cast<size_t>(g) * p.Ls + j0) * D, nbytes, abar);
+          }
           mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(p.R * D * 2));
           for (int t = 0; t < p.T; ++t)
             bulk_g2s(q_sh + t * p.G * D * 2, p.q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + kvh * p.G) * D,
@@ -362,8 +382,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
       // the fused cache append: no score the top-k reads depends on it, and the attention takes
       // the new rows from the inputs, so it runs here, off the critical path, in rank 1 (rank 0
       // after its top-k when the cluster has one CTA)
-      if (p.k_new && warp < kSdConsumers && static_cast<int>(rank) == (CS > 1 ? 1 : 0))
-        append_rows<D>(p, g, b, kvh, red);
+      if (appender && warp < kSdConsumers && !append_rows<D>(p, g, b, kvh, red, astage, abar, giter & 1)) ok = false;
       cluster_sync();  // the selection is in rank 0's shared memory
     }
     // --------------------------------------------------- this CTA's block list
