@@ -444,25 +444,24 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
         gbs, cores, sample = cpu_oracle_decode(wl, x, cpu_seconds)
         res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                "sample": sample}
-    traffic = os.path.join(ROOT, "profiles", "decode_%s_traffic.txt" % wl.name)
-    if os.path.exists(traffic) and bf and wl.G * wl.T <= 16:
-        try:
-            t = {}
-            for line in open(traffic):
-                if ":" in line and not line.startswith("#"):
-                    key, val = line.split(":", 1)
-                    t[key.strip()] = val.strip()
-            if t.get("kernel_source_hash") == _kernel_hash():
-                res["roofline"]["traffic"] = int(t["dram_bytes_per_launch"])
-        except Exception:
-            pass
+        if wl.name == "c1":  # the small parity config also on one core
+            import oracle
+            oracle.set_threads(1)
+            try:
+                gbs1, cores1, sample1 = cpu_oracle_decode(wl, x, min(cpu_seconds, 5.0))
+            finally:
+                oracle.set_threads(cores)
+            res["cpu_baseline_1core"] = {"value": round(gbs1, 4), "unit": "GB/s", "cores": cores1, "kind": "oracle",
+                                         "sample": sample1}
+    if bf and wl.G * wl.T <= 16:
+        res["roofline"]["traffic"] = _stored_traffic("decode_%s_traffic.txt" % wl.name, DECODE_SOURCES)
     return res
 
 
 def _leg_summary(r):
     """A secondary decode workload's result, without the keys that only the headline line carries."""
     keep = ("value", "unit", "ms_per_step", "steps", "dtype", "config", "pct_hbm_peak", "roofline", "decode_roofline",
-            "e2e", "kernels_us", "gpu_launches", "clocks", "cpu_baseline")
+            "e2e", "kernels_us", "gpu_launches", "clocks", "cpu_baseline", "cpu_baseline_1core")
     out = {k: r[k] for k in keep if k in r}
     out["metric"] = r["metric"]
     return out
@@ -544,9 +543,10 @@ def cpu_oracle_prefill(wl, x, budget_s, executed_flop):
             "kind": "oracle", "sample": sample, "extrapolated": True, "step_s": round(step_s, 3)}
 
 
-def bench_prefill(wl, steps, peaks, peak_src, cpu_seconds=0.0):
+def bench_prefill(wl, steps, peaks, peak_src, cpu_seconds=0.0, full_size=True):
     """One prefill step = (sketch build + sketch select | oracle mass + mass select) + sparse prefill,
-    on the full workload.  Returns a dict with per-kernel times and tensor-core rooflines."""
+    on the full workload.  Returns a dict with per-kernel times and tensor-core rooflines (stored DRAM
+    traffic per launch only at the full, unmodified workload)."""
     import numpy as np
     import torch
 
@@ -602,9 +602,14 @@ def bench_prefill(wl, steps, peaks, peak_src, cpu_seconds=0.0):
         raise RuntimeError("device status word set during prefill warm-up")
     t_step = _events_ms(lambda: [step() for _ in range(steps)], 1, stream) / steps
     reps = max(3, steps)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
     t_score = _events_ms(score, reps, stream)
+    score_clocks = sampler.stop()
     t_select = _events_ms(select, reps, stream)
+    sampler.start()
     t_attend = _events_ms(attend, reps, stream)
+    attend_clocks = sampler.stop()
     pairs = int(cnt.sum().item())  # (group, tile, block) triples executed
     tile_flops = 4 * wl.d * wl.Qt * wl.Bk  # QK^T + PV of one 128 x 128 tile, one head
     executed = pairs * wl.G * tile_flops
@@ -626,8 +631,11 @@ def bench_prefill(wl, steps, peaks, peak_src, cpu_seconds=0.0):
         "tflops_dense_equivalent": round(dense / (t_attend * 1e-3) / 1e12, 1),
         "roofline": {"kernel": "sa_prefill (prefill_kernel, tcgen05)", "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks["bf16_tflops"], "peak_source": peak_src + " bf16 burst", "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
-                     "avg_launch_ms": round(t_attend, 4), "algorithmic_flop_per_launch": executed},
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": _stored_traffic("prefill_%s_traffic.txt" % wl.name, PREFILL_SOURCES)
+                     if full_size else None,
+                     "avg_launch_ms": round(t_attend, 4), "algorithmic_flop_per_launch": executed,
+                     "clocks": attend_clocks},
         "l2": "inputs %.2f GB resident, larger than L2" % ((q.numel() + k.numel() + v.numel()) * 2 / 1e9),
     }
     if wl.mode == "mass":
@@ -636,7 +644,9 @@ def bench_prefill(wl, steps, peaks, peak_src, cpu_seconds=0.0):
                                 "achieved": round(mass_flops / (t_score * 1e-3) / 1e12, 2),
                                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                 "frac": round(mass_flops / (t_score * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                                "algorithmic_flop_per_launch": mass_flops}
+                                "traffic": _stored_traffic("mass_%s_traffic.txt" % wl.name, MASS_SOURCES)
+                                if full_size else None,
+                                "algorithmic_flop_per_launch": mass_flops, "clocks": score_clocks}
     del q, k, v, out
     torch.cuda.empty_cache()
     if cpu_seconds > 0:
@@ -842,14 +852,40 @@ def bench_prefill_tokens(reps, peaks, peak_src):
     }
 
 
-def _kernel_hash():
-    """Hash of the sources of the step's dominant kernel (stored DRAM traffic is used while it matches)."""
+# Sources of each measured kernel: a stored DRAM-traffic figure is reported only while their hash
+# still matches the one recorded beside it (null once the kernel has changed).
+DECODE_SOURCES = ("k_seldec.cu", "k_select.cu", "k_decode_mma.cu", "sa_ptx.cuh")
+PREFILL_SOURCES = ("k_prefill.cu", "sa_tc.cuh", "sa_f32x2.cuh", "sa_ptx.cuh")
+MASS_SOURCES = ("k_mass.cu", "sa_tc.cuh", "sa_f32x2.cuh", "sa_ptx.cuh")
+
+
+def _kernel_hash(sources=DECODE_SOURCES):
+    """Hash of a kernel's sources (stored DRAM traffic is used while it matches)."""
     import hashlib
     h = hashlib.sha256()
-    for fn in ("k_seldec.cu", "k_select.cu", "k_decode_mma.cu", "sa_ptx.cuh"):
+    for fn in sources:
         with open(os.path.join(ROOT, "top_block_sparse_pooled_b300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def _stored_traffic(name, sources):
+    """DRAM bytes per launch from profiles/<name> (an ncu capture summary), or None when the file is
+    missing or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    t = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            key, val = line.split(":", 1)
+            t[key.strip()] = val.strip()
+    if t.get("kernel_source_hash") != _kernel_hash(sources):
+        return None
+    try:
+        return int(t["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def bench_reference(args, wl, rank, world):
@@ -958,7 +994,8 @@ def main():
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
             peaks, src = load_peaks()
-            res = {"prefill": [bench_prefill(pf_wl(n), max(1, args.prefill_steps), peaks, src) for n in ("c5", "c4")]}
+            res = {"prefill": [bench_prefill(pf_wl(n), max(1, args.prefill_steps), peaks, src,
+                                             full_size=not (args.prefill_B or args.prefill_L)) for n in ("c5", "c4")]}
         else:
             res = bench_decode(args, wl, rank, world)
             if args.decode_legs and res is not None:
@@ -974,7 +1011,9 @@ def main():
             if args.prefill_steps > 0 and res is not None:
                 peaks, src = load_peaks()
                 cs = min(args.cpu_seconds, 10.0) if (args.cpu_baseline and rank == 0) else 0.0
-                res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src, cs) for n in ("c5", "c4")]
+                res["prefill"] = [bench_prefill(pf_wl(n), args.prefill_steps, peaks, src, cs,
+                                                 full_size=not (args.prefill_B or args.prefill_L))
+                                   for n in ("c5", "c4")]
                 res["gpu_launches"] += 4 * args.prefill_steps * 2
             if args.tokens_reps > 0 and res is not None:
                 peaks, src = load_peaks()

@@ -265,6 +265,32 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
     const int nch = r1s > r0s ? (r1s - r0s + kSdBk - 1) / kSdBk : 0;  // sketch chunks
     // the CTA that appends this group's new rows (while rank 0 selects)
     const bool appender = kSel && p.k_new && static_cast<int>(rank) == (CS > 1 ? 1 : 0);
+    // With selection, the forced blocks are known before it: block 0 is list position 0 (rank 0)
+    // and the local block nb - 1 is the last position, cnt - 1, where the top-k returns
+    // cnt = forced + min(k, nb - 2) entries.  Their K / V loads are issued right after the
+    // sketch chunks, so they land while the top-k runs; each owner attends over them first.
+    int ne = 0;                   // forced blocks loaded early: 0, 1 or 2
+    int early0 = -1, early1 = -1;  // ... in list order
+    if (kSel) {
+      const int cnt_sel = (p.nb >= 2 ? 2 : 1) + (p.k <= 0 ? 0 : min(p.k, max(p.nb - 2, 0)));
+      const bool sink = rank == 0;
+      const bool local = p.nb >= 2 && static_cast<int>(rank) == (cnt_sel - 1) % CS;
+      early0 = sink ? 0 : (local ? p.nb - 1 : -1);
+      early1 = (sink && local) ? p.nb - 1 : -1;
+      ne = (sink ? 1 : 0) + (local ? 1 : 0);
+    }
+    // K and V tiles of block blk into ring stage st (producer lane)
+    auto issue_kv = [&](uint32_t st, int blk) {
+      const uint32_t full = full0 + 8 * st;
+      mbar_arrive_expect_tx(full, kStageBytes);
+      const uint32_t kt = sbase + st * kStageBytes;
+      const int row = g * p.Ls + blk * kSdBk;
+#pragma unroll
+      for (int bx = 0; bx < C::ROWB / 128; ++bx) {
+        tma_g2s_2d(kt + bx * kSdBk * 128, &kmap, bx * 64, row, full);
+        tma_g2s_2d(kt + C::TILEB + bx * kSdBk * 128, &vmap, bx * 64, row, full);
+      }
+    };
     // ------------------------------------------------------------- phase S
     if (kSel) {
       if (warp == kSdConsumers) {
@@ -290,6 +316,11 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
             for (int bx = 0; bx < kBoxes; ++bx)
               tma_g2s_2d(sbase + st * kStageBytes + bx * kSdBk * 128, &skmap, bx * 32, g * p.nb_cap + r0s + c * kSdBk,
                          full);
+          }
+          for (int e = 0; e < ne && ok; ++e) {  // the forced blocks, sequence numbers after the chunks
+            const uint32_t v = vi + nch + e, st = v % NS;
+            if (v >= static_cast<uint32_t>(NS)) ok = mbar_wait(empty0 + 8 * st, ((v / NS) - 1) & 1);
+            if (ok) issue_kv(st, e == 0 ? early0 : early1);
           }
         }
         __syncwarp();
@@ -395,11 +426,16 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
       }
       n = max(0, min(n, p.kmax));
       const int mine = n > static_cast<int>(rank) ? (n - static_cast<int>(rank) + CS - 1) / CS : 0;
+      // the forced blocks loaded early lead the list (the sink is position 0 already; the local
+      // block, this CTA's last position, moves up behind it)
+      const bool local_early = ne > (rank == 0 ? 1 : 0);
       for (int i = tid; i < mine; i += kSdConsumers * 32) {
         const int j = static_cast<int>(rank) + i * CS;
         int blk = kSel ? ld_cluster_s32(sel0 + 4u * j) : p.idx[static_cast<size_t>(g) * p.kmax + j];
         if (blk < 0 || blk * kSdBk >= p.L) blk = -1;
-        list[i] = blk;
+        int at = i;
+        if (local_early) at = (i == mine - 1) ? (rank == 0 ? 1 : 0) : ((rank == 0 && i == 0) ? 0 : i + 1);
+        list[at] = blk;
       }
       if (tid == 0) misc[0] = mine;
     }
@@ -408,22 +444,14 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
     // ------------------------------------------------------------- phase A
     if (warp == kSdConsumers) {
       if (lane == 0) {
-        uint32_t v = vi;
-        for (int i = 0; i < nlist; ++i) {
+        uint32_t v = vi + ne;  // the forced blocks (list[0, ne)) were issued during the selection
+        for (int i = ne; i < nlist; ++i) {
           const int blk = list[i];
           if (blk < 0) continue;
           const uint32_t st = v % NS;
           if (v >= static_cast<uint32_t>(NS) && ok) ok = mbar_wait(empty0 + 8 * st, ((v / NS) - 1) & 1);
           if (!ok) break;
-          const uint32_t full = full0 + 8 * st;
-          mbar_arrive_expect_tx(full, kStageBytes);
-          const uint32_t kt = sbase + st * kStageBytes;
-          const int row = g * p.Ls + blk * kSdBk;
-#pragma unroll
-          for (int bx = 0; bx < C::ROWB / 128; ++bx) {
-            tma_g2s_2d(kt + bx * kSdBk * 128, &kmap, bx * 64, row, full);
-            tma_g2s_2d(kt + C::TILEB + bx * kSdBk * 128, &vmap, bx * 64, row, full);
-          }
+          issue_kv(st, blk);
           ++v;
         }
         // every copy issued has landed before the ring is reused or the CTA exits
