@@ -836,7 +836,18 @@ def bench_prefill_tokens(reps, peaks, peak_src):
     mass_bytes = 2 * B * Hq * (L * (L + 1) // 2) * 4 + B * L * L * 4 + B * Hkv * L * d * 2
     ach = mass_bytes / (us["token_mass_prefill"] * 1e-6) / 1e9
     sel = int(cnt.sum().item())
-    gathered = sel * Hkv * d * 2 * 2
+    # the tensor-core path attends each 128-query tile over the 128-key blocks that hold any of its
+    # queries' tokens (each query over its own tokens only): its executed tiles, from the lists
+    ih, ch = idx.reshape(B, L, kmax).cpu().numpy(), cnt.reshape(B, L).cpu().numpy()
+    tiles = 0
+    for b in range(B):
+        for i0 in range(0, L, 128):
+            blocks = set()
+            for t in range(i0, min(i0 + 128, L)):
+                row = ih[b, t, :ch[b, t]]
+                blocks.update((row[(row >= 0) & (row <= t)] // 128).tolist())
+            tiles += len(blocks)
+    executed = tiles * Hq * 4 * d * 128 * 128  # QK^T + PV per (tile, block, head)
     return {
         "workload": "per-query (b_sel = 1) head-collapsed prefill: B=%d L=%d Hq=%d Hkv=%d d=%d, top-%d tokens per "
                     "query + token 0 + the query's own (bf16)" % (B, L, Hq, Hkv, d, wl.k),
@@ -846,8 +857,12 @@ def bench_prefill_tokens(reps, peaks, peak_src):
                                 "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
                                 "bytes": mass_bytes,
                                 "bytes_note": "causal base-2 logits written and read back, mass written, K read"},
-        "prefill_tokens": {"tokens_gathered_per_kv_head": sel, "bytes_gathered": gathered,
-                           "GB_s": round(gathered / (us["prefill_tokens"] * 1e-6) / 1e9, 1)},
+        "prefill_tokens": {"kernel": "prefill_kernel<true> (tcgen05): 128-query tiles over the 128-key blocks "
+                                     "holding their queries' tokens, per-query token masks",
+                           "tokens_selected": sel, "executed_tiles": tiles, "executed_tflop": round(executed / 1e12, 4),
+                           "tflops_executed": round(executed / (us["prefill_tokens"] * 1e-6) / 1e12, 1),
+                           "frac_of_bf16_peak": round(executed / (us["prefill_tokens"] * 1e-6) / 1e12
+                                                      / peaks["bf16_tflops"], 4)},
         "l2": "flushed before every timed call (256 MB write, untimed)",
     }
 

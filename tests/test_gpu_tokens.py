@@ -179,6 +179,8 @@ PREFILL_CASES = {
     "d64_g1_b2": synth.WORKLOADS["c5"].replace(B=2, Hq=4, Hkv=4, d=64, L=257, k=32, needles=2, seed=102),
     # G = 16 (one M tile per query), budget past most rows' candidates
     "g16": synth.WORKLOADS["c5"].replace(B=1, Hq=32, Hkv=2, L=200, k=150, needles=2, seed=103),
+    # two batch rows, several 128-query tiles and a ragged last one (the tensor-core path: d = 128)
+    "g4_b2_tiles": synth.WORKLOADS["c5"].replace(B=2, Hq=8, Hkv=2, L=128 * 3 + 40, k=40, needles=3, seed=105),
 }
 
 
@@ -271,3 +273,32 @@ def test_prefill_tokens_pipeline_1k(sa):
     out = _prefill_tokens(sa, wl, x, idx, cnt)
     ref, _ = oracle.token_attend_prefill(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, g_idx, g_cnt, _prefill_rows(wl))
     assert_close(host(out).reshape(-1, wl.d), ref, what="per-query prefill (1k)")
+
+
+def test_prefill_tokens_ignores_invalid_entries(sa):
+    """Lists with entries that are not tokens of the query's support (negative, future, past L) and
+    counts below the list length: only the valid entries j <= t before the count are attended."""
+    wl = synth.WORKLOADS["c5"].replace(B=1, Hq=8, Hkv=2, L=300, k=24, needles=2, seed=106)
+    x = synth.make_inputs(wl)
+    rng = np.random.default_rng(7)
+    kmax = 32
+    idx = np.full((wl.B, wl.L, kmax), -1, dtype=np.int32)
+    cnt = np.zeros((wl.B, wl.L), dtype=np.int32)
+    clean = np.full_like(idx, -1)
+    ccnt = np.zeros_like(cnt)
+    for b in range(wl.B):
+        for t in range(wl.L):
+            own = rng.choice(t + 1, size=min(t + 1, 20), replace=False)
+            bad = np.array([-1, -5, t + 1 + rng.integers(0, 50), wl.L + 3], dtype=np.int64)
+            row = np.concatenate([own, bad])
+            rng.shuffle(row)
+            n = min(len(row), kmax - 2)
+            idx[b, t, :n] = row[:n]
+            idx[b, t, n:n + 2] = [0, t]  # past the count: must be ignored
+            cnt[b, t] = n
+            keep = np.sort([j for j in row[:n] if 0 <= j <= t])
+            clean[b, t, :len(keep)] = keep
+            ccnt[b, t] = len(keep)
+    out = _prefill_tokens(sa, wl, x, torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda())
+    ref, _ = oracle.token_attend_prefill(x.q, x.k, x.v, wl.Hkv, wl.L, wl.scale, clean, ccnt, _prefill_rows(wl))
+    assert_close(host(out).reshape(-1, wl.d), ref, what="per-query prefill, invalid entries")

@@ -66,9 +66,14 @@ struct PfSmem {
 };
 
 struct PfParams {
-  const int32_t* idx;  // [groups, nq, kmax]
-  const int32_t* cnt;  // [groups, nq]
+  const int32_t* idx;  // [groups, nq, kmax] ([B, nq, kmax] in token mode)
+  const int32_t* cnt;  // [groups, nq]       ([B, nq])
   int kmax;
+  // Optional per-query token mask [B, L, wpr] (wpr = 4 * nb words; bit j of row (b, t): key j is
+  // in query t's support): keys whose bit is clear get no weight.  The per-query token prefill
+  // runs here with, per tile, the blocks that hold any of its queries' tokens.
+  const uint32_t* tokmask;
+  int wpr;
   int L, Hq, Hkv, G, groups, nq, nb, npairs, units;
   float qscale;  // softmax scale * log2(e)
   __nv_bfloat16* out;
@@ -80,7 +85,9 @@ struct PfUnit {
   const int32_t* ids;
 };
 
-// Unit u -> (tile, group, head pair), tiles in descending order.
+// Unit u -> (tile, group, head pair), tiles in descending order.  kTok: the block lists are per
+// batch row (shared by its kv heads).
+template <bool kTok>
 __device__ __forceinline__ PfUnit pf_unit(const PfParams& p, int u) {
   PfUnit w;
   const int per_i = p.groups * p.npairs;
@@ -92,7 +99,7 @@ __device__ __forceinline__ PfUnit pf_unit(const PfParams& p, int u) {
   w.b = w.g / p.Hkv;
   w.kvh = w.g % p.Hkv;
   w.h0 = w.kvh * p.G + 2 * pair;
-  const size_t sel = static_cast<size_t>(w.g) * p.nq + w.i;
+  const size_t sel = static_cast<size_t>(kTok ? w.b : w.g) * p.nq + w.i;
   w.n = min(p.cnt[sel], p.kmax);
   w.ids = p.idx + sel * p.kmax;
   return w;
@@ -100,6 +107,9 @@ __device__ __forceinline__ PfUnit pf_unit(const PfParams& p, int u) {
 
 __device__ __forceinline__ bool pf_valid(int blk, int nb) { return blk >= 0 && blk < nb; }
 
+// kTok: the per-query token mode (p.tokmask set), a separate instantiation so that the
+// block mode keeps its registers.
+template <bool kTok>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                                                                  const __grid_constant__ CUtensorMap kmap,
                                                                  const __grid_constant__ CUtensorMap vmap,
@@ -152,7 +162,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       int nu = 0;       // units processed
       bool ok = true;
       for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd), ++nu) {
-        const PfUnit w = pf_unit(p, u);
+        const PfUnit w = pf_unit<kTok>(p, u);
         if (nu > 0 && ok) ok = mbar_wait(bar(PfSmem::Q_EMPTY), (nu - 1) & 1);
         mbar_arrive_expect_tx(bar(PfSmem::Q_FULL), w.nt * kPfTile);
         for (int t = 0; t < w.nt; ++t)
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       bool pv_pending[2] = {false, false};
       bool ok = true;
       for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd), ++nu) {
-        const PfUnit w = pf_unit(p, u);
+        const PfUnit w = pf_unit<kTok>(p, u);
         if (ok) ok = mbar_wait(bar(PfSmem::Q_FULL), nu & 1);
         tc::fence_after_sync();
         int last_valid = w.n - 1;  // Q is released right after the S MMAs of the unit's last block
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     uint32_t s_waits = 0, o_waits = 0;
     bool ok = true;
     for (int rnd = 0, u = snake_unit(0); u < p.units; u = snake_unit(++rnd)) {
-      const PfUnit w = pf_unit(p, u);
+      const PfUnit w = pf_unit<kTok>(p, u);
       if (t >= w.nt) continue;
       const int qpos = w.i * kPfRows + r;  // query position of this row
       float m_run = -INFINITY, l_run = 0.f;
@@ -283,6 +293,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         const int kbase = blk * kPfKeys;
         const bool full = kbase + kPfKeys - 1 <= qpos && kbase + kPfKeys <= p.L;
         const int lim = full ? kPfKeys - 1 : min(qpos, p.L - 1) - kbase;  // last visible key column
+        uint4 tm = make_uint4(0u, 0u, 0u, 0u);  // token mask words of this row and block
+        if (kTok && qpos < p.L)
+          tm = __ldg(reinterpret_cast<const uint4*>(p.tokmask + (static_cast<size_t>(w.b) * p.L + qpos) * p.wpr) + blk);
         float sr[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_addr + 32 * c, sr + 32 * c);
@@ -290,6 +303,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         if (!full) {
 #pragma unroll
           for (int e = 0; e < 128; ++e) sr[e] = (e <= lim) ? sr[e] : -INFINITY;
+        }
+        if (kTok) {
+          const uint32_t tw[4] = {tm.x, tm.y, tm.z, tm.w};
+#pragma unroll
+          for (int e = 0; e < 128; ++e) sr[e] = ((tw[e >> 5] >> (e & 31)) & 1u) ? sr[e] : -INFINITY;
         }
         float mx;
         {
@@ -397,6 +415,57 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   if (warp == 1) {
     __syncwarp();
     tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Per-query token supports to the prefill kernel's form.  grid (nq, B), 256 threads; dynamic
+// shared memory 8 * wpr + ceil(nb / 32) words.  For query tile i of batch row b: each query t's
+// token list idx[b, t, 0:cnt[b, t]] becomes its mask row tokmask[b, t, :] (distinct tokens
+// 0 <= j <= t; others ignored), and the tile's block list blist[b, i, :] (bcnt[b, i] entries,
+// ascending) holds every 128-key block with a token of one of its queries.
+__global__ void __launch_bounds__(256) tokprefill_prep_kernel(const int32_t* __restrict__ idx,
+                                                              const int32_t* __restrict__ cnt, int kmax, int L, int nq,
+                                                              int nb, int wpr, uint32_t* __restrict__ tokmask,
+                                                              int32_t* __restrict__ blist, int32_t* __restrict__ bcnt) {
+  extern __shared__ uint32_t tp_sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x, b = blockIdx.y;
+  uint32_t* rowbm = tp_sm + warp * wpr;  // one query row per warp at a time
+  uint32_t* tilebm = tp_sm + 8 * wpr;    // blocks touched by the tile
+  for (int x = threadIdx.x; x < (nb + 31) / 32; x += 256) tilebm[x] = 0u;
+  __syncthreads();
+  for (int rl = warp; rl < kPfRows; rl += 8) {
+    const int t = i * kPfRows + rl;
+    if (t >= L) break;  // uniform in the warp
+    for (int x = lane; x < wpr; x += 32) rowbm[x] = 0u;
+    __syncwarp();
+    const int n = min(cnt[static_cast<size_t>(b) * L + t], kmax);
+    const int32_t* row = idx + (static_cast<size_t>(b) * L + t) * kmax;
+    for (int e = lane; e < n; e += 32) {
+      const int tok = row[e];
+      if (tok >= 0 && tok <= t) atomicOr(rowbm + (tok >> 5), 1u << (tok & 31));
+    }
+    __syncwarp();
+    uint32_t* dst = tokmask + (static_cast<size_t>(b) * L + t) * wpr;
+    for (int x = lane; x < wpr; x += 32) {
+      const uint32_t wv = rowbm[x];
+      dst[x] = wv;
+      if (wv) atomicOr(tilebm + ((x >> 2) >> 5), 1u << ((x >> 2) & 31));  // 4 words per block
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int base = 0;
+    int32_t* out = blist + (static_cast<size_t>(b) * nq + i) * nb;
+    for (int j0 = 0; j0 < nb; j0 += 32) {
+      const int j = j0 + lane;
+      const bool in = j < nb && ((tilebm[j >> 5] >> (j & 31)) & 1u);
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, in);
+      if (in) out[base + __popc(bal & ((1u << lane) - 1u))] = j;
+      base += __popc(bal);
+    }
+    if (lane == 0) bcnt[static_cast<size_t>(b) * nq + i] = base;
   }
 }
 

@@ -918,7 +918,7 @@ sa_status_t validate_select(const SelectArgs& a) {
 // ---------------------------------------------------------- prefill / mass
 sa_status_t prefill_impl(const void* q, const void* k, const void* v, const int32_t* idx, const int32_t* cnt,
                          int kmax, int B, int L, int Hq, int Hkv, float scale, void* out, float* lse,
-                         cudaStream_t st) {
+                         cudaStream_t st, const uint32_t* tokmask = nullptr, int wpr = 0) {
   DevInfo di;
   SA_TRY(dev_info(&di));
   constexpr int D = 128;
@@ -926,6 +926,8 @@ sa_status_t prefill_impl(const void* q, const void* k, const void* v, const int3
   p.idx = idx;
   p.cnt = cnt;
   p.kmax = kmax;
+  p.tokmask = tokmask;
+  p.wpr = wpr;
   p.L = L;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -948,9 +950,14 @@ sa_status_t prefill_impl(const void* q, const void* k, const void* v, const int3
                      CU_TENSOR_MAP_SWIZZLE_128B));
   SA_TRY(make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, D, rows, D * 2, 64, sa::kPfKeys,
                      CU_TENSOR_MAP_SWIZZLE_128B));
-  SA_TRY(set_smem(sa::prefill_kernel, sa::PfSmem::kBytes));
   const int grid = static_cast<int>(std::min<long long>(units, di.sms));
-  sa::prefill_kernel<<<grid, sa::kPfThreads, sa::PfSmem::kBytes, st>>>(qm, km, vm, p);
+  if (tokmask) {
+    SA_TRY(set_smem(sa::prefill_kernel<true>, sa::PfSmem::kBytes));
+    sa::prefill_kernel<true><<<grid, sa::kPfThreads, sa::PfSmem::kBytes, st>>>(qm, km, vm, p);
+  } else {
+    SA_TRY(set_smem(sa::prefill_kernel<false>, sa::PfSmem::kBytes));
+    sa::prefill_kernel<false><<<grid, sa::kPfThreads, sa::PfSmem::kBytes, st>>>(qm, km, vm, p);
+  }
   SA_CUDA(cudaGetLastError());
   return SA_OK;
 }
@@ -1346,9 +1353,44 @@ sa_status_t sa_token_mass_prefill(const void* q, const void* k, int dtype, int B
                   : launch_token_mass<64>(q, k, B, L, Hq, Hkv, L, L, scale, mass, workspace, di, st, true);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The per-query token prefill runs on the tensor-core prefill kernel when its shape allows
+// (bf16, d = 128, L <= kTokPfMaxL): every query's support becomes a bit mask row, and each
+// 128-query tile attends over the 128-key blocks holding any of its queries' tokens, each query
+// over its own tokens only.  Other shapes take the token-gather decode kernel.
+constexpr int kTokPfMaxL = 16384;
+
+bool tokpf_fits(int dtype, int d, int L) { return dtype == SA_BF16 && d == 128 && L <= kTokPfMaxL; }
+
+struct TokPfWs {
+  size_t mask, list, count, total;
+  int nq, nb, wpr;
+};
+TokPfWs tokpf_ws(int B, int L) {
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  TokPfWs w;
+  w.nq = cdiv(L, sa::kPfRows);
+  w.nb = cdiv(L, sa::kPfKeys);
+  w.wpr = 4 * w.nb;
+  w.mask = 0;
+  w.list = up(static_cast<size_t>(B) * L * w.wpr * 4);
+  w.count = w.list + up(static_cast<size_t>(B) * w.nq * w.nb * 4);
+  w.total = w.count + up(static_cast<size_t>(B) * w.nq * 4);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t sa_prefill_tokens_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int kmax) {
   if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || kmax < 1) return 0;
-  return tok_ws_bytes(static_cast<long long>(B) * L * Hkv, Hq / Hkv, d, kmax);
+  const size_t gather = tok_ws_bytes(static_cast<long long>(B) * L * Hkv, Hq / Hkv, d, kmax);
+  const size_t tc = L <= kTokPfMaxL ? tokpf_ws(B, L).total : 0;
+  return std::max(gather, tc);
 }
 
 sa_status_t sa_prefill_tokens(const void* q, const void* k, const void* v, int dtype, const int32_t* idx,
@@ -1359,6 +1401,22 @@ sa_status_t sa_prefill_tokens(const void* q, const void* k, const void* v, int d
   // each (batch row, query) pair is one selection row with a single query at position t
   DecodeArgs a{q, k, v, dtype, idx, cnt, kmax, B * L, 1, Hq, Hkv, d, L, L, 1, scale, out, workspace, ws_bytes, 1, L};
   SA_TRY(validate_decode(a));
+  if (tokpf_fits(dtype, d, L)) {
+    const TokPfWs w = tokpf_ws(B, L);
+    SA_ARG(ws_bytes >= w.total, "workspace too small: %zu < %zu bytes", ws_bytes, w.total);
+    SA_ARG(aligned16(workspace) && aligned16(out), "workspace and out must be 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    char* ws = static_cast<char*>(workspace);
+    uint32_t* mask = reinterpret_cast<uint32_t*>(ws + w.mask);
+    int32_t* blist = reinterpret_cast<int32_t*>(ws + w.list);
+    int32_t* bcnt = reinterpret_cast<int32_t*>(ws + w.count);
+    const int smem = (8 * w.wpr + (w.nb + 31) / 32) * 4;
+    SA_TRY(set_smem(sa::tokprefill_prep_kernel, smem));
+    sa::tokprefill_prep_kernel<<<dim3(w.nq, B), 256, smem, st>>>(idx, cnt, kmax, L, w.nq, w.nb, w.wpr, mask, blist,
+                                                                 bcnt);
+    SA_CUDA(cudaGetLastError());
+    return prefill_impl(q, k, v, blist, bcnt, w.nb, B, L, Hq, Hkv, scale, out, nullptr, st, mask, w.wpr);
+  }
   return run_decode(a, as_stream(stream));
 }
 
