@@ -366,7 +366,11 @@ sa_status_t sa_token_mass_prefill(const void* q, const void* k, int dtype, int B
  * q, out: [B, L, Hq, d]; k, v: [B, Hkv, L, d].  workspace: >=
  * sa_prefill_tokens_workspace_bytes(...) bytes, zero-filled before first use,
  * as for sa_decode.  Requires dtype SA_BF16, d in {64, 128}, G <= 16,
- * B*L*Hkv <= 2^24, 16-byte-aligned q, k, v.
+ * B*L*Hkv <= 2^24, 16-byte-aligned q, k, v, out and workspace.
+ * With d == 128 and L <= 16384 the lists become per-query bit masks in the
+ * workspace and every 128-query tile is attended on the tensor cores over the
+ * 128-key blocks that hold any of its queries' tokens, each query over its own
+ * tokens only; otherwise each query's token rows are gathered.
  */
 size_t sa_prefill_tokens_workspace_bytes(int B, int L, int Hq, int Hkv, int d, int kmax);
 sa_status_t sa_prefill_tokens(const void* q, const void* k, const void* v, int dtype, const int32_t* idx,
