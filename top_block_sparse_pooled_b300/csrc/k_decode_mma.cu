@@ -46,7 +46,9 @@
 namespace sa {
 
 constexpr int kDmConsumers = 4;
-constexpr int kDmThreads = (kDmConsumers + 1) * 32;
+constexpr int kDmThreads = (kDmConsumers + 1) * 32;  // block mode: one producer warp
+constexpr int kDmTokProducers = 4;                   // token mode: four gathering warps
+constexpr int kDmThreadsTok = (kDmConsumers + kDmTokProducers) * 32;
 constexpr int kDmBk = 64;
 constexpr int kDmMaxList = 1024;
 constexpr int kDmMaxParts = 64;  // partials per group (CTAs touching one group)
@@ -149,7 +151,7 @@ __device__ __forceinline__ int dm_lds_s32(uint32_t a) {
 }
 
 template <int D, bool kTok>
-__global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kTok ? kDmThreadsTok : kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap vmap,
                                                                    const DmParams p) {
   using C = DmCfg<D>;
@@ -176,7 +178,8 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(full0 + 8 * s, kTok ? 33 : 1);  // token mode: 32 copy arrivals + the producer's own
+      // token mode: per gathering warp 32 copy arrivals + its own
+      mbar_init(full0 + 8 * s, kTok ? kDmTokProducers * 33 : 1);
       mbar_init(empty0 + 8 * s, kDmConsumers);
     }
     fence_mbar_init();
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
   // unit list: (group, block id -- token mode: chunk -- or -1 when the unit is
   // past the count); the count and the id are loaded together (the id slot is
   // always in bounds)
-  for (int i = tid; i < nu; i += kDmThreads) {
+  for (int i = tid; i < nu; i += (kTok ? kDmThreadsTok : kDmThreads)) {
     const int u = u0 + i;
     const int g = u / p.upg, s = u % p.upg;
     if constexpr (kTok) {
@@ -200,8 +203,9 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
   }
   __syncthreads();
 
-  if (kTok && warp == kDmConsumers) {
-    // ------------------------------------------------ producer, token gather (whole warp)
+  if (kTok && warp >= kDmConsumers) {
+    // ---------------------------------- producers, token gather: warp pw takes rows 16pw .. 16pw+15
+    const int pw = warp - kDmConsumers;
     int vi = 0;
     bool ok = true;
     for (int i = 0; i < nu && ok; ++i) {
@@ -224,26 +228,24 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
       const size_t kvg = p.qpb ? static_cast<size_t>(b / p.qpb) * p.Hkv + e.x % p.Hkv : static_cast<size_t>(e.x);
       const __nv_bfloat16* kg = p.kc + kvg * p.Ls * D;
       const __nv_bfloat16* vg = p.vc + kvg * p.Ls * D;
-      int tk[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = lane + 32 * h, s = e.y * kDmBk + row;
+      int tk = 0;
+      if (lane < 16) {
+        const int row = 16 * pw + lane, s = e.y * kDmBk + row;
         const int t = s < n ? sel[s] : -1;
         const bool valid = t >= 0 && t < p.L;
         dm_sts_s32(pos + 4 * row, valid ? t : 0x7FFFFFFF);
-        tk[h] = valid ? t : 0;  // filler rows repeat token 0 (finite values, never visible)
+        tk = valid ? t : 0;  // filler rows repeat token 0 (finite values, never visible)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(full);  // releases the key positions written above
-      // 16-byte pieces: D/8 per row, K rows 0..63 then V rows; lane-strided
+      // 16-byte pieces: D/8 per row, this warp's 16 K rows then its 16 V rows; lane-strided
       constexpr int kPpr = D / 8;
 #pragma unroll 4
-      for (int pc = lane; pc < 2 * kDmBk * kPpr; pc += 32) {
-        const int row = pc / kPpr, col = pc % kPpr, r64 = row & (kDmBk - 1);
-        const int t0 = __shfl_sync(0xFFFFFFFFu, tk[0], r64 & 31), t1 = __shfl_sync(0xFFFFFFFFu, tk[1], r64 & 31);
-        const int t = (r64 >> 5) ? t1 : t0;  // row r64's token is held by lane r64 % 32, in its half r64 / 32
-        const __nv_bfloat16* src = (row < kDmBk ? kg : vg) + static_cast<size_t>(t) * D + col * 8;
-        dm_cp_async16((row < kDmBk ? kt : vt) + r64 * lay.rowb() + col * 16, src);
+      for (int pc = lane; pc < 32 * kPpr; pc += 32) {
+        const int rr = pc / kPpr, col = pc % kPpr, r16 = rr & 15;
+        const int t = __shfl_sync(0xFFFFFFFFu, tk, r16);  // row r16's token is held by lane r16
+        const __nv_bfloat16* src = (rr < 16 ? kg : vg) + static_cast<size_t>(t) * D + col * 8;
+        dm_cp_async16((rr < 16 ? kt : vt) + (16 * pw + r16) * lay.rowb() + col * 16, src);
       }
       dm_cp_async_arrive(full);
       ++vi;
@@ -346,24 +348,35 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
     const size_t slot = static_cast<size_t>(c) + g;
-    for (int i = tid; i < p.R * D; i += kDmConsumers * 32) {
-      const int r = i / D, dd = i % D;
+    if (tid < p.R) {  // row tid: the four warps' weights (into mw), the partial's max and sum
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDmConsumers; ++w) M = fmaxf(M, mw[w * p.R + r]);
+      for (int w = 0; w < kDmConsumers; ++w) M = fmaxf(M, mw[w * p.R + tid]);
       const float mu = (M == -INFINITY) ? 0.f : M;
-      float num = 0.f, den = 0.f;
+      float den = 0.f;
 #pragma unroll
       for (int w = 0; w < kDmConsumers; ++w) {
-        const float wt = exp2f(mw[w * p.R + r] - mu);
-        num = fmaf(ow[(w * p.R + r) * D + dd], wt, num);
-        den = fmaf(lw[w * p.R + r], wt, den);
+        const float wt = exp2f(mw[w * p.R + tid] - mu);
+        den = fmaf(lw[w * p.R + tid], wt, den);
+        mw[w * p.R + tid] = wt;
       }
-      p.part_o[(slot * p.R + r) * D + dd] = num;
-      if (dd == 0) {
-        p.part_ml[(slot * p.R + r) * 2] = M;
-        p.part_ml[(slot * p.R + r) * 2 + 1] = den;
+      p.part_ml[(slot * p.R + tid) * 2] = M;
+      p.part_ml[(slot * p.R + tid) * 2 + 1] = den;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
+    for (int i = tid; i < p.R * D / 4; i += kDmConsumers * 32) {
+      const int r = i / (D / 4), d4 = i % (D / 4);
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kDmConsumers; ++w) {
+        const float wt = mw[w * p.R + r];
+        const float4 x = reinterpret_cast<const float4*>(ow + (w * p.R + r) * D)[d4];
+        num.x = fmaf(x.x, wt, num.x);
+        num.y = fmaf(x.y, wt, num.y);
+        num.z = fmaf(x.z, wt, num.z);
+        num.w = fmaf(x.w, wt, num.w);
       }
+      reinterpret_cast<float4*>(p.part_o + (slot * p.R + r) * D)[d4] = num;
     }
     // The CTA that completes group g merges its partials (no waiting: the
     // others just leave).  Writers: stores, fence, count.  Last: count, fence,
@@ -417,7 +430,7 @@ __global__ void __launch_bounds__(kDmThreads, SA_DM_CTAS_PER_SM) decode_mma_kern
           acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           rr[j] = (j0 + j * kDmConsumers * 32) * 4 / D;
         }
-#pragma unroll 2
+#pragma unroll 4
         for (int k = 0; k < np; ++k) {
           const size_t sl0 = (static_cast<size_t>(cf + k) + g) * p.R;
           float4 v[4];

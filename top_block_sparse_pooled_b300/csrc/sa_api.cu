@@ -592,7 +592,7 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
                      CU_TENSOR_MAP_SWIZZLE_128B));
   SA_TRY(make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.vc, D, rows, D * 2, 64, sa::kDmBk,
                      CU_TENSOR_MAP_SWIZZLE_128B));
-  return launch_pdl(kern, dim3(nctas), dim3(sa::kDmThreads), smem, st, km, vm, p);
+  return launch_pdl(kern, dim3(nctas), dim3(kTok ? sa::kDmThreadsTok : sa::kDmThreads), smem, st, km, vm, p);
 }
 
 // --------------------------------------------------- cluster decode (seldec)
