@@ -468,13 +468,16 @@ def _leg_summary(r):
 
 
 def _events_ms(fn, reps, stream):
-    """Median over reps of the CUDA-event time of fn() on `stream` (one launch sequence each)."""
+    """Median over reps of the CUDA-event time of fn() on `stream` (one launch sequence each).  A
+    sleep kernel queued first keeps the device busy while the host enqueues fn(), so the events
+    time the device work, not the host's launch overhead."""
     import torch
     ts = []
     with torch.cuda.stream(stream):
         fn()
         for _ in range(reps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(2_000_000)
             e0.record(stream)
             fn()
             e1.record(stream)

@@ -30,6 +30,12 @@
 #ifndef SA_DM_MAXSTAGES
 #define SA_DM_MAXSTAGES 4
 #endif
+// Token mode: at least this many 64-token units per CTA, so that the last CTA of a group has
+// fewer partials to merge (measured on the 2050-token decode: 1 -> 22.5 us, 3 -> 18.5 us, 4 and
+// 6 slower again).
+#ifndef SA_DM_TOK_MIN_PER
+#define SA_DM_TOK_MIN_PER 3
+#endif
 
 #include "k_decode.cu"
 #include "k_decode_mma.cu"
@@ -549,6 +555,7 @@ sa_status_t launch_decode_mma(const DecodeArgs& a, const DevInfo& di, cudaStream
   const long long target = static_cast<long long>(SA_DM_WAVES) * SA_DM_CTAS_PER_SM * di.sms;
   long long per = (U + target - 1) / target;
   per = std::max<long long>(per, (upg + sa::kDmMaxParts - 2) / (sa::kDmMaxParts - 1));  // <= 64 partials per group
+  if (kTok) per = std::max<long long>(per, SA_DM_TOK_MIN_PER);
   per = std::min<long long>(std::max<long long>(per, 1), sa::kDmMaxList);
   const int nctas = static_cast<int>((U + per - 1) / per);
   sa::DmLayout lay{2, R, D, static_cast<int>(per), kTok ? 1 : 0};
