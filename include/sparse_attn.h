@@ -388,6 +388,16 @@ sa_status_t sa_prefill_tokens(const void* q, const void* k, const void* v, int d
 sa_status_t sa_selftest_wait_timeout(long long limit_ns, void* stream);
 
 /*
+ * Self-test of sa_decode_noalloc's recovery: fills the first `bytes` bytes of
+ * the library's decode scratch on the current device (where its arrival
+ * counters live) with a non-zero byte pattern, as a call that gave up
+ * mid-way could leave them.  The next sa_decode_noalloc must still be exact
+ * (it clears the counters on its stream before each launch).  bytes in
+ * [1, 8 MiB]; SA_ERR_INVALID_ARG otherwise.  No counterpart in the pages.
+ */
+sa_status_t sa_selftest_poison_noalloc(int bytes, void* stream);
+
+/*
  * One decode step: a1 append (k_new, v_new at cache rows L-T..L-1, sketch
  * refreshed), a2+a3 sketch selection with budget k, a4 decode.  If
  * host_io != 0, q, k_new, v_new and out are HOST pointers: q is copied to

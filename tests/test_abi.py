@@ -207,6 +207,9 @@ def test_invalid_arguments_rejected_on_host(sa):
     # the bounded-wait self-test rejects a limit outside [1 ms, 1 s] before any launch
     assert L.sa_selftest_wait_timeout(5, None) == sa.SA_ERR_INVALID_ARG
     assert L.sa_selftest_wait_timeout(5_000_000_000, None) == sa.SA_ERR_INVALID_ARG
+    # the scratch poisoning self-test takes 1 .. 8 MiB
+    assert L.sa_selftest_poison_noalloc(0, None) == sa.SA_ERR_INVALID_ARG
+    assert L.sa_selftest_poison_noalloc(9 << 20, None) == sa.SA_ERR_INVALID_ARG
     # device status needs an output pointer
     assert L.sa_device_status(None, 0) == sa.SA_ERR_INVALID_ARG
 

@@ -71,3 +71,24 @@ def test_noalloc_rejects_oversized_problem(sa):
     with pytest.raises(sa.SparseAttnError) as e:
         sa.sa_decode_noalloc(q, kc, kc, idx, cnt, 64 * 512, 64, 0.088, out)
     assert e.value.status == sa.SA_ERR_INVALID_ARG and "scratch" in str(e.value)
+
+
+@pytest.mark.parametrize("name", ["bf16_gqa", "f32_split"])
+def test_noalloc_recovers_from_left_over_counters(sa, name):
+    """Arrival counters left non-zero in the scratch (as by a call that gave up) do not change the
+    next call's result: it clears them on its stream before the launch."""
+    wl = {"bf16_gqa": synth.WORKLOADS["c2"].replace(B=2, L=4096 + 9, T=1, k=16, seed=603),
+          "f32_split": synth.WORKLOADS["c1"].replace(Hq=8, Hkv=2, d=128, L=2000, k=5, seed=604)}[name]
+    x = synth.make_inputs(wl)
+    q, k, v = dev(x.q), dev(x.k), dev(x.v)
+    idx, cnt, kmax = _selection(sa, wl, x, None)
+    ws = torch.zeros(sa.sa_decode_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, kmax), dtype=torch.uint8,
+                     device="cuda")
+    ref = torch.empty_like(q)
+    sa.sa_decode(q, k, v, idx, cnt, wl.L, wl.Bk, wl.scale, ref, ws)
+    sa.sa_selftest_poison_noalloc(4096)
+    got = torch.full_like(q, float("nan"))
+    sa.sa_decode_noalloc(q, k, v, idx, cnt, wl.L, wl.Bk, wl.scale, got)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status(clear=True) == 0
+    assert_close(host(got), host(ref), what="%s after poisoned counters" % name)

@@ -69,6 +69,7 @@ SIGNATURES = {
     "sa_prefill_tokens_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "sa_prefill_tokens": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "sa_selftest_wait_timeout": ([ctypes.c_longlong, _vp], _i),
+    "sa_selftest_poison_noalloc": ([_i, _vp], _i),
     "sa_decode_step_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "sa_decode_step": ([_vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _i,
                         _vp, _vp, _i, _vp, _sz, _vp], _i),
@@ -274,6 +275,11 @@ def sa_prefill_tokens(q, k, v, idx, cnt, scale, out, workspace, stream=None):
 def sa_selftest_wait_timeout(limit_ns, stream=None):
     """Launch the bounded-wait self-test (a wait that nothing completes, given up after limit_ns)."""
     _check(lib.sa_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def sa_selftest_poison_noalloc(nbytes, stream=None):
+    """Fill the head of sa_decode_noalloc's scratch with a non-zero pattern (recovery test)."""
+    _check(lib.sa_selftest_poison_noalloc(int(nbytes), _stream(stream)))
 
 
 def sa_decode_step_workspace_bytes(B, T, Hq, Hkv, d, dtype, kmax) -> int:

@@ -91,3 +91,15 @@ extern "C" sa_status_t sa_decode_noalloc(const void* q, const void* k_cache, con
   SA_CUDA(cudaMemsetAsync(ws, 0, ctr_bytes, as_stream(stream)));
   return run_decode(a, as_stream(stream));
 }
+
+// Test-only: overwrite the head of the scratch (where the arrival counters live) with a
+// non-zero byte pattern, as a call that gave up mid-way would leave it.
+extern "C" sa_status_t sa_selftest_poison_noalloc(int bytes, void* stream) {
+  t_err.clear();
+  SA_ARG(bytes >= 1 && static_cast<size_t>(bytes) <= kNoAllocScratchBytes, "bytes must be in [1, %zu]",
+         kNoAllocScratchBytes);
+  void* s = nullptr;
+  SA_TRY(noalloc_scratch(&s));
+  SA_CUDA(cudaMemsetAsync(s, 0x5A, static_cast<size_t>(bytes), as_stream(stream)));
+  return SA_OK;
+}
