@@ -148,3 +148,40 @@ def test_select_small_budgets_patterns(sa, n):
             assert g_cnt[g] == o_cnt[g] and np.array_equal(g_idx[g], o_idx[g]), (
                 "n=%d k=%d pattern %d: gpu %s (cnt %d), oracle %s (cnt %d)" % (
                     n, k, g, g_idx[g][:12].tolist(), g_cnt[g], o_idx[g][:12].tolist(), o_cnt[g]))
+
+
+@pytest.mark.parametrize("n", [300, 512, 700, 3000, 4096])
+def test_select_fallback_patterns(sa, n):
+    """Scores for which the register-resident value-histogram search gives up and the general
+    search takes over: infinite scores (no finite key range), a range too wide for a float
+    (values near +-3e38), and a crowded threshold bin (most candidates share one value just
+    below a few larger ones); plus a tiny range of a few ulps.  Bit-exact against the oracle."""
+    rng = np.random.default_rng(2000 + n)
+    base = rng.standard_normal(n)
+    crowded = np.full(n, 0.5)
+    crowded[rng.choice(n, size=8, replace=False)] = 10.0 + rng.random(8)
+    pats = [
+        np.where(rng.random(n) < 0.05, -np.inf, base),               # -inf entries
+        np.where(rng.random(n) < 0.02, np.inf, base),                # +inf entries
+        np.where(rng.random(n) < 0.5, 3.0e38, -3.0e38) * rng.random(n),  # width beyond float range
+        crowded,                                                     # the threshold bin holds most keys
+        1.0 + rng.integers(0, 3, size=n) * 2.0 ** -23,               # three adjacent floats
+    ]
+    s = np.stack(pats).astype(np.float32)
+    groups = s.shape[0]
+    for k in (1, 5, 32, 80, n // 3, n - 3):
+        kmax = sa.sa_select_kmax(n, 1, 0, False, k)
+        scores = torch.from_numpy(np.ascontiguousarray(s.reshape(1, groups, 1, n))).cuda()
+        idx = torch.full((1, groups, 1, kmax), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((1, groups, 1), -7, dtype=torch.int32, device="cuda")
+        sa.sa_select_topk(sa.SA_SELECT_MASS, None, None, scores, groups, n, n, 1, 0, False, k, 0, 1, 1.0,
+                          idx, cnt, d=128, dtype=sa.SA_BF16, B=1, Tq=1, Hq=groups)
+        torch.cuda.synchronize()
+        assert sa.sa_device_status(clear=True) == 0
+        o_idx, o_cnt = oracle.select(s.astype(np.float64), n, n - 1, k, kmax)
+        g_idx = idx.cpu().numpy().reshape(groups, kmax)
+        g_cnt = cnt.cpu().numpy().reshape(groups)
+        for g in range(groups):
+            assert g_cnt[g] == o_cnt[g] and np.array_equal(g_idx[g], o_idx[g]), (
+                "n=%d k=%d pattern %d: gpu %s (cnt %d), oracle %s (cnt %d)" % (
+                    n, k, g, g_idx[g][:12].tolist(), g_cnt[g], o_idx[g][:12].tolist(), o_cnt[g]))

@@ -54,7 +54,9 @@ constexpr int kSdBk = 64;            // keys per block; sketch rows per chunk
 constexpr int kSdRmax = 16;          // query rows per group (G * T)
 constexpr int kSdRecvRows = 32;      // >= CS * ceil(R / CS) for CS <= 16, R <= 16
 
-// Shared-memory layout (runtime, from a 1024-aligned base).  A ring stage holds
+// Shared-memory layout (runtime, from a 1024-aligned base).  The ring depth (nstages) must be
+// even: stage s then always carries sequence numbers of one parity, i.e. of one quad, which
+// waits on its mbarrier phases in order.  A ring stage holds
 // one block's K and V tiles (64 rows of 2*D bytes each, 128-byte swizzle) or one
 // 64-row chunk of the fp32 sketch (4*D bytes per row, 128-byte swizzle): the
 // same number of bytes.

@@ -695,8 +695,13 @@ sa_status_t launch_seldec(const SdArgs& a, cudaStream_t st) {
   int cs = 1, ncl = 1;
   SA_TRY((sd_shape<D, kSel>(groups, nb, a.kmax, &cs, &ncl)));
   const int per = cdiv(cdiv(nb, cs), sa::kSdBk) * sa::kSdBk;  // sketch rows per CTA, whole chunks
+  // The ring depth must be even: each quad then always owns the same stages, so no waiter can
+  // be two phases behind a stage's mbarrier (with an odd depth the two quads alternate on a
+  // stage and a parity wait can pass on the wrong phase).
   sa::SdLayout lay{4, D, nb, a.kmax, kSel ? 1 : 0};
   if (lay.bytes() > 227 * 1024) lay.nstages = 2;
+  static_assert(sa::kSdQuads == 2, "the ring-depth rule below assumes two consumer quads");
+  if (lay.nstages % 2 != 0) return fail(SA_ERR_UNSUPPORTED, "decode ring depth %d is odd", lay.nstages);
   SA_SUP(lay.bytes() <= 227 * 1024, "decode over %d blocks needs %d bytes of shared memory", nb, lay.bytes());
   const int smem = std::max(lay.bytes(), kSdMinSmem);
   SA_TRY(set_smem(kern, smem));
