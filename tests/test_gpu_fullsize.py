@@ -107,7 +107,8 @@ def test_full_size_prefill_step_sampled(sa, name):
         o_idx, o_cnt, o_scores, _ = oracle.prefill_select(x.q, x.k, wl, units, kmax=kmax)
         fin = np.isfinite(o_scores)
         scale = np.abs(np.where(fin, o_scores, 0)).max(axis=1, keepdims=True)
-        assert np.all(np.abs(np.where(fin, g_scores[uid] - o_scores, 0)) <= 2e-6 * scale)
+        diff = np.subtract(g_scores[uid], o_scores, out=np.zeros_like(o_scores), where=fin)  # finite entries only
+        assert np.all(np.abs(diff) <= 2e-6 * scale)
         rel = 1e-5
     assert_selection(g_idx[uid], g_cnt[uid], o_idx, o_cnt, o_scores, rel=rel, what=name)
     # every unit: ascending, unique, forced blocks present, count as the budget rule says

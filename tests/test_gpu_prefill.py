@@ -140,7 +140,8 @@ def test_prefill_select_sketch_matches_oracle(sa, name):
     fin = np.isfinite(o_s)
     assert np.array_equal(fin, np.isfinite(g_s))
     scale = np.abs(np.where(fin, o_s, 0)).max(axis=1, keepdims=True)
-    assert np.all(np.abs(np.where(fin, g_s - o_s, 0)) <= 2e-6 * scale), "tile scores differ beyond fp32 rounding"
+    diff = np.subtract(g_s, o_s, out=np.zeros_like(o_s), where=fin)  # finite entries only
+    assert np.all(np.abs(diff) <= 2e-6 * scale), "tile scores differ beyond fp32 rounding"
     assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s, what=name)
 
 
