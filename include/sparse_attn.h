@@ -400,12 +400,13 @@ sa_status_t sa_selftest_poison_noalloc(int bytes, void* stream);
 /*
  * One decode step: a1 append (k_new, v_new at cache rows L-T..L-1, sketch
  * refreshed), a2+a3 sketch selection with budget k, a4 decode.  If
- * host_io != 0, q, k_new, v_new and out are HOST pointers: q is copied to
- * the device staging area in `workspace`; k_new, v_new and out are read and
- * written in place by the kernels when they are page-locked memory mapped
- * into the device's address space (cudaHostAlloc, or pinned memory under
- * unified addressing), and staged by copies otherwise (pageable memory: the
- * copies are then synchronous).  Otherwise they are device pointers.
+ * host_io != 0, q, k_new, v_new and out are HOST pointers: k_new, v_new and
+ * out are read and written in place by the kernels when they are page-locked
+ * memory mapped into the device's address space (cudaHostAlloc, or pinned
+ * memory under unified addressing), and so is q when the step is one launch
+ * (bf16, block 64, G*T <= 16, the new rows inside the last block, no scores);
+ * otherwise each is staged by a copy through `workspace` (pageable memory:
+ * the copies are then synchronous).  Otherwise they are device pointers.
  * sketch, caches, idx, cnt, scores (optional) are device memory as above.
  * workspace: >= sa_decode_step_workspace_bytes(...) bytes of device memory,
  * zero-filled before first use exactly as for sa_decode (its head is

@@ -259,6 +259,37 @@ def test_decode_step_multi_token(sa, T, L):
     _check_appended_state(wl, x, kc, vc, sk)
 
 
+@pytest.mark.parametrize("T,L", [(4, 8192), (1, 4096 + 37)])
+def test_decode_step_host_io_reads_q_in_place(sa, T, L):
+    """Pinned host I/O in the one-launch step: q (T rows per sequence, G heads each) is read in place
+    from mapped host memory together with the new rows, and out is written in place."""
+    wl = DECODE_CASES["c3"].replace(L=L, T=T, k=12, needles=2, seed=720 + T)
+    x = synth.make_inputs(wl)
+    pos = wl.L - wl.T
+    kc, vc = dev(x.k).clone(), dev(x.v).clone()
+    kc[:, :, pos:] = 0
+    vc[:, :, pos:] = 0
+    sk = _sketch_buf(wl)
+    sa.sa_build_sketch(kc, pos, wl.Bk, sk)
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
+    idx = torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sa.sa_decode_step_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, sa.SA_BF16, kmax),
+                     dtype=torch.uint8, device="cuda")
+    q = dev(x.q).cpu().pin_memory()
+    k_new = dev(x.k)[:, :, pos:].permute(0, 2, 1, 3).contiguous().cpu().pin_memory()
+    v_new = dev(x.v)[:, :, pos:].permute(0, 2, 1, 3).contiguous().cpu().pin_memory()
+    out = torch.full(q.shape, float("nan"), dtype=q.dtype).pin_memory()
+    sa.sa_decode_step(q, k_new, v_new, kc, vc, sk, wl.L, wl.Bk, wl.k, wl.scale, idx, cnt, out, ws, host_io=True)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    o_idx, o_cnt, o_s, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax)
+    assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s, what="host I/O T=%d" % T)
+    ref, _ = oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, pos, wl.Bk, wl.scale, _all_rows(wl), o_idx, o_cnt)
+    assert_close(host(out).reshape(ref.shape), ref, what="host I/O decode step T=%d" % T)
+    _check_appended_state(wl, x, kc, vc, sk)
+
+
 def test_decode_step_graph_replay_reads_new_inputs(sa):
     """On a non-default stream the step is captured once and replayed: a second call with the same
     buffers but new query contents gives the new query's exact result."""

@@ -110,6 +110,9 @@ struct SdParams {
   __nv_bfloat16* vc;
   float* sketch;      // [groups, nb_cap, D] (the rewritten row)
   int pos;
+  // q may be page-locked host memory mapped into the device's address space (the decode step
+  // with host I/O): it is then read with plain loads only, never by a bulk copy
+  int q_host;
   float scale;  // score scale (the softmax scale)
   float qscale;  // softmax scale * log2(e)
   SdLayout lay;
@@ -304,10 +307,12 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
             if (nbytes > 0)
               bulk_g2s(smem_u32(astage), p.kc + (static_cast<size_t>(g) * p.Ls + j0) * D, nbytes, abar);
           }
-          mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(p.R * D * 2));
-          for (int t = 0; t < p.T; ++t)
-            bulk_g2s(q_sh + t * p.G * D * 2, p.q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + kvh * p.G) * D,
-                     p.G * D * 2, qbar);
+          if (!p.q_host) {
+            mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(p.R * D * 2));
+            for (int t = 0; t < p.T; ++t)
+              bulk_g2s(q_sh + t * p.G * D * 2, p.q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + kvh * p.G) * D,
+                       p.G * D * 2, qbar);
+          }
           for (int c = 0; c < nch; ++c) {
             const uint32_t v = vi + c, st = v % NS;
             if (v >= static_cast<uint32_t>(NS) && ok) ok = mbar_wait(empty0 + 8 * st, ((v / NS) - 1) & 1);
@@ -329,7 +334,18 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
       } else {
         const int quad = warp >> 2, wq = warp & 3;
         const int gq = lane >> 2, tq = lane & 3;
-        if (ok) ok = mbar_wait(qbar, giter & 1);
+        if (p.q_host) {  // the group's R query rows (row t * G + head), 16 bytes per thread and load
+          for (int i = tid; i < p.R * (D / 8); i += kSdConsumers * 32) {
+            const int r = i / (D / 8), c = i % (D / 8);
+            const uint4 x = *reinterpret_cast<const uint4*>(
+                p.q + ((static_cast<size_t>(b) * p.T + r / p.G) * p.Hq + kvh * p.G + r % p.G) * D + c * 8);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(q_sh + 2u * (r * D + c * 8)), "r"(x.x),
+                         "r"(x.y), "r"(x.z), "r"(x.w) : "memory");
+          }
+          bar_named(1, kSdConsumers * 32);
+        } else if (ok) {
+          ok = mbar_wait(qbar, giter & 1);
+        }
         uint32_t bq[2][D / 16][2];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -481,13 +497,24 @@ __global__ void __launch_bounds__(kSdThreads, 1) seldec_kernel(const __grid_cons
           q1 = p.q + ((static_cast<size_t>(b) * p.T + r1 / p.G) * p.Hq + kvh * p.G + r1 % p.G) * D;
           lim1 = p.L - p.T + r1 / p.G;
         }
+        if (kSel) {  // the rows staged in phase S (same row order), not a second read of q
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-          const int col = kk * 16 + 2 * tq;
-          qa[kk][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col) : 0u;
-          qa[kk][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col) : 0u;
-          qa[kk][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col + 8) : 0u;
-          qa[kk][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col + 8) : 0u;
+          for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            const int col = kk * 16 + 2 * tq;
+            qa[kk][0] = q0 ? lds_u32(q_sh + 2u * (r0 * D + col)) : 0u;
+            qa[kk][1] = q1 ? lds_u32(q_sh + 2u * (r1 * D + col)) : 0u;
+            qa[kk][2] = q0 ? lds_u32(q_sh + 2u * (r0 * D + col + 8)) : 0u;
+            qa[kk][3] = q1 ? lds_u32(q_sh + 2u * (r1 * D + col + 8)) : 0u;
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            const int col = kk * 16 + 2 * tq;
+            qa[kk][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col) : 0u;
+            qa[kk][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col) : 0u;
+            qa[kk][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col + 8) : 0u;
+            qa[kk][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col + 8) : 0u;
+          }
         }
 #pragma unroll
         for (int j = 0; j < C::NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;

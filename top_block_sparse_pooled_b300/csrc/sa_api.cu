@@ -622,6 +622,7 @@ struct SdArgs {
   const void* v_new = nullptr;
   float* sketch_w = nullptr;
   int pos = 0;
+  bool q_host = false;  // q is mapped host memory: plain loads only (see SdParams::q_host)
 };
 
 constexpr int kSdMinSmem = 120 * 1024;  // keeps the kernel at one CTA per SM
@@ -731,6 +732,7 @@ sa_status_t launch_seldec(const SdArgs& a, cudaStream_t st) {
   p.vc = static_cast<__nv_bfloat16*>(const_cast<void*>(a.vc));
   p.sketch = a.sketch_w;
   p.pos = a.pos;
+  p.q_host = a.q_host ? 1 : 0;
   p.scale = a.scale;
   p.qscale = a.scale * 1.4426950408889634f;
   p.lay = lay;
@@ -1212,7 +1214,8 @@ namespace {
 sa_status_t select_decode_impl(const void* q, int dtype, const float* sketch, const void* k_cache,
                                const void* v_cache, int B, int T, int Hq, int Hkv, int d, int L, int L_stride,
                                int block, int k, float scale, int32_t* idx, int32_t* cnt, int kmax, float* scores,
-                               void* out, const void* k_new, const void* v_new, cudaStream_t st) {
+                               void* out, const void* k_new, const void* v_new, cudaStream_t st,
+                               bool q_host = false) {
   SelectArgs sel{SA_SELECT_SKETCH, q, dtype, sketch, scores, B, T, Hq, Hkv, d, L, L_stride, block, 0, 0, k,
                  0, 1, scale, idx, cnt, kmax};
   SA_TRY(validate_select(sel));
@@ -1235,6 +1238,7 @@ sa_status_t select_decode_impl(const void* q, int dtype, const float* sketch, co
   a.v_new = v_new;
   a.sketch_w = const_cast<float*>(sketch);
   a.pos = L - T;
+  a.q_host = q_host;
   return run_seldec(a, st);
 }
 
@@ -1494,17 +1498,29 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
   const void* vnd = a.v_new;
   void* outd = a.out;
   bool out_mapped = false;
+  const bool fused = seldec_fits(a.dtype, a.block, a.Hq / a.Hkv, a.T);
+  // the append runs inside the fused launch when its rows lie in the local block (kept whatever
+  // its score) and no scores are returned; otherwise it is a launch of its own
+  const bool fused_append = fused && a.L >= a.T && a.T >= 1 && (a.L - a.T) / a.block == (a.L - 1) / a.block &&
+                            a.scores == nullptr;
+  bool q_host = false;
   if (a.host_io) {
-    // q is staged on the device (the selection reads it with bulk copies); k_new, v_new and out
-    // are used in place when they are page-locked host memory mapped into the device's address
-    // space (the append kernel reads them and the decode merge writes out with plain accesses),
-    // and staged by copies otherwise.
+    // q, k_new, v_new and out are used in place when they are page-locked host memory mapped
+    // into the device's address space (the fused launch reads q and the new rows with plain
+    // loads and writes out the same way; the other launches read q with bulk copies, so there it
+    // is staged), and staged by copies otherwise.
     void* q_dev = w + dec;
     void* out_dev = w + dec + up(qb);
     void* kn_dev = w + dec + 2 * up(qb);
     void* vn_dev = w + dec + 2 * up(qb) + up(kb);
-    SA_CUDA(cudaMemcpyAsync(q_dev, a.q, qb, cudaMemcpyHostToDevice, st));
-    qd = q_dev;
+    const void* q_map = fused_append ? mapped_host(a.q) : nullptr;
+    if (q_map) {
+      qd = q_map;
+      q_host = true;
+    } else {
+      SA_CUDA(cudaMemcpyAsync(q_dev, a.q, qb, cudaMemcpyHostToDevice, st));
+      qd = q_dev;
+    }
     const void* kn_map = mapped_host(a.k_new);
     const void* vn_map = mapped_host(a.v_new);
     void* out_map = const_cast<void*>(mapped_host(a.out));
@@ -1524,15 +1540,11 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
     outd = out_mapped ? out_map : out_dev;
   }
   void* sp = static_cast<void*>(st);
-  const bool fused = seldec_fits(a.dtype, a.block, a.Hq / a.Hkv, a.T);
-  // the append runs inside the fused launch when its rows lie in the local block (kept whatever
-  // its score) and no scores are returned; otherwise it is a launch of its own
-  const bool fused_append = fused && a.L >= a.T && a.T >= 1 && (a.L - a.T) / a.block == (a.L - 1) / a.block &&
-                            a.scores == nullptr;
   if (fused_append) {
     SA_ARG(a.k_cache && a.v_cache && a.sketch, "null pointer argument");
     SA_TRY(select_decode_impl(qd, a.dtype, a.sketch, a.k_cache, a.v_cache, a.B, a.T, a.Hq, a.Hkv, a.d, a.L,
-                              a.L_stride, a.block, a.k, a.scale, a.idx, a.cnt, a.kmax, a.scores, outd, knd, vnd, st));
+                              a.L_stride, a.block, a.k, a.scale, a.idx, a.cnt, a.kmax, a.scores, outd, knd, vnd, st,
+                              q_host));
   } else if (fused) {
     SA_TRY(sa_append_kv(knd, vnd, a.dtype, a.B, a.Hkv, a.T, a.d, a.k_cache, a.v_cache, a.L_stride, a.L - a.T,
                         a.block, a.sketch, sp));
