@@ -259,11 +259,12 @@ def test_decode_step_multi_token(sa, T, L):
     _check_appended_state(wl, x, kc, vc, sk)
 
 
-@pytest.mark.parametrize("T,L", [(4, 8192), (1, 4096 + 37)])
-def test_decode_step_host_io_reads_q_in_place(sa, T, L):
-    """Pinned host I/O in the one-launch step: q (T rows per sequence, G heads each) is read in place
-    from mapped host memory together with the new rows, and out is written in place."""
-    wl = DECODE_CASES["c3"].replace(L=L, T=T, k=12, needles=2, seed=720 + T)
+@pytest.mark.parametrize("base,B,T,L", [("c3", 1, 4, 8192), ("c3", 1, 1, 4096 + 37), ("c2", 8, 2, 4096 + 37)])
+def test_decode_step_host_io_multi_token(sa, base, B, T, L):
+    """Pinned host I/O in the one-launch step with T query rows per sequence: the new rows are read
+    and out is written in place in mapped host memory; q is read in place too when each group's
+    cluster has at most two CTAs (many groups), else staged by one copy (few groups)."""
+    wl = DECODE_CASES[base].replace(B=B, L=L, T=T, k=12, needles=2, seed=720 + T)
     x = synth.make_inputs(wl)
     pos = wl.L - wl.T
     kc, vc = dev(x.k).clone(), dev(x.v).clone()

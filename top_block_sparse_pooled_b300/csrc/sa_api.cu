@@ -1513,7 +1513,16 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
     void* out_dev = w + dec + up(qb);
     void* kn_dev = w + dec + 2 * up(qb);
     void* vn_dev = w + dec + 2 * up(qb) + up(kb);
-    const void* q_map = fused_append ? mapped_host(a.q) : nullptr;
+    // Every CTA of a group's cluster reads the group's q rows, so in place the host link carries
+    // q once per CTA: worth it for clusters of up to two CTAs (c2: 47.6 -> 40.1 us per step end to
+    // end), not for ten (c3: 44.0 -> 44.7 us); larger clusters get q by one copy.
+    int cs = 0, ncl = 0;
+    if (fused_append) {
+      const int nb = cdiv(a.L, a.block);
+      SA_TRY((a.d == 128 ? sd_shape<128, true>(a.B * a.Hkv, nb, a.kmax, &cs, &ncl)
+                         : sd_shape<64, true>(a.B * a.Hkv, nb, a.kmax, &cs, &ncl)));
+    }
+    const void* q_map = (fused_append && cs <= 2) ? mapped_host(a.q) : nullptr;
     if (q_map) {
       qd = q_map;
       q_host = true;
