@@ -13,13 +13,18 @@
 // SM in alternating directions (snake_unit), which evens out the CTAs'
 // totals.
 //
-// Roles (320 threads, kPfThreads):
+// Roles (384 threads, kPfThreads; three warpgroups):
 //   warp 0    TMA producer: the unit's Q tiles (3-D map: d, head, row), then
 //             the K and V tiles of each selected block into 2-stage rings.
 //   warp 1    TMEM allocator and MMA issuer (one thread):
 //               S_t = Q_t K^T  (M=128, N=128 keys, K=d; both K-major in smem)
 //               O_t += P_t V   (A = P_t from TMEM, B = V MN-major in smem)
-//   warps 2-5, 6-9   softmax warpgroup t = 0, 1: thread r owns query row r of
+//   warps 2-3 idle.  Warpgroup 0 (warps 0-3) hands registers to the other two:
+//             launched at 168 per thread (three warps per SM sub-partition), it
+//             drops to 96 and the softmax warpgroups rise to 200 (128 x 96 +
+//             256 x 200 = 63,488 <= 384 x 168), so that a softmax thread holds its
+//             whole S row without spilling.
+//   warps 4-7, 8-11  softmax warpgroup t = 0, 1: thread r owns query row r of
 //             M tile t (= TMEM lane r).  It reads its S row from TMEM, masks
 //             (causal on the diagonal block, keys past L), keeps the running
 //             max m and sum l (base 2), writes P = exp2(S - m) as bf16 pairs
@@ -48,7 +53,11 @@ constexpr int kPfBox = 128 * 128;       // bytes of one 64-column box of 128 row
 #endif
 constexpr int kPfKStages = SA_PF_KSTAGES;  // K ring (K is consumed first, so it runs ahead)
 constexpr int kPfVStages = 2;              // V ring
-constexpr int kPfThreads = 320;  // warp 0 producer, warp 1 MMA, warps 2-9 two softmax warpgroups
+constexpr int kPfThreads = 384;  // warp 0 producer, warp 1 MMA, warps 4-11 two softmax warpgroups
+constexpr int kPfRegsLow = 96;    // registers per thread of warpgroup 0 after the split
+constexpr int kPfRegsHigh = 200;  // ... of the softmax warpgroups
+static_assert(128 * kPfRegsLow + 256 * kPfRegsHigh <= kPfThreads * 168,
+              "the register split must fit the registers the block is launched with (168 per thread)");
 constexpr float kPfRescale = 8.0f;  // log2 growth of the running max that forces an O rescale
 
 struct PfSmem {
@@ -157,6 +166,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<kPfRegsLow>();
     if (lane == 0) {
       uint32_t it = 0;  // K/V ring iteration (valid blocks, across units)
       int nu = 0;       // units processed
@@ -196,6 +206,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
+    setmaxnreg_dec<kPfRegsLow>();
     if (lane == 0) {
       constexpr uint32_t kIdQK = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdPV = tc::idesc_bf16(128, 128, false, true);
@@ -265,9 +276,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       tc::mma_commit(bar(PfSmem::DONE));
       mbar_wait_drain(bar(PfSmem::DONE), 0);
     }
+  } else if (warp < 4) {
+    setmaxnreg_dec<kPfRegsLow>();  // idle: its registers go to the softmax warpgroups
   } else {
     // -------------------------------------------------------------- softmax
-    const int t = (warp - 2) >> 2;           // M tile of this warpgroup
+    setmaxnreg_inc<kPfRegsHigh>();
+    const int t = (warp - 4) >> 2;           // M tile of this warpgroup
     const int r = ((warp & 3) << 5) | lane;  // row within the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_addr = lane_base + t * 128;
