@@ -60,6 +60,20 @@ static_assert(128 * kPfRegsLow + 256 * kPfRegsHigh <= kPfThreads * 168,
               "the register split must fit the registers the block is launched with (168 per thread)");
 constexpr float kPfRescale = 8.0f;  // log2 growth of the running max that forces an O rescale
 
+// Per-warpgroup register budget change (all four warps of the warpgroup execute it).  An
+// increase waits until the registers are free, so the increases and decreases of a block must
+// balance within the registers it was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg: 24..256 in steps of 8");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg: 24..256 in steps of 8");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 struct PfSmem {
   static constexpr int kQ = 0;                         // [2] M tiles
   static constexpr int kK = kQ + 2 * kPfTile;           // [kPfKStages]

@@ -136,20 +136,6 @@ __device__ __forceinline__ void tma_g2s_3d(uint32_t dst, const CUtensorMap* map,
       : "memory");
 }
 
-// Per-warpgroup register budget change (all four warps of the warpgroup execute it).  An
-// increase waits until the registers are free, so the increases and decreases of a block must
-// balance within the registers it was launched with.
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg: 24..256 in steps of 8");
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg: 24..256 in steps of 8");
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
