@@ -968,6 +968,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5,
                     help="steps of each prefill leg (c5 sketch-selected, c4 oracle-mass); 0 skips them")
     ap.add_argument("--prefill-only", action="store_true", help="run only the prefill legs (profiling)")
+    ap.add_argument("--prefill-workload", default="both", choices=["both", "c4", "c5"],
+                    help="with --prefill-only: which prefill leg to run (profiling one workload)")
     ap.add_argument("--sweep-length", action="store_true",
                     help="decode across context lengths with the length-aware budget (separate report)")
     ap.add_argument("--prefill-B", type=int, default=0, help="override the prefill legs' batch (profiling)")
@@ -1012,8 +1014,9 @@ def main():
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
             peaks, src = load_peaks()
+            names = ("c5", "c4") if args.prefill_workload == "both" else (args.prefill_workload,)
             res = {"prefill": [bench_prefill(pf_wl(n), max(1, args.prefill_steps), peaks, src,
-                                             full_size=not (args.prefill_B or args.prefill_L)) for n in ("c5", "c4")]}
+                                             full_size=not (args.prefill_B or args.prefill_L)) for n in names]}
         else:
             res = bench_decode(args, wl, rank, world)
             if args.decode_legs and res is not None:
