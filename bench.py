@@ -278,13 +278,16 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / (calls * reps)
 
-    # the step as CUDA graphs: R consecutive steps over the R input sets
-    g_full = capture([lambda s=s: step(s) for s in sets])
+    # the step as CUDA graphs of GS consecutive steps cycling through the R input sets (at least
+    # 32 steps per graph, so that the boundaries between replays, where one step cannot start
+    # early behind the previous one, are rare)
+    GS = R * max(1, 32 // R)
+    g_full = capture([lambda s=s: step(s) for s in sets * (GS // R)])
     K = steps
-    rem = K % R
-    g_rem = capture([lambda s=s: step(s) for s in sets[:rem]]) if rem else None
+    rem = K % GS
+    g_rem = capture([lambda i=i: step(sets[i % R]) for i in range(rem)]) if rem else None
     with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup // R)):
+        for _ in range(max(1, args.warmup // GS)):
             g_full.replay()
     torch.cuda.synchronize()
 
@@ -298,7 +301,7 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
     with torch.cuda.stream(stream):
         torch.cuda._sleep(20_000_000)  # keep the device busy while the host queues the replays
         ev0.record(stream)
-        for _ in range(K // R):
+        for _ in range(K // GS):
             g_full.replay()
         if g_rem is not None:
             g_rem.replay()
@@ -406,7 +409,7 @@ def bench_decode(args, wl, rank, world, steps=None, rotate=None, cpu_seconds=Non
             "step": ("append+sketch refresh, score+top-k select and sparse decode in one launch" if fused_append else
                      "append+sketch refresh, then score+top-k select and sparse decode in one launch" if fused_ok else
                      "append+sketch refresh, score+top-k select, split-KV sparse decode") + (
-                " (CUDA graphs of %d steps)" % R),
+                " (CUDA graphs of %d steps over %d input sets)" % (GS, R)),
             "bytes_per_step": {"selected_kv": kv_b, "sketch_scan": sk_b, "append": ap_b},
             "l2": "%d resident input sets rotated (%.1f GB of K/V); no step reuses L2 from the previous" % (
                 R, R * x.k.nbytes * 2 / 1e9),
