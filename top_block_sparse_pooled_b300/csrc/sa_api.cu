@@ -1514,8 +1514,9 @@ sa_status_t step_enqueue(const StepArgs& a, cudaStream_t st) {
     void* kn_dev = w + dec + 2 * up(qb);
     void* vn_dev = w + dec + 2 * up(qb) + up(kb);
     // Every CTA of a group's cluster reads the group's q rows, so in place the host link carries
-    // q once per CTA: worth it for clusters of up to two CTAs (c2: 47.6 -> 40.1 us per step end to
-    // end), not for ten (c3: 44.0 -> 44.7 us); larger clusters get q by one copy.
+    // q once per CTA: worth it for clusters of up to two CTAs (batch 8, 8 kv heads, 32K context:
+    // 47.6 -> 40.1 us per step end to end), not for ten (batch 1, 8 kv heads, 256K context: 44.0
+    // -> 44.7 us); larger clusters get q by one copy.
     int cs = 0, ncl = 0;
     if (fused_append) {
       const int nb = cdiv(a.L, a.block);
