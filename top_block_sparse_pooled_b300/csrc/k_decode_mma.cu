@@ -395,27 +395,48 @@ __global__ void __launch_bounds__(kTok ? kDmThreadsTok : kDmThreads, SA_DM_CTAS_
     asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
     if (last) {
       __threadfence();
-      // stage every partial's (max, denominator) per row; np <= kDmMaxParts
-      float* pm = ow;                          // [np][R] maxima, then weights
-      float* pl = ow + kDmMaxParts * p.R;      // [np][R] denominators
-      for (int i = tid; i < np * p.R; i += kDmConsumers * 32) {
-        const int k = i / p.R, r = i % p.R;
-        const size_t sl = (static_cast<size_t>(cf + k) + g) * p.R + r;
-        pm[i] = __ldcg(p.part_ml + sl * 2);
-        pl[i] = __ldcg(p.part_ml + sl * 2 + 1);
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
-      if (tid < p.R) {
+      // every partial's weight per row (into pm [np][R]) and the row's 1 / denominator: eight
+      // lanes per row (row tid / 8; R <= 16), lane j taking partials j, j + 8, ... (np <=
+      // kDmMaxParts = 64), their (max, denominator) pairs read from L2 all at once, the row max
+      // and the denominator combined across the eight lanes
+      static_assert(kDmConsumers * 32 == 8 * 16 && kDmMaxParts <= 64, "eight lanes per row, eight partials each");
+      float* pm = ow;
+      {
+        const int r = tid >> 3, j = tid & 7;
+        float mk[8], lk[8];
         float M = -INFINITY;
-        for (int k = 0; k < np; ++k) M = fmaxf(M, pm[k * p.R + tid]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int k = j + 8 * q;
+          mk[q] = -INFINITY;
+          lk[q] = 0.f;
+          if (r < p.R && k < np) {
+            const float2 ml =
+                __ldcg(reinterpret_cast<const float2*>(p.part_ml) + (static_cast<size_t>(cf + k) + g) * p.R + r);
+            mk[q] = ml.x;
+            lk[q] = ml.y;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) M = fmaxf(M, mk[q]);
+        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 1));
+        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 2));
+        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 4));
         const float mu = (M == -INFINITY) ? 0.f : M;
         float den = 0.f;
-        for (int k = 0; k < np; ++k) {
-          const float w = exp2f(pm[k * p.R + tid] - mu);
-          pm[k * p.R + tid] = w;
-          den = fmaf(pl[k * p.R + tid], w, den);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int k = j + 8 * q;
+          if (r < p.R && k < np) {
+            const float w = exp2f(mk[q] - mu);
+            pm[k * p.R + r] = w;
+            den = fmaf(lk[q], w, den);
+          }
         }
-        lw[tid] = den > 0.f ? 1.f / den : 0.f;
+        den += __shfl_xor_sync(0xFFFFFFFFu, den, 1);
+        den += __shfl_xor_sync(0xFFFFFFFFu, den, 2);
+        den += __shfl_xor_sync(0xFFFFFFFFu, den, 4);
+        if (j == 0 && r < p.R) lw[r] = den > 0.f ? 1.f / den : 0.f;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kDmConsumers * 32) : "memory");
       // out[r, d:d+4] = sum_k w[k, r] * part_o[k, r, d:d+4] / den[r]; up to 4 float4 slots per thread,
