@@ -35,6 +35,9 @@ DECODE_CASES = {
     "f32_d128": synth.WORKLOADS["c1"].replace(d=128, Hq=8, Hkv=2, L=2048 + 5, k=7, seed=78),
     # bf16, d=64, G*T = 32
     "bf16_d64": synth.WORKLOADS["c2"].replace(B=2, Hq=16, Hkv=2, d=64, L=3000, T=4, k=9, seed=79),
+    # many groups (80: more than half the SMs), so the decode is the split-KV launch over all SMs
+    # with the last CTA of each group merging its partials (G*T = 8, ragged tail)
+    "many_groups": synth.WORKLOADS["c2"].replace(B=20, Hq=16, Hkv=4, L=2048 + 13, T=2, k=10, needles=2, seed=80),
 }
 
 
@@ -289,6 +292,40 @@ def test_decode_step_host_io_multi_token(sa, base, B, T, L):
     ref, _ = oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, pos, wl.Bk, wl.scale, _all_rows(wl), o_idx, o_cnt)
     assert_close(host(out).reshape(ref.shape), ref, what="host I/O decode step T=%d" % T)
     _check_appended_state(wl, x, kc, vc, sk)
+
+
+def test_decode_step_many_groups(sa):
+    """The one-launch step with more groups than co-resident clusters: clusters take several
+    groups in turn (append, selection and attention of each), and sa_decode on the same selection
+    takes the split-KV launch over all SMs; both agree with the oracle."""
+    wl = DECODE_CASES["many_groups"].replace(B=40, seed=81)  # 160 groups
+    x = synth.make_inputs(wl)
+    pos = wl.L - wl.T
+    kc, vc = dev(x.k).clone(), dev(x.v).clone()
+    kc[:, :, pos:] = 0
+    vc[:, :, pos:] = 0
+    sk = _sketch_buf(wl)
+    sa.sa_build_sketch(kc, pos, wl.Bk, sk)
+    kmax = sa.sa_select_kmax(wl.L, wl.Bk, 0, False, wl.k)
+    idx = torch.empty((wl.B, wl.Hkv, 1, kmax), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((wl.B, wl.Hkv, 1), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sa.sa_decode_step_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, sa.SA_BF16, kmax),
+                     dtype=torch.uint8, device="cuda")
+    q = dev(x.q)
+    k_new = dev(x.k)[:, :, pos:].permute(0, 2, 1, 3).contiguous()
+    v_new = dev(x.v)[:, :, pos:].permute(0, 2, 1, 3).contiguous()
+    out = torch.empty_like(q)
+    sa.sa_decode_step(q, k_new, v_new, kc, vc, sk, wl.L, wl.Bk, wl.k, wl.scale, idx, cnt, out, ws)
+    torch.cuda.synchronize()
+    _check_status(sa)
+    o_idx, o_cnt, o_s, _ = oracle.decode_select(x.q, x.k, wl, kmax=kmax)
+    assert_selection(idx.cpu().numpy(), cnt.cpu().numpy(), o_idx, o_cnt, o_s, what="many groups")
+    ref, _ = oracle.attend(x.q, x.k, x.v, wl.Hkv, wl.L, pos, wl.Bk, wl.scale, _all_rows(wl), o_idx, o_cnt)
+    assert_close(host(out).reshape(ref.shape), ref, what="many-group decode step")
+    _check_appended_state(wl, x, kc, vc, sk)
+    # the attention alone on the oracle's selection (split-KV launch, last-CTA merge)
+    got = _decode_gpu(sa, wl, x, o_idx, o_cnt, kmax)
+    assert_close(got.reshape(ref.shape), ref, what="many-group decode")
 
 
 def test_decode_step_graph_replay_reads_new_inputs(sa):
